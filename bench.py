@@ -1,0 +1,485 @@
+"""Benchmark of the expert slot cache decode step on one GB300 (or N replicas).
+
+One step = restore the prepared cache state, then ensure_experts -> copy_missing ->
+expert FFN for one synthetic batch, as the cache-copy benchmark of the FreeToken
+benchmark guide (section 4: prepared state where the driven layer misses, CUDA-event
+timing, time_ms of ensure + copy, copy_MiB = misses * bytes per expert,
+bw_GBps = copied bytes / time, tok_ms = time_ms * L). The headline line reports:
+  value      copy GB/s of ensure + copy (bytes copied / summed event time);
+  roofline   the copy kernel against the host-to-device link peak measured in this
+             run (max of a 1 GiB pinned->device cudaMemcpyAsync and an SM zero-copy
+             read of 1 GiB);
+  roofline_ffn  the FFN kernels against the measured HBM copy bandwidth;
+  e2e        the same metric with the step's inputs copied from pinned host memory
+             and the output read back inside the timed region;
+  cpu_baseline  the CPU oracle timed on a bounded sample of the same workload.
+``--impl reference`` times the CPU oracle itself on the same workload (host cores).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_CFG = "c2"
+DEFAULT_BS = 16
+DEFAULT_MR = 1.0
+METRIC = "per-layer expert copy GB/s & tok_ms vs bs/miss_rate; expert FFN us/layer"
+LINK_PROBE_BYTES = 1 << 30
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ftmoe", choices=["ftmoe", "reference"])
+    ap.add_argument("--config", default=DEFAULT_CFG)
+    ap.add_argument("--bs", type=int, default=DEFAULT_BS)
+    ap.add_argument("--miss-rate", type=float, default=DEFAULT_MR)
+    ap.add_argument("--repeat", type=int, default=25, help="repeats per sweep point (median)")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--copy-mode", default="fused", choices=["fused", "per_bank", "engine"])
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------------------ dist
+
+
+def dist_setup(n):
+    import torch
+
+    if n <= 1 or "RANK" not in os.environ:
+        return 0, 1, None
+    import torch.distributed as dist
+
+    rank, world = int(os.environ["RANK"]), int(os.environ["WORLD_SIZE"])
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", rank)))
+    dist.init_process_group("nccl")
+    return rank, world, dist
+
+
+def aggregate(dist, total_bytes: float, seconds: float, device=None):
+    """Whole-job throughput of independent replicas: bytes summed, time = max over ranks."""
+    import torch
+
+    if dist is None:
+        return total_bytes, seconds
+    t = torch.tensor([total_bytes, seconds], dtype=torch.float64, device=device)
+    b = t[:1].clone()
+    s = t[1:].clone()
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    dist.all_reduce(s, op=dist.ReduceOp.MAX)
+    return float(b.item()), float(s.item())
+
+
+# ------------------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while a region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int = 0):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([v.strip() for v in line.split(",")])
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm = [float(r[1]) for r in self.rows if len(r) >= 9 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if len(r) >= 9 and r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in self.rows:
+            if len(r) >= 9:
+                for n, v in zip(names, r[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------ helpers
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs"), "measured (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy burst)"
+    return 6800.0, "fallback 6.8 TB/s"
+
+
+def link_peak(torch, F, stream):
+    """Host-to-device link ceiling in this run: best of 5 for a 1 GiB pinned->device
+    cudaMemcpyAsync and for the SM zero-copy read kernel."""
+    src = torch.empty(LINK_PROBE_BYTES, dtype=torch.uint8, pin_memory=True)
+    src.fill_(7)
+    dst = torch.empty(LINK_PROBE_BYTES, dtype=torch.uint8, device="cuda")
+    out = {}
+    for name in ("memcpy", "sm_read"):
+        best = 1e30
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            if name == "memcpy":
+                with torch.cuda.stream(stream):
+                    dst.copy_(src, non_blocking=True)
+            else:
+                F.ftmoe_h2d_stream_copy(dst.data_ptr(), src.data_ptr(), LINK_PROBE_BYTES, stream.cuda_stream)
+            b.record(stream)
+            b.synchronize()
+            best = min(best, a.elapsed_time(b) / 1e3)
+        out[name] = LINK_PROBE_BYTES / best / 1e9
+    del src, dst
+    return out
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(cfg, r, host_banks_np, threads, ffn_tokens=4, reps=None, budget_s=12.0):
+    """Time the CPU oracle on a bounded sample of one step: ensure + copy of the whole
+    step (the copy into a host-side slot buffer), and the FFN for `ffn_tokens` tokens.
+    Returns dict(copy GB/s, ensure+copy seconds per step, ffn seconds per token)."""
+    import oracle
+
+    schema_bytes = [b.shape[1] for b in host_banks_np]
+    slot_bufs = [np.empty((cfg.S, n), np.uint8) for n in schema_bytes]
+    t_ec = []
+    t0 = time.perf_counter()
+    m = 0
+    while True:
+        orc = oracle.Cache(cfg.E, cfg.L, cfg.S, r.owner, r.stamp, r.clock)
+        a = time.perf_counter()
+        rc, slots, mids, msl = orc.ensure(0, r.topk_ids)
+        oracle.copy_missing(schema_bytes, host_banks_np, slot_bufs, cfg.E, mids, msl)
+        t_ec.append(time.perf_counter() - a)
+        m = mids.size
+        if (reps is not None and len(t_ec) >= reps) or (reps is None and time.perf_counter() - t0 > budget_s / 2):
+            break
+    B = sum(schema_bytes)
+    toks = list(range(min(ffn_tokens, r.topk_ids.shape[0])))
+    pairs = [[hb.ctypes.data + int(e) * hb.shape[1] for hb in host_banks_np] for e in r.topk_ids[toks].reshape(-1)]
+    a = time.perf_counter()
+    oracle.expert_ffn(cfg.fmt, cfg.H, cfg.I, pairs, r.x[toks], r.weights[toks], threads=threads)
+    t_ffn = (time.perf_counter() - a) / max(1, len(toks))
+    ec = statistics.median(t_ec)
+    return {"copy_gbps": m * B / ec / 1e9, "ensure_copy_s": ec, "ffn_s_per_token": t_ffn, "reps": len(t_ec),
+            "misses": m, "ffn_tokens": len(toks)}
+
+
+# ------------------------------------------------------------------------------ reference arm
+
+
+def reference_banks(cfg, wl):
+    """Host banks of layer 0 for the oracle (seeded; drawn on the GPU when there is one,
+    which only generates inputs)."""
+    import torch
+
+    out = []
+    for b, g in enumerate(wl.bank_schema(cfg)):
+        if torch.cuda.is_available():
+            t = torch.empty((cfg.E, g.bytes), dtype=torch.uint8)
+            wl.fill_bank_device(cfg, b, t)
+            out.append(t.numpy())
+        else:
+            a = np.empty((cfg.E, g.bytes), np.uint8)
+            wl.fill_bank(cfg, b, a)
+            out.append(a)
+    return out
+
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    from expert_slot_cache_device_gb300 import workload as wl
+
+    oracle.build()
+    cfg = wl.CONFIGS[args.config]
+    r = wl.make_route(cfg, args.bs, args.miss_rate)
+    banks = reference_banks(cfg, wl)
+    cores = cpu_cores()
+    times = []
+    for i in range(args.warmup + args.steps):
+        res = oracle_sample(cfg, r, banks, cores, ffn_tokens=1, reps=1)
+        if i >= args.warmup:
+            times.append(res)
+    ec = sum(t["ensure_copy_s"] for t in times)
+    B = cfg.bytes_per_expert
+    value = r.misses * B * len(times) / ec / 1e9
+    ffn_s = statistics.median(t["ffn_s_per_token"] for t in times) * args.bs
+    step_s = ec / len(times) + ffn_s
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{cfg.name} bs={args.bs} miss_rate={args.miss_rate}", "bs": args.bs,
+                   "miss_rate": args.miss_rate, "misses": r.misses, "parallelism": "host cores"},
+        "time_ms": ec / len(times) * 1e3, "tok_ms": ec / len(times) * 1e3 * cfg.L,
+        "ffn_us": ffn_s * 1e6,
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"per step: ensure + copy of the full step ({r.misses} experts, "
+                                   f"{r.misses * B / 2**20:.0f} MiB memcpy into a host slot buffer, 1 thread); "
+                                   f"FFN of 1 of {args.bs} tokens on {cores} threads, scaled to {args.bs}"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ------------------------------------------------------------------------------ GPU arm
+
+
+def run_gpu(args):
+    import torch
+
+    rank, world, dist = dist_setup(args.gpus)
+    from expert_slot_cache_device_gb300 import build as B
+
+    if rank == 0:
+        B.build()
+    if dist is not None:
+        dist.barrier()
+    from expert_slot_cache_device_gb300 import ftmoe as F
+    from expert_slot_cache_device_gb300 import workload as wl
+    from expert_slot_cache_device_gb300.cache import ExpertSlotCache
+
+    dev = torch.cuda.current_device()
+    stream = torch.cuda.Stream()
+    cfg = wl.CONFIGS[args.config]
+    bs, mr = args.bs, args.miss_rate
+    r = wl.make_route(cfg, bs, mr)
+    B = cfg.bytes_per_expert
+    cache = ExpertSlotCache(cfg, max(max(cfg.bs_list), bs) * cfg.topk, stream=stream)
+    cache.set_copy_mode({"fused": F.COPY_FUSED, "per_bank": F.COPY_PER_BANK, "engine": F.COPY_ENGINE}[args.copy_mode])
+    s = stream.cuda_stream
+    d_ids = torch.from_numpy(r.topk_ids).cuda()
+    d_slots = torch.empty_like(d_ids)
+    d_w = torch.from_numpy(r.weights).cuda()
+    d_x = torch.from_numpy(r.x.view(np.int16).copy()).view(torch.bfloat16).cuda()
+    d_y = torch.empty((bs, cfg.H), dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()
+
+    def step(ev):
+        cache.set_state(r.owner, r.stamp, r.clock, stream=s)
+        ev[0].record(stream)
+        F.ftmoe_ensure_experts(cache.handle, 0, d_ids.data_ptr(), bs, cfg.topk, d_slots.data_ptr(), s)
+        ev[1].record(stream)
+        F.ftmoe_copy_missing(cache.handle, s)
+        ev[2].record(stream)
+        F.ftmoe_expert_ffn(cache.handle, d_x.data_ptr(), bs, d_slots.data_ptr(), d_w.data_ptr(), cfg.topk,
+                           d_y.data_ptr(), s)
+        ev[3].record(stream)
+
+    mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for _ in range(args.warmup):
+        step(mk())
+    torch.cuda.synchronize()
+    assert cache.status() == F.OK
+    evs = [mk() for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev)
+    clocks.start()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    total_s = start.elapsed_time(end) / 1e3
+    ens = [e[0].elapsed_time(e[1]) / 1e3 for e in evs]
+    cpy = [e[1].elapsed_time(e[2]) / 1e3 for e in evs]
+    ffn = [e[2].elapsed_time(e[3]) / 1e3 for e in evs]
+    ec_sum = sum(a + b for a, b in zip(ens, cpy))
+    bytes_total = r.misses * B * args.steps
+    agg_bytes, agg_ec = aggregate(dist, bytes_total, ec_sum, device="cuda")
+    _, agg_total = aggregate(dist, 0.0, total_s, device="cuda")
+    value = agg_bytes / agg_ec / 1e9 if agg_ec > 0 else 0.0
+    assert cache.status() == F.OK
+
+    # end to end through the C-ABI with host buffers: inputs H2D, output D2H each step
+    h_ids = torch.from_numpy(r.topk_ids).pin_memory()
+    h_w = torch.from_numpy(r.weights).pin_memory()
+    h_x = torch.from_numpy(r.x.view(np.int16).copy()).view(torch.bfloat16).pin_memory()
+    h_y = torch.empty((bs, cfg.H), dtype=torch.bfloat16).pin_memory()
+    h2d = h_ids.numel() * 4 + h_w.numel() * 4 + h_x.numel() * 2
+    d2h = h_y.numel() * 2
+    e_ev = []
+    for i in range(args.warmup + args.steps):
+        cache.set_state(r.owner, r.stamp, r.clock, stream=s)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        with torch.cuda.stream(stream):
+            d_ids.copy_(h_ids, non_blocking=True)
+            d_w.copy_(h_w, non_blocking=True)
+            d_x.copy_(h_x, non_blocking=True)
+        F.ftmoe_ensure_experts(cache.handle, 0, d_ids.data_ptr(), bs, cfg.topk, d_slots.data_ptr(), s)
+        F.ftmoe_copy_missing(cache.handle, s)
+        F.ftmoe_expert_ffn(cache.handle, d_x.data_ptr(), bs, d_slots.data_ptr(), d_w.data_ptr(), cfg.topk,
+                           d_y.data_ptr(), s)
+        with torch.cuda.stream(stream):
+            h_y.copy_(d_y, non_blocking=True)
+        b.record(stream)
+        if i >= args.warmup:
+            e_ev.append((a, b))
+    torch.cuda.synchronize()
+    e2e_s = sum(a.elapsed_time(b) for a, b in e_ev) / 1e3
+    agg_b2, agg_e2e = aggregate(dist, bytes_total, e2e_s, device="cuda")
+    e2e_value = agg_b2 / agg_e2e / 1e9 if agg_e2e > 0 else 0.0
+
+    line = None
+    if rank == 0:
+        hbm_peak, hbm_src = measured_peaks()
+        links = link_peak(torch, F, stream)
+        link = max(links.values())
+        copy_s = statistics.median(cpy)
+        ens_s = statistics.median(ens)
+        ffn_s = statistics.median(ffn)
+        time_ms = statistics.median([a + b for a, b in zip(ens, cpy)]) * 1e3
+        copy_ach = r.misses * B / copy_s / 1e9 if r.misses else 0.0
+        w_bytes = r.active * (cfg.bytes_per_expert) + 2 * bs * cfg.H * 2
+        ffn_ach = w_bytes / ffn_s / 1e9
+        launches_per_step = 2 + 1 + (1 if args.copy_mode == "fused" else (cache.nb if args.copy_mode == "per_bank" else 0)) + 4
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": agg_total / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{cfg.name} bs={bs} miss_rate={mr}", "E": cfg.E, "topk": cfg.topk, "H": cfg.H,
+                       "I": cfg.I, "L": cfg.L, "S": cfg.S, "bs": bs, "miss_rate": mr, "active": r.active,
+                       "misses": r.misses, "copy_MiB": r.misses * B / 2 ** 20, "copy_mode": args.copy_mode,
+                       "l2": f"inputs larger than L2: {r.misses * B / 2**20:.0f} MiB copied and "
+                             f"{r.active * B / 2**20:.0f} MiB of expert weights read per step",
+                       "parallelism": f"replicas x{world}",
+                       "step": "set_state (prepared state, 2 small kernels) + ensure + copy + FFN"},
+            "time_ms": time_ms, "ensure_us": ens_s * 1e6, "copy_ms": copy_s * 1e3,
+            "bw_GBps": r.misses * B / (time_ms / 1e3) / 1e9 if time_ms > 0 else 0.0,
+            "tok_ms": time_ms * cfg.L, "ffn_us": ffn_s * 1e6,
+            "roofline": {"bound": "host_link", "kernel": "copy_missing_kernel", "achieved": copy_ach, "peak": link,
+                         "unit": "GB/s", "frac": copy_ach / link if link else None, "traffic": None,
+                         "peak_source": f"measured in this run: max(1 GiB pinned->device cudaMemcpyAsync "
+                                        f"{links['memcpy']:.1f}, SM zero-copy read {links['sm_read']:.1f}) GB/s"},
+            "roofline_ffn": {"bound": "hbm", "kernel": "expert FFN (route + gate_up + down + combine)",
+                             "achieved": ffn_ach, "peak": hbm_peak, "unit": "GB/s", "frac": ffn_ach / hbm_peak,
+                             "traffic": None, "peak_source": hbm_src},
+            "link_peak_GBps": links,
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk,
+        }
+        if not args.no_sweep:
+            line["sweep"] = sweep(args, cfg, cache, stream, torch, F, wl)
+    cache.close()
+    if rank == 0 and not args.no_cpu_baseline:
+        hb = [cache.host[b][0].numpy() for b in range(cache.nb)]
+        cores = cpu_cores()
+        res = oracle_sample(cfg, r, hb, cores, ffn_tokens=2)
+        line["cpu_baseline"] = {"value": res["copy_gbps"], "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                "sample": f"ensure + copy of the full step ({res['misses']} experts into a host slot "
+                                          f"buffer, 1 thread, median of {res['reps']}); FFN of "
+                                          f"{res['ffn_tokens']} of {bs} tokens on {cores} threads: "
+                                          f"{res['ffn_s_per_token'] * 1e3:.1f} ms/token",
+                                "ffn_us_per_layer_est": res["ffn_s_per_token"] * bs * 1e6}
+    if rank == 0:
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def sweep(args, cfg, cache, stream, torch, F, wl):
+    """Every (bs, miss_rate) point of the workload: median of `repeat` ensure+copy times
+    and FFN times (each repeat from the prepared state)."""
+    out = []
+    s = stream.cuda_stream
+    B = cfg.bytes_per_expert
+    for bs in cfg.bs_list:
+        for mr in cfg.mr_list:
+            r = wl.make_route(cfg, bs, mr)
+            d_ids = torch.from_numpy(r.topk_ids).cuda()
+            d_slots = torch.empty_like(d_ids)
+            d_w = torch.from_numpy(r.weights).cuda()
+            d_x = torch.from_numpy(r.x.view(np.int16).copy()).view(torch.bfloat16).cuda()
+            d_y = torch.empty((bs, cfg.H), dtype=torch.bfloat16, device="cuda")
+            tec, tf = [], []
+            for i in range(args.repeat + 2):
+                cache.set_state(r.owner, r.stamp, r.clock, stream=s)
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                ev[0].record(stream)
+                F.ftmoe_ensure_experts(cache.handle, 0, d_ids.data_ptr(), bs, cfg.topk, d_slots.data_ptr(), s)
+                F.ftmoe_copy_missing(cache.handle, s)
+                ev[1].record(stream)
+                F.ftmoe_expert_ffn(cache.handle, d_x.data_ptr(), bs, d_slots.data_ptr(), d_w.data_ptr(), cfg.topk,
+                                   d_y.data_ptr(), s)
+                ev[2].record(stream)
+                ev[2].synchronize()
+                if i >= 2:
+                    tec.append(ev[0].elapsed_time(ev[1]))
+                    tf.append(ev[1].elapsed_time(ev[2]))
+            t = statistics.median(tec)
+            f = statistics.median(tf)
+            out.append({"bs": bs, "active": r.active, "miss_rate": mr, "misses": r.misses, "time_ms": t,
+                        "copy_MiB": r.misses * B / 2 ** 20, "bw_GBps": r.misses * B / (t / 1e3) / 1e9,
+                        "tok_ms": t * cfg.L, "ffn_us": f * 1e3,
+                        "ffn_GBps": (r.active * B + 2 * bs * cfg.H * 2) / (f / 1e3) / 1e9})
+    return out
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,456 @@
+// Host side of the C-ABI: argument checks, workspace layout, host-bank mapping and
+// kernel launches. See include/ftmoe.h for the contract of every entry point.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <vector>
+
+#include "internal.cuh"
+
+using namespace ftmoe;
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what) {
+    return fail(FTMOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define CK(call, what)                            \
+    do {                                          \
+        cudaError_t e_ = (call);                  \
+        if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+    } while (0)
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+struct Layout {
+    size_t hdr, id2slot, owner, stamp, miss_ids, miss_slots;
+    size_t n_unique, uslot, ucnt, uoff, upairs, h, o;
+    size_t total;
+    bool ffn;
+};
+
+int schema_banks(int fmt) {
+    switch (fmt) {
+        case FTMOE_FMT_BF16: return 2;
+        case FTMOE_FMT_NVFP4: return 6;
+        case FTMOE_FMT_MXFP4: return 6;
+        default: return -1;
+    }
+}
+
+// Per-expert bytes of bank b of a format's schema.
+int64_t schema_bytes(int fmt, int b, int64_t H, int64_t I) {
+    if (fmt == FTMOE_FMT_BF16) return b == 0 ? 2 * I * H * 2 : H * I * 2;
+    const int64_t N = b < 3 ? 2 * I : H, K = b < 3 ? H : I;
+    if (fmt == FTMOE_FMT_NVFP4) {
+        switch (b % 3) {
+            case 0: return N * K / 2;
+            case 1: return N * K / 16;
+            default: return N * 2;
+        }
+    }
+    if (fmt == FTMOE_FMT_MXFP4) {
+        switch (b % 3) {
+            case 0: return K / 2 * N;
+            case 1: return K / 32 * N;
+            default: return N * 2;
+        }
+    }
+    return -1;
+}
+
+int schema_dtype(int fmt, int b) {
+    if (fmt == FTMOE_FMT_BF16) return FTMOE_DT_BF16;
+    if (fmt == FTMOE_FMT_NVFP4) {
+        const int d[3] = {FTMOE_DT_U8, FTMOE_DT_E4M3, FTMOE_DT_F16};
+        return d[b % 3];
+    }
+    const int d[3] = {FTMOE_DT_U8, FTMOE_DT_E8M0, FTMOE_DT_BF16};
+    return d[b % 3];
+}
+
+Layout make_layout(int fmt, int E, int L, int S, int H, int I, int max_pairs) {
+    Layout l{};
+    size_t off = 0;
+    const int maxm = E < S ? E : S;
+    l.hdr = off; off += 256;
+    l.id2slot = off; off += align256((size_t)E * L * 4);
+    l.owner = off; off += align256((size_t)S * 4);
+    l.stamp = off; off += align256((size_t)S * 4);
+    l.miss_ids = off; off += align256((size_t)maxm * 4);
+    l.miss_slots = off; off += align256((size_t)maxm * 4);
+    l.ffn = fmt != FTMOE_FMT_RAW && max_pairs > 0;
+    if (l.ffn) {
+        const size_t P = (size_t)max_pairs;
+        l.n_unique = off; off += 256;
+        l.uslot = off; off += align256(P * 4);
+        l.ucnt = off; off += align256(P * 4);
+        l.uoff = off; off += align256(P * 4);
+        l.upairs = off; off += align256(P * 4);
+        l.h = off; off += align256(P * (size_t)I * 4);
+        l.o = off; off += align256(P * (size_t)H * 4);
+    }
+    l.total = off;
+    return l;
+}
+
+int check_geometry(int fmt, int nb, int E, int L, int S, int H, int I, int max_pairs) {
+    if (E <= 0 || E > FTMOE_MAX_EXPERTS) return fail(FTMOE_ERR_INVALID_ARG, "E=%d outside [1, %d]", E, FTMOE_MAX_EXPERTS);
+    if (S <= 0 || S > FTMOE_MAX_SLOTS) return fail(FTMOE_ERR_INVALID_ARG, "S=%d outside [1, %d]", S, FTMOE_MAX_SLOTS);
+    if (L <= 0 || (int64_t)L * E > (int64_t)1 << 30) return fail(FTMOE_ERR_INVALID_ARG, "L=%d invalid", L);
+    if (nb <= 0 || nb > FTMOE_MAX_BANKS) return fail(FTMOE_ERR_INVALID_ARG, "num_banks=%d outside [1, %d]", nb, FTMOE_MAX_BANKS);
+    if (max_pairs < 0) return fail(FTMOE_ERR_INVALID_ARG, "max_pairs < 0");
+    if (fmt == FTMOE_FMT_RAW) return FTMOE_OK;
+    if (schema_banks(fmt) < 0) return fail(FTMOE_ERR_FORMAT, "unknown format %d", fmt);
+    if (nb != schema_banks(fmt))
+        return fail(FTMOE_ERR_FORMAT, "format %d needs %d banks, got %d", fmt, schema_banks(fmt), nb);
+    if (H <= 0 || I <= 0) return fail(FTMOE_ERR_INVALID_ARG, "H=%d, I=%d must be positive", H, I);
+    const int q = fmt == FTMOE_FMT_BF16 ? 8 : 32;
+    if (H % q || I % q)
+        return fail(FTMOE_ERR_FORMAT, "format %d needs H and I multiples of %d (H=%d, I=%d)", fmt, q, H, I);
+    return FTMOE_OK;
+}
+
+}  // namespace
+
+struct ftmoe_cache {
+    int fmt, E, L, S, H, I, max_pairs, nb;
+    int num_sms;
+    int copy_mode = FTMOE_COPY_FUSED;
+    int last_layer = -1;
+    bool vec16 = true;
+    std::vector<std::vector<const void *>> host;      // [nb][L] host addresses
+    std::vector<std::vector<const unsigned char *>> dev_view;  // [nb][L] device views
+    unsigned char *dev_slots[FTMOE_MAX_BANKS];
+    int64_t bytes[FTMOE_MAX_BANKS];
+    Tables t;
+    FfnScratch s;
+    bool ffn;
+};
+
+extern "C" {
+
+const char *ftmoe_last_error(void) { return g_err; }
+
+int ftmoe_cache_workspace_bytes(int32_t format, int32_t num_banks, int32_t E, int32_t L, int32_t S, int32_t H,
+                                int32_t I, int32_t max_pairs, size_t *bytes) {
+    if (!bytes) return fail(FTMOE_ERR_INVALID_ARG, "bytes is NULL");
+    int rc = check_geometry(format, num_banks, E, L, S, H, I, max_pairs);
+    if (rc) return rc;
+    *bytes = make_layout(format, E, L, S, H, I, max_pairs).total;
+    return FTMOE_OK;
+}
+
+int ftmoe_cache_create(const ftmoe_bank_spec *banks, int32_t num_banks, int32_t format, int32_t E, int32_t L,
+                       int32_t S, int32_t H, int32_t I, int32_t max_pairs, void *d_workspace,
+                       size_t workspace_bytes, void *stream, ftmoe_cache_t **out) {
+    if (!out) return fail(FTMOE_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (!banks) return fail(FTMOE_ERR_INVALID_ARG, "banks is NULL");
+    int rc = check_geometry(format, num_banks, E, L, S, H, I, max_pairs);
+    if (rc) return rc;
+    const Layout lay = make_layout(format, E, L, S, H, I, max_pairs);
+    if (!d_workspace || ((uintptr_t)d_workspace & 255))
+        return fail(FTMOE_ERR_INVALID_ARG, "workspace must be a 256-byte aligned device pointer");
+    if (workspace_bytes < lay.total)
+        return fail(FTMOE_ERR_INVALID_ARG, "workspace has %zu bytes, needs %zu", workspace_bytes, lay.total);
+
+    ftmoe_cache *c = new ftmoe_cache();
+    c->fmt = format; c->E = E; c->L = L; c->S = S; c->H = H; c->I = I;
+    c->max_pairs = max_pairs; c->nb = num_banks; c->ffn = lay.ffn;
+    c->host.assign(num_banks, std::vector<const void *>(L, nullptr));
+    c->dev_view.assign(num_banks, std::vector<const unsigned char *>(L, nullptr));
+    for (int b = 0; b < num_banks; b++) {
+        const ftmoe_bank_spec &bs = banks[b];
+        const int64_t nbytes = bs.rows * bs.row_bytes;
+        if (bs.rows <= 0 || bs.row_bytes <= 0) {
+            delete c;
+            return fail(FTMOE_ERR_INVALID_ARG, "bank %d: rows and row_bytes must be positive", b);
+        }
+        if (format != FTMOE_FMT_RAW) {
+            const int64_t want = schema_bytes(format, b, H, I);
+            if (nbytes != want) {
+                delete c;
+                return fail(FTMOE_ERR_FORMAT, "bank %d (%s): %lld bytes per expert, schema needs %lld", b,
+                            bs.name ? bs.name : "?", (long long)nbytes, (long long)want);
+            }
+            if (bs.dtype != schema_dtype(format, b)) {
+                delete c;
+                return fail(FTMOE_ERR_FORMAT, "bank %d (%s): dtype %d, schema needs %d", b, bs.name ? bs.name : "?",
+                            bs.dtype, schema_dtype(format, b));
+            }
+        }
+        if (!bs.dev_slots || !bs.host_src) {
+            delete c;
+            return fail(FTMOE_ERR_INVALID_ARG, "bank %d: NULL dev_slots or host_src", b);
+        }
+        c->dev_slots[b] = static_cast<unsigned char *>(bs.dev_slots);
+        c->bytes[b] = nbytes;
+        if (nbytes % 16 || (uintptr_t)bs.dev_slots % 16) c->vec16 = false;
+    }
+    // map the host banks only once every bank passed the host-side checks
+    for (int b = 0; b < num_banks; b++) {
+        for (int l = 0; l < L; l++) {
+            const void *h = banks[b].host_src[l];
+            c->host[b][l] = h;
+            if (!h) continue;
+            if ((uintptr_t)h % 16) c->vec16 = false;
+            cudaPointerAttributes attr;
+            cudaError_t e = cudaPointerGetAttributes(&attr, h);
+            if (e != cudaSuccess || attr.type != cudaMemoryTypeHost || !attr.devicePointer) {
+                cudaGetLastError();
+                delete c;
+                return fail(FTMOE_ERR_INVALID_ARG, "bank %d layer %d: host pointer is not page-locked mapped memory", b,
+                            l);
+            }
+            c->dev_view[b][l] = static_cast<const unsigned char *>(attr.devicePointer);
+        }
+    }
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) {
+        delete c;
+        return cuda_fail(e, "device query");
+    }
+
+    unsigned char *ws = static_cast<unsigned char *>(d_workspace);
+    c->t.clock = reinterpret_cast<uint32_t *>(ws + lay.hdr);
+    c->t.status = reinterpret_cast<int32_t *>(ws + lay.hdr + 4);
+    c->t.num_miss = reinterpret_cast<int32_t *>(ws + lay.hdr + 8);
+    c->t.id2slot = reinterpret_cast<int32_t *>(ws + lay.id2slot);
+    c->t.owner = reinterpret_cast<int32_t *>(ws + lay.owner);
+    c->t.stamp = reinterpret_cast<uint32_t *>(ws + lay.stamp);
+    c->t.miss_ids = reinterpret_cast<int32_t *>(ws + lay.miss_ids);
+    c->t.miss_slots = reinterpret_cast<int32_t *>(ws + lay.miss_slots);
+    if (lay.ffn) {
+        c->s.n_unique = reinterpret_cast<int32_t *>(ws + lay.n_unique);
+        c->s.uslot = reinterpret_cast<int32_t *>(ws + lay.uslot);
+        c->s.ucnt = reinterpret_cast<int32_t *>(ws + lay.ucnt);
+        c->s.uoff = reinterpret_cast<int32_t *>(ws + lay.uoff);
+        c->s.upairs = reinterpret_cast<int32_t *>(ws + lay.upairs);
+        c->s.h = reinterpret_cast<float *>(ws + lay.h);
+        c->s.o = reinterpret_cast<float *>(ws + lay.o);
+    }
+    e = launch_init_state(c->t, E, L, S, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        delete c;
+        return cuda_fail(e, "init state");
+    }
+    *out = c;
+    return FTMOE_OK;
+}
+
+int ftmoe_cache_destroy(ftmoe_cache_t *cache) {
+    delete cache;
+    return FTMOE_OK;
+}
+
+int ftmoe_set_copy_mode(ftmoe_cache_t *c, int32_t mode) {
+    if (!c) return fail(FTMOE_ERR_INVALID_ARG, "cache is NULL");
+    if (mode != FTMOE_COPY_FUSED && mode != FTMOE_COPY_PER_BANK && mode != FTMOE_COPY_ENGINE)
+        return fail(FTMOE_ERR_INVALID_ARG, "unknown copy mode %d", mode);
+    c->copy_mode = mode;
+    return FTMOE_OK;
+}
+
+int ftmoe_ensure_experts(ftmoe_cache_t *c, int32_t layer, const int32_t *d_topk_ids, int32_t bs, int32_t topk,
+                         int32_t *d_slots_out, void *stream) {
+    if (!c) return fail(FTMOE_ERR_INVALID_ARG, "cache is NULL");
+    if (layer < 0 || layer >= c->L) return fail(FTMOE_ERR_INVALID_ARG, "layer %d outside [0, %d)", layer, c->L);
+    if (bs < 0 || topk < 0) return fail(FTMOE_ERR_INVALID_ARG, "bs and topk must be >= 0");
+    const int64_t n = (int64_t)bs * topk;
+    if (n > FTMOE_MAX_IDS_PER_CALL) return fail(FTMOE_ERR_INVALID_ARG, "bs*topk=%lld above %d", (long long)n, FTMOE_MAX_IDS_PER_CALL);
+    if (n > 0 && (!d_topk_ids || !d_slots_out)) return fail(FTMOE_ERR_INVALID_ARG, "NULL ids or slots_out");
+    for (int b = 0; b < c->nb; b++)
+        if (!c->dev_view[b][layer])
+            return fail(FTMOE_ERR_INVALID_ARG, "layer %d of bank %d has no host source", layer, b);
+    EnsureParams p;
+    p.t = c->t;
+    p.ids = d_topk_ids;
+    p.slots_out = d_slots_out;
+    p.E = c->E; p.L = c->L; p.S = c->S; p.layer = layer; p.n = (int)n;
+    int spad = 2;
+    while (spad < c->S) spad <<= 1;
+    p.Spad = spad;
+    p.maxm = c->E < c->S ? c->E : c->S;
+    cudaError_t e = launch_ensure(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ensure kernel");
+    c->last_layer = layer;
+    return FTMOE_OK;
+}
+
+static void fill_copy_params(const ftmoe_cache *c, int b_first, int b_count, CopyParams &p) {
+    memset(&p, 0, sizeof p);
+    p.nb = b_count;
+    p.E = c->E;
+    p.miss_ids = c->t.miss_ids;
+    p.miss_slots = c->t.miss_slots;
+    p.num_miss = c->t.num_miss;
+    int64_t tiles = 0;
+    for (int i = 0; i < b_count; i++) {
+        const int b = b_first + i;
+        p.src[i] = c->dev_view[b][c->last_layer];
+        p.dst[i] = c->dev_slots[b];
+        p.bytes[i] = c->bytes[b];
+        p.tile0[i] = tiles;
+        tiles += (c->bytes[b] + kCopyTile - 1) / kCopyTile;
+    }
+    p.tile0[b_count] = tiles;
+}
+
+int ftmoe_copy_missing(ftmoe_cache_t *c, void *stream) {
+    if (!c) return fail(FTMOE_ERR_INVALID_ARG, "cache is NULL");
+    if (c->last_layer < 0) return fail(FTMOE_ERR_STATE, "copy_missing before any ensure_experts call");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int grid = c->num_sms * 4;
+    if (c->copy_mode == FTMOE_COPY_FUSED) {
+        CopyParams p;
+        fill_copy_params(c, 0, c->nb, p);
+        CK(launch_copy(p, c->vec16, grid, st), "copy kernel");
+    } else if (c->copy_mode == FTMOE_COPY_PER_BANK) {
+        for (int b = 0; b < c->nb; b++) {
+            CopyParams p;
+            fill_copy_params(c, b, 1, p);
+            CK(launch_copy(p, c->vec16, grid, st), "copy kernel (per bank)");
+        }
+    } else {
+        const int maxm = c->E < c->S ? c->E : c->S;
+        std::vector<int32_t> ids(maxm), slots(maxm);
+        int32_t m = 0;
+        CK(cudaMemcpyAsync(&m, c->t.num_miss, 4, cudaMemcpyDeviceToHost, st), "read miss count");
+        CK(cudaStreamSynchronize(st), "sync");
+        if (m > 0) {
+            CK(cudaMemcpyAsync(ids.data(), c->t.miss_ids, (size_t)m * 4, cudaMemcpyDeviceToHost, st), "read miss ids");
+            CK(cudaMemcpyAsync(slots.data(), c->t.miss_slots, (size_t)m * 4, cudaMemcpyDeviceToHost, st), "read miss slots");
+            CK(cudaStreamSynchronize(st), "sync");
+        }
+        for (int j = 0; j < m; j++) {
+            const int64_t e = ids[j] % c->E, s = slots[j];
+            for (int b = 0; b < c->nb; b++) {
+                const unsigned char *src = static_cast<const unsigned char *>(c->host[b][c->last_layer]) + e * c->bytes[b];
+                CK(cudaMemcpyAsync(c->dev_slots[b] + s * c->bytes[b], src, (size_t)c->bytes[b],
+                                   cudaMemcpyHostToDevice, st),
+                   "copy engine");
+            }
+        }
+    }
+    return FTMOE_OK;
+}
+
+int ftmoe_expert_ffn(ftmoe_cache_t *c, const void *d_x_bf16, int32_t bs, const int32_t *d_slots,
+                     const float *d_weights, int32_t topk, void *d_y_bf16, void *stream) {
+    if (!c) return fail(FTMOE_ERR_INVALID_ARG, "cache is NULL");
+    if (c->fmt == FTMOE_FMT_RAW) return fail(FTMOE_ERR_FORMAT, "a raw-format cache has no FFN");
+    if (!c->ffn) return fail(FTMOE_ERR_INVALID_ARG, "cache created with max_pairs = 0");
+    if (bs < 0 || topk <= 0) return fail(FTMOE_ERR_INVALID_ARG, "bs >= 0 and topk > 0 required");
+    const int64_t P = (int64_t)bs * topk;
+    if (P > c->max_pairs) return fail(FTMOE_ERR_INVALID_ARG, "bs*topk=%lld above max_pairs=%d", (long long)P, c->max_pairs);
+    if (P == 0) return FTMOE_OK;
+    if (!d_x_bf16 || !d_slots || !d_weights || !d_y_bf16) return fail(FTMOE_ERR_INVALID_ARG, "NULL FFN argument");
+    if (((uintptr_t)d_x_bf16 | (uintptr_t)d_y_bf16) % 16)
+        return fail(FTMOE_ERR_INVALID_ARG, "x and y must be 16-byte aligned");
+    FfnParams p;
+    memset(&p, 0, sizeof p);
+    p.s = c->s;
+    for (int b = 0; b < c->nb && b < 6; b++) {
+        p.bank[b] = c->dev_slots[b];
+        p.bank_bytes[b] = c->bytes[b];
+    }
+    p.x = static_cast<const uint16_t *>(d_x_bf16);
+    p.slots = d_slots;
+    p.weights = d_weights;
+    p.y = static_cast<uint16_t *>(d_y_bf16);
+    p.status = c->t.status;
+    p.fmt = c->fmt; p.H = c->H; p.I = c->I; p.S = c->S; p.bs = bs; p.topk = topk; p.P = (int)P;
+    CK(launch_ffn(p, c->num_sms, static_cast<cudaStream_t>(stream)), "ffn kernels");
+    return FTMOE_OK;
+}
+
+int ftmoe_cache_get_state(ftmoe_cache_t *c, int32_t *h_owner, uint32_t *h_stamp, uint32_t *h_clock, void *stream) {
+    if (!c || !h_owner || !h_stamp || !h_clock) return fail(FTMOE_ERR_INVALID_ARG, "NULL argument");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    CK(cudaMemcpyAsync(h_owner, c->t.owner, (size_t)c->S * 4, cudaMemcpyDeviceToHost, st), "read owner");
+    CK(cudaMemcpyAsync(h_stamp, c->t.stamp, (size_t)c->S * 4, cudaMemcpyDeviceToHost, st), "read stamp");
+    CK(cudaMemcpyAsync(h_clock, c->t.clock, 4, cudaMemcpyDeviceToHost, st), "read clock");
+    CK(cudaStreamSynchronize(st), "sync");
+    return FTMOE_OK;
+}
+
+int ftmoe_cache_set_state(ftmoe_cache_t *c, const int32_t *h_owner, const uint32_t *h_stamp, uint32_t clock,
+                          void *stream) {
+    if (!c || !h_owner || !h_stamp) return fail(FTMOE_ERR_INVALID_ARG, "NULL argument");
+    const int64_t LE = (int64_t)c->L * c->E;
+    std::vector<char> seen((size_t)LE, 0);
+    for (int s = 0; s < c->S; s++) {
+        const int32_t f = h_owner[s];
+        if (f < -1 || f >= LE) return fail(FTMOE_ERR_STATE, "owner[%d]=%d outside [-1, %lld)", s, f, (long long)LE);
+        if (f >= 0) {
+            if (seen[f]) return fail(FTMOE_ERR_STATE, "id %d owns two slots", f);
+            seen[f] = 1;
+        }
+        if (h_stamp[s] > clock) return fail(FTMOE_ERR_STATE, "stamp[%d]=%u above clock %u", s, h_stamp[s], clock);
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // pageable sources: cudaMemcpyAsync stages them before it returns
+    CK(cudaMemcpyAsync(c->t.owner, h_owner, (size_t)c->S * 4, cudaMemcpyHostToDevice, st), "write owner");
+    CK(cudaMemcpyAsync(c->t.stamp, h_stamp, (size_t)c->S * 4, cudaMemcpyHostToDevice, st), "write stamp");
+    CK(cudaMemcpyAsync(c->t.clock, &clock, 4, cudaMemcpyHostToDevice, st), "write clock");
+    CK(launch_rebuild_id2slot(c->t, c->E, c->L, c->S, st), "rebuild id2slot");
+    CK(cudaStreamSynchronize(st), "sync");
+    return FTMOE_OK;
+}
+
+int ftmoe_get_miss_list(ftmoe_cache_t *c, int32_t *h_ids, int32_t *h_slots, int32_t *h_m, void *stream) {
+    if (!c || !h_ids || !h_slots || !h_m) return fail(FTMOE_ERR_INVALID_ARG, "NULL argument");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    CK(cudaMemcpyAsync(h_m, c->t.num_miss, 4, cudaMemcpyDeviceToHost, st), "read miss count");
+    CK(cudaStreamSynchronize(st), "sync");
+    if (*h_m > 0) {
+        CK(cudaMemcpyAsync(h_ids, c->t.miss_ids, (size_t)*h_m * 4, cudaMemcpyDeviceToHost, st), "read miss ids");
+        CK(cudaMemcpyAsync(h_slots, c->t.miss_slots, (size_t)*h_m * 4, cudaMemcpyDeviceToHost, st), "read miss slots");
+        CK(cudaStreamSynchronize(st), "sync");
+    }
+    return FTMOE_OK;
+}
+
+int ftmoe_get_device_status(ftmoe_cache_t *c, int32_t *h_status, void *stream) {
+    if (!c || !h_status) return fail(FTMOE_ERR_INVALID_ARG, "NULL argument");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    CK(cudaMemcpyAsync(h_status, c->t.status, 4, cudaMemcpyDeviceToHost, st), "read status");
+    CK(cudaMemsetAsync(c->t.status, 0, 4, st), "clear status");
+    CK(cudaStreamSynchronize(st), "sync");
+    return FTMOE_OK;
+}
+
+int ftmoe_h2d_stream_copy(void *d_dst, const void *h_src, size_t bytes, void *stream) {
+    if (!d_dst || !h_src) return fail(FTMOE_ERR_INVALID_ARG, "NULL argument");
+    if (bytes == 0) return FTMOE_OK;
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, h_src);
+    if (e != cudaSuccess || attr.type != cudaMemoryTypeHost || !attr.devicePointer) {
+        cudaGetLastError();
+        return fail(FTMOE_ERR_INVALID_ARG, "source is not page-locked mapped host memory");
+    }
+    int dev = 0, sms = 0;
+    CK(cudaGetDevice(&dev), "device");
+    CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "device query");
+    const bool vec = ((uintptr_t)d_dst % 16 == 0) && ((uintptr_t)attr.devicePointer % 16 == 0) && (bytes % 16 == 0);
+    CK(launch_linear_copy(static_cast<unsigned char *>(d_dst), static_cast<const unsigned char *>(attr.devicePointer),
+                          (int64_t)bytes, vec, sms * 4, static_cast<cudaStream_t>(stream)),
+       "linear copy");
+    return FTMOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,241 @@
+// K1: ensure_experts — dedup, slot lookup and LRU eviction in one CTA.
+//
+// FreeToken benchmark guide ("FreeToken MoE 离线推理基准完全指南"), section 4.1:
+// ensure_experts is the LRU slot remap of a layer's routed experts; section 4.3:
+// flat id = layer * E + expert. Architecture deep-dive, section 五: one global
+// LRU cache shared by all layers. Victim rule: the misses, ascending by flat id,
+// take the slots not hit in this call in ascending (stamp, slot) order.
+//
+// One CTA of 1024 threads does the whole call so that the miss list is ready on
+// the device for the copy kernel without a host round trip:
+//   1. mark the routed local ids in a shared table over E (dedup; scanning the
+//      table in index order yields the distinct ids already ascending);
+//   2. probe id2slot for every distinct id; hits mark their slot as used;
+//   3. block-wide prefix sum over the miss flags gives every miss its rank;
+//   4. 64-bit keys (stamp << 32 | slot) of the unused slots are sorted in shared
+//      memory (bitonic network: shuffles inside a warp, shared memory across
+//      warps); the j-th smallest key is the j-th victim — exactly the
+//      lowest-(stamp, slot) rule;
+//   5. tables are updated and every routed position gets its slot.
+// Errors (id out of range, clock exhausted, too many misses) write only the
+// status word, -1 slots and an empty miss list.
+#include "internal.cuh"
+
+namespace ftmoe {
+namespace {
+
+constexpr int kThreads = 1024;
+
+__device__ __forceinline__ void set_status(int32_t *status, int err) { atomicCAS(status, 0, err); }
+
+// Exclusive prefix sum of `flag` over the block (deterministic, in thread order).
+__device__ __forceinline__ int block_excl_scan(int flag, int *warp_tot, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    unsigned ball = __ballot_sync(0xffffffffu, flag);
+    int pre = __popc(ball & ((1u << lane) - 1u));
+    if (lane == 0) warp_tot[warp] = __popc(ball);
+    __syncthreads();
+    if (warp == 0) {
+        int v = (lane < (int)(blockDim.x >> 5)) ? warp_tot[lane] : 0;
+        int incl = v;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            int u = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += u;
+        }
+        warp_tot[lane] = incl - v;  // exclusive warp offsets
+        if (lane == 31) *total = incl;
+    }
+    __syncthreads();
+    int r = warp_tot[warp] + pre;
+    __syncthreads();  // warp_tot reused by the next call
+    return r;
+}
+
+// In-place ascending bitonic sort of n (power of two) keys in shared memory.
+__device__ void bitonic_sort(uint64_t *keys, int n) {
+    for (int k = 2; k <= n; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = threadIdx.x; i < (n >> 1); i += blockDim.x) {
+                int lo = ((i & ~(j - 1)) << 1) | (i & (j - 1));
+                int hi = lo + j;
+                bool up = (lo & k) == 0;
+                uint64_t a = keys[lo], b = keys[hi];
+                if ((a > b) == up) {
+                    keys[lo] = b;
+                    keys[hi] = a;
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) ensure_kernel(EnsureParams p) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    uint64_t *keys = reinterpret_cast<uint64_t *>(smem);          // [Spad]
+    int32_t *s_slot = reinterpret_cast<int32_t *>(keys + p.Spad);  // [E]: -2 absent, -1 miss, >=0 slot
+    int32_t *s_miss = s_slot + p.E;                               // [maxm] flat ids by rank
+    unsigned char *s_hit = reinterpret_cast<unsigned char *>(s_miss + p.maxm);  // [S]
+    __shared__ int warp_tot[32];
+    __shared__ int s_bad_id, s_m, s_h, s_tmp;
+
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int E = p.E, S = p.S;
+    if (tid == 0) {
+        s_bad_id = 0;
+        s_h = 0;
+    }
+    for (int e = tid; e < E; e += nt) s_slot[e] = -2;
+    for (int s = tid; s < S; s += nt) s_hit[s] = 0;
+    __syncthreads();
+
+    // 1. dedup (benign races: every writer stores the same value)
+    for (int t = tid; t < p.n; t += nt) {
+        int id = p.ids[t];
+        if ((unsigned)id >= (unsigned)E)
+            s_bad_id = 1;
+        else
+            s_slot[id] = -1;
+    }
+    const uint32_t clock = *p.t.clock;
+    __syncthreads();
+
+    int err = s_bad_id ? FTMOE_ERR_ID_RANGE : (clock == 0xFFFFFFFFu ? FTMOE_ERR_STATE : 0);
+    if (err == 0) {
+        // 2. probe
+        const int32_t *row = p.t.id2slot + (int64_t)p.layer * E;
+        int hits = 0;
+        for (int e = tid; e < E; e += nt) {
+            if (s_slot[e] == -1) {
+                int s = row[e];
+                if (s >= 0) {
+                    s_slot[e] = s;
+                    s_hit[s] = 1;
+                    hits++;
+                }
+            }
+        }
+        if (hits) atomicAdd(&s_h, hits);
+        // 3. miss ranks in ascending id (s_slot writes above are read only by their writer)
+        int base = 0;
+        for (int e0 = 0; e0 < E; e0 += nt) {
+            int e = e0 + tid;
+            int flag = (e < E) && (s_slot[e] == -1);
+            int r = block_excl_scan(flag, warp_tot, &s_tmp);
+            // more than min(E, S) misses is a capacity error found below; never write past the list
+            if (flag && base + r < p.maxm) s_miss[base + r] = p.layer * E + e;
+            base += s_tmp;  // every thread reads the same total (synchronised in the scan)
+            __syncthreads();
+        }
+        if (tid == 0) s_m = base;
+        __syncthreads();
+        if (s_m > S - s_h) err = FTMOE_ERR_CAPACITY;
+    }
+    if (err != 0) {
+        for (int t = tid; t < p.n; t += nt) p.slots_out[t] = -1;
+        if (tid == 0) {
+            *p.t.num_miss = 0;
+            set_status(p.t.status, err);
+        }
+        return;
+    }
+
+    const int m = s_m;
+    const uint32_t now = clock + 1;
+    // 4. victims: m smallest (stamp, slot) keys among the slots not hit in this call
+    if (m > 0) {
+        for (int s = tid; s < p.Spad; s += nt)
+            keys[s] = (s < S && !s_hit[s]) ? ((uint64_t)p.t.stamp[s] << 32) | (uint32_t)s : ~0ull;
+        __syncthreads();
+        bitonic_sort(keys, p.Spad);
+    }
+    // 5. update: hit stamps, then victims (hit and victim slots are disjoint; an
+    //    evicted owner is never one of this call's misses, whose id2slot is -1)
+    for (int s = tid; s < S; s += nt)
+        if (s_hit[s]) p.t.stamp[s] = now;
+    for (int j = tid; j < m; j += nt) {
+        int s = (int)(uint32_t)(keys[j] & 0xffffffffu);
+        int f = s_miss[j];
+        int old = p.t.owner[s];
+        if (old >= 0) p.t.id2slot[old] = -1;
+        p.t.owner[s] = f;
+        p.t.id2slot[f] = s;
+        p.t.stamp[s] = now;
+        p.t.miss_ids[j] = f;
+        p.t.miss_slots[j] = s;
+        s_slot[f - p.layer * E] = s;
+    }
+    __syncthreads();
+    for (int t = tid; t < p.n; t += nt) p.slots_out[t] = s_slot[p.ids[t]];
+    if (tid == 0) {
+        *p.t.clock = now;
+        *p.t.num_miss = m;
+    }
+}
+
+__global__ void init_state_kernel(Tables t, int LE, int S) {
+    int i = blockIdx.x * blockDim.x + threadIdx.x;
+    int stride = gridDim.x * blockDim.x;
+    for (int f = i; f < LE; f += stride) t.id2slot[f] = -1;
+    for (int s = i; s < S; s += stride) {
+        t.owner[s] = -1;
+        t.stamp[s] = 0;
+    }
+    if (i == 0) {
+        *t.clock = 0;
+        *t.status = 0;
+        *t.num_miss = 0;
+    }
+}
+
+__global__ void clear_id2slot_kernel(Tables t, int LE) {
+    int i = blockIdx.x * blockDim.x + threadIdx.x;
+    for (int f = i; f < LE; f += gridDim.x * blockDim.x) t.id2slot[f] = -1;
+}
+
+__global__ void scatter_owner_kernel(Tables t, int S) {
+    int s = blockIdx.x * blockDim.x + threadIdx.x;
+    if (s < S) {
+        int f = t.owner[s];
+        if (f >= 0) t.id2slot[f] = s;
+    }
+    if (s == 0) *t.num_miss = 0;
+}
+
+}  // namespace
+
+size_t ensure_smem_bytes(int E, int S, int Spad, int maxm) {
+    size_t b = (size_t)Spad * 8 + (size_t)E * 4 + (size_t)maxm * 4 + (size_t)S;
+    return (b + 15) & ~(size_t)15;
+}
+
+cudaError_t launch_ensure(const EnsureParams &p, cudaStream_t st) {
+    size_t smem = ensure_smem_bytes(p.E, p.S, p.Spad, p.maxm);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(ensure_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    ensure_kernel<<<1, kThreads, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_init_state(Tables t, int E, int L, int S, cudaStream_t st) {
+    int LE = E * L;
+    int n = LE > S ? LE : S;
+    int grid = (n + 255) / 256;
+    if (grid > 1024) grid = 1024;
+    init_state_kernel<<<grid, 256, 0, st>>>(t, LE, S);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rebuild_id2slot(Tables t, int E, int L, int S, cudaStream_t st) {
+    int LE = E * L;
+    int grid = (LE + 255) / 256;
+    if (grid > 1024) grid = 1024;
+    clear_id2slot_kernel<<<grid, 256, 0, st>>>(t, LE);
+    scatter_owner_kernel<<<(S + 255) / 256, 256, 0, st>>>(t, S);
+    return cudaGetLastError();
+}
+
+}  // namespace ftmoe

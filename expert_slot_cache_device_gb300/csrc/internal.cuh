@@ -1,0 +1,85 @@
+// Internal declarations of libftmoe (not part of the C-ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ftmoe.h"
+
+namespace ftmoe {
+
+// ---------------------------------------------------------------- cache tables
+// Device-resident state of one cache; all pointers point into the caller's
+// workspace.
+struct Tables {
+    uint32_t *clock;      // [1]
+    int32_t *status;      // [1] sticky device error
+    int32_t *num_miss;    // [1] misses of the last ensure call
+    int32_t *id2slot;     // [L * E]
+    int32_t *owner;       // [S]
+    uint32_t *stamp;      // [S]
+    int32_t *miss_ids;    // [min(E, S)] flat ids, ascending
+    int32_t *miss_slots;  // [min(E, S)]
+};
+
+// ---------------------------------------------------------------- K1 ensure
+struct EnsureParams {
+    Tables t;
+    const int32_t *ids;   // [n] routed local ids
+    int32_t *slots_out;   // [n]
+    int32_t E, L, S, layer, n;
+    int32_t Spad;         // power of two >= S (bitonic sort width)
+    int32_t maxm;         // min(E, S)
+};
+size_t ensure_smem_bytes(int E, int S, int Spad, int maxm);
+cudaError_t launch_ensure(const EnsureParams &p, cudaStream_t st);
+
+// ---------------------------------------------------------------- K2 copy
+constexpr int kCopyThreads = 256;
+constexpr int kCopyUnroll = 8;
+constexpr int64_t kCopyTile = (int64_t)kCopyThreads * 16 * kCopyUnroll;  // 32 KiB
+
+struct CopyParams {
+    const unsigned char *src[FTMOE_MAX_BANKS];  // device view of the layer's host bank
+    unsigned char *dst[FTMOE_MAX_BANKS];        // slot bank
+    int64_t bytes[FTMOE_MAX_BANKS];             // per-expert bytes of each bank
+    int64_t tile0[FTMOE_MAX_BANKS + 1];         // prefix of tiles per expert over banks
+    const int32_t *miss_ids;
+    const int32_t *miss_slots;
+    const int32_t *num_miss;
+    int32_t nb, E;
+};
+cudaError_t launch_copy(const CopyParams &p, bool vec16, int grid, cudaStream_t st);
+cudaError_t launch_linear_copy(unsigned char *dst, const unsigned char *src, int64_t bytes, bool vec16,
+                               int grid, cudaStream_t st);
+
+// ---------------------------------------------------------------- state rebuild
+cudaError_t launch_init_state(Tables t, int E, int L, int S, cudaStream_t st);
+cudaError_t launch_rebuild_id2slot(Tables t, int E, int L, int S, cudaStream_t st);
+
+// ---------------------------------------------------------------- K3 expert FFN
+struct FfnScratch {
+    int32_t *n_unique;  // [1] distinct slots of the call (0 on a bad slot)
+    int32_t *uslot;     // [P] distinct slots, ascending
+    int32_t *ucnt;      // [P] routed pairs per distinct slot
+    int32_t *uoff;      // [P] first entry of the slot's pairs in upairs
+    int32_t *upairs;    // [P] pair indices t * topk + j grouped by slot
+    float *h;           // [P, I] SiLU(gate) * up per pair
+    float *o;           // [P, H] down output per pair
+};
+
+struct FfnParams {
+    FfnScratch s;
+    // slot banks (schema order of the format)
+    const unsigned char *bank[6];
+    int64_t bank_bytes[6];
+    const uint16_t *x;      // [bs, H] bf16
+    const int32_t *slots;   // [P]
+    const float *weights;   // [P]
+    uint16_t *y;            // [bs, H] bf16
+    int32_t *status;
+    int32_t fmt, H, I, S, bs, topk, P;
+};
+cudaError_t launch_ffn(const FfnParams &p, int num_sms, cudaStream_t st);
+
+}  // namespace ftmoe

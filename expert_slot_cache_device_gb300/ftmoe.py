@@ -1,0 +1,167 @@
+"""Thin ctypes binding of libftmoe (see include/ftmoe.h for every contract).
+
+Functions keep the C names and only marshal arguments: device pointers and streams
+are plain integers (``tensor.data_ptr()``, ``torch.cuda.Stream.cuda_stream``). Every
+non-zero status raises :class:`FtmoeError` with the library's message. Loading fails
+loudly when the compiled library is missing; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Sequence
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libftmoe.so")
+
+OK = 0
+ERR_INVALID_ARG, ERR_CAPACITY, ERR_ID_RANGE, ERR_CUDA, ERR_FORMAT, ERR_STATE = -1, -2, -3, -4, -5, -6
+ERR_NAMES = {0: "OK", -1: "INVALID_ARG", -2: "CAPACITY", -3: "ID_RANGE", -4: "CUDA", -5: "FORMAT", -6: "STATE"}
+FMT_RAW, FMT_BF16, FMT_NVFP4, FMT_MXFP4 = 0, 1, 2, 3
+FORMATS = {"raw": FMT_RAW, "bf16": FMT_BF16, "nvfp4": FMT_NVFP4, "mxfp4": FMT_MXFP4}
+DT_U8, DT_BF16, DT_F16, DT_E4M3, DT_E8M0 = 0, 1, 2, 3, 4
+DTYPES = {"u8": DT_U8, "bf16": DT_BF16, "f16": DT_F16, "e4m3": DT_E4M3, "e8m0": DT_E8M0}
+COPY_FUSED, COPY_PER_BANK, COPY_ENGINE = 0, 1, 2
+MAX_BANKS = 8
+
+EXPORTS = [
+    "ftmoe_cache_workspace_bytes", "ftmoe_cache_create", "ftmoe_cache_destroy", "ftmoe_ensure_experts",
+    "ftmoe_copy_missing", "ftmoe_expert_ffn", "ftmoe_set_copy_mode", "ftmoe_cache_get_state",
+    "ftmoe_cache_set_state", "ftmoe_get_miss_list", "ftmoe_get_device_status", "ftmoe_h2d_stream_copy",
+    "ftmoe_last_error",
+]
+
+
+class FtmoeError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"ftmoe error {code} ({ERR_NAMES.get(code, '?')}): {msg}")
+        self.code = code
+
+
+class BankSpec(ctypes.Structure):
+    _fields_ = [
+        ("name", ctypes.c_char_p),
+        ("dtype", ctypes.c_int32),
+        ("rows", ctypes.c_int64),
+        ("row_bytes", ctypes.c_int64),
+        ("host_src", ctypes.POINTER(ctypes.c_void_p)),
+        ("dev_slots", ctypes.c_void_p),
+    ]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libftmoe.so (built by ``expert_slot_cache_device_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it first (python -m expert_slot_cache_device_gb300.build)")
+    L = ctypes.CDLL(LIB_PATH)
+    i32, u32, P, sz = ctypes.c_int32, ctypes.c_uint32, ctypes.c_void_p, ctypes.c_size_t
+    sig = {
+        "ftmoe_cache_workspace_bytes": [i32, i32, i32, i32, i32, i32, i32, i32, ctypes.POINTER(sz)],
+        "ftmoe_cache_create": [ctypes.POINTER(BankSpec), i32, i32, i32, i32, i32, i32, i32, i32, P, sz, P,
+                               ctypes.POINTER(P)],
+        "ftmoe_cache_destroy": [P],
+        "ftmoe_ensure_experts": [P, i32, P, i32, i32, P, P],
+        "ftmoe_copy_missing": [P, P],
+        "ftmoe_expert_ffn": [P, P, i32, P, P, i32, P, P],
+        "ftmoe_set_copy_mode": [P, i32],
+        "ftmoe_cache_get_state": [P, P, P, P, P],
+        "ftmoe_cache_set_state": [P, P, P, u32, P],
+        "ftmoe_get_miss_list": [P, P, P, P, P],
+        "ftmoe_get_device_status": [P, P, P],
+        "ftmoe_h2d_stream_copy": [P, P, sz, P],
+    }
+    for name, args in sig.items():
+        f = getattr(L, name)
+        f.argtypes = args
+        f.restype = ctypes.c_int
+    L.ftmoe_last_error.argtypes = []
+    L.ftmoe_last_error.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def _check(rc: int) -> int:
+    if rc != OK:
+        raise FtmoeError(rc, lib().ftmoe_last_error().decode(errors="replace"))
+    return rc
+
+
+def ftmoe_last_error() -> str:
+    return lib().ftmoe_last_error().decode(errors="replace")
+
+
+def ftmoe_cache_workspace_bytes(fmt: int, num_banks: int, E: int, L: int, S: int, H: int, I: int,
+                                max_pairs: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().ftmoe_cache_workspace_bytes(fmt, num_banks, E, L, S, H, I, max_pairs, ctypes.byref(out)))
+    return out.value
+
+
+def make_bank_specs(banks: Sequence[dict]):
+    """ctypes array of ftmoe_bank_spec from dicts with keys name, dtype (code), rows,
+    row_bytes, host_src (list of L integer host addresses, 0 = unfilled), dev_slots
+    (integer device address). Returns (array, keepalive)."""
+    arr = (BankSpec * len(banks))()
+    keep = []
+    for i, b in enumerate(banks):
+        srcs = (ctypes.c_void_p * len(b["host_src"]))(*[v or None for v in b["host_src"]])
+        name = b.get("name", "").encode()
+        keep += [srcs, name]
+        arr[i] = BankSpec(name, b["dtype"], b["rows"], b["row_bytes"], srcs, b["dev_slots"])
+    return arr, keep
+
+
+def ftmoe_cache_create(specs, num_banks: int, fmt: int, E: int, L: int, S: int, H: int, I: int, max_pairs: int,
+                       d_workspace: int, workspace_bytes: int, stream: int) -> int:
+    out = ctypes.c_void_p(0)
+    _check(lib().ftmoe_cache_create(specs, num_banks, fmt, E, L, S, H, I, max_pairs, d_workspace, workspace_bytes,
+                                    stream, ctypes.byref(out)))
+    return out.value
+
+
+def ftmoe_cache_destroy(cache: int) -> None:
+    _check(lib().ftmoe_cache_destroy(cache))
+
+
+def ftmoe_ensure_experts(cache: int, layer: int, d_topk_ids: int, bs: int, topk: int, d_slots_out: int,
+                         stream: int) -> None:
+    _check(lib().ftmoe_ensure_experts(cache, layer, d_topk_ids, bs, topk, d_slots_out, stream))
+
+
+def ftmoe_copy_missing(cache: int, stream: int) -> None:
+    _check(lib().ftmoe_copy_missing(cache, stream))
+
+
+def ftmoe_expert_ffn(cache: int, d_x: int, bs: int, d_slots: int, d_weights: int, topk: int, d_y: int,
+                     stream: int) -> None:
+    _check(lib().ftmoe_expert_ffn(cache, d_x, bs, d_slots, d_weights, topk, d_y, stream))
+
+
+def ftmoe_set_copy_mode(cache: int, mode: int) -> None:
+    _check(lib().ftmoe_set_copy_mode(cache, mode))
+
+
+def ftmoe_cache_get_state(cache: int, h_owner: int, h_stamp: int, h_clock: int, stream: int) -> None:
+    _check(lib().ftmoe_cache_get_state(cache, h_owner, h_stamp, h_clock, stream))
+
+
+def ftmoe_cache_set_state(cache: int, h_owner: int, h_stamp: int, clock: int, stream: int) -> None:
+    _check(lib().ftmoe_cache_set_state(cache, h_owner, h_stamp, clock, stream))
+
+
+def ftmoe_get_miss_list(cache: int, h_ids: int, h_slots: int, h_m: int, stream: int) -> None:
+    _check(lib().ftmoe_get_miss_list(cache, h_ids, h_slots, h_m, stream))
+
+
+def ftmoe_get_device_status(cache: int, h_status: int, stream: int) -> None:
+    _check(lib().ftmoe_get_device_status(cache, h_status, stream))
+
+
+def ftmoe_h2d_stream_copy(d_dst: int, h_src: int, nbytes: int, stream: int) -> None:
+    _check(lib().ftmoe_h2d_stream_copy(d_dst, h_src, nbytes, stream))

@@ -88,6 +88,9 @@ class BankGeom:
 def bank_schema(cfg: Config) -> List[BankGeom]:
     """Per-expert bank geometry, in the schema order of the benchmark guide section 4.2."""
     H, I = cfg.H, cfg.I
+    if cfg.fmt == "raw":
+        # copy-only cache: one byte bank of H bytes per expert (tiny LRU/copy tests)
+        return [BankGeom("rows", "u8", 1, H)]
     if cfg.fmt == "bf16":
         down = BankGeom("down", "bf16", I, 2 * H) if cfg.down_rows_literal else BankGeom("down", "bf16", H, 2 * I)
         return [BankGeom("gate_up", "bf16", 2 * I, 2 * H), down]
@@ -190,6 +193,42 @@ def fill_bank(cfg: Config, b: int, out: np.ndarray, experts: Optional[Sequence[i
     else:
         with ThreadPoolExecutor(threads) as ex:
             list(ex.map(one, range(len(ids))))
+
+
+def fill_bank_device(cfg: Config, b: int, out, experts: Optional[Sequence[int]] = None,
+                     device: str = "cuda") -> None:
+    """Like :func:`fill_bank` but draws the values with torch's seeded Philox generator on
+    ``device`` and copies them into ``out`` (a torch uint8 tensor [n, bytes_b], normally
+    page-locked host memory). Same value distributions, different (but seeded) draws;
+    used for the multi-GiB banks, which the numpy path generates too slowly."""
+    import torch
+
+    geom = bank_schema(cfg)[b]
+    ids = list(range(cfg.E)) if experts is None else list(experts)
+    assert tuple(out.shape) == (len(ids), geom.bytes) and out.dtype == torch.uint8
+    gen = torch.Generator(device=device)
+    for i, e in enumerate(ids):
+        seed = int(np.random.SeedSequence([cfg.seed, cfg.index, _SEED_BANK, b, e, 0xD]).generate_state(1,
+                                                                                                      np.uint64)[0])
+        gen.manual_seed(seed)
+        n = geom.bytes
+        if geom.dtype == "u8":
+            t = torch.randint(0, 256, (n,), dtype=torch.uint8, device=device, generator=gen)
+        elif geom.dtype == "bf16":
+            t = (torch.randn(n // 2, device=device, generator=gen) * 0.02).to(torch.bfloat16).view(torch.uint8)
+        elif geom.dtype == "e4m3":
+            v = torch.randn(n, device=device, generator=gen).abs().clamp(max=448.0)
+            t = v.to(torch.float8_e4m3fn).view(torch.uint8)
+        elif geom.dtype == "f16":
+            K = cfg.H if geom.name.startswith("gate_up") else cfg.I
+            u = torch.rand(n // 2, device=device, generator=gen, dtype=torch.float64)
+            t = ((0.5 + u) / np.sqrt(8.5625 * K)).to(torch.float16).view(torch.uint8)
+        elif geom.dtype == "e8m0":
+            t = torch.randint(117, 121, (n,), dtype=torch.uint8, device=device, generator=gen)
+        else:
+            raise ValueError(geom.dtype)
+        out[i].copy_(t, non_blocking=True)
+    torch.cuda.synchronize()
 
 
 def make_banks(cfg: Config, experts: Optional[Sequence[int]] = None) -> List[np.ndarray]:

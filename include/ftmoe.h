@@ -1,0 +1,208 @@
+/*
+ * ftmoe — offloaded MoE expert slot cache for one GB300 (sm_103a).
+ *
+ * C-ABI of the per-layer decode step of an offloaded mixture-of-experts expert
+ * cache: expert weights live in page-locked host "banks"; a fixed pool of GPU
+ * slots caches them under one global LRU over the flat id space
+ * id = layer * E + expert. A decode step of one layer is
+ *
+ *   ftmoe_ensure_experts  -> dedup the routed ids, look them up, evict LRU slots
+ *                            for the misses (one kernel, no host sync);
+ *   ftmoe_copy_missing    -> copy every missed expert's bytes of every bank from
+ *                            the host banks into its new slot (one fused kernel);
+ *   ftmoe_expert_ffn      -> gate_up -> SiLU * up -> down over the resolved slots,
+ *                            combined with the router probabilities.
+ *
+ * Sources (FreeToken pages): the architecture deep-dive "深入FreeToken架构：从HTTP
+ * API到CUDA内核的本地MoE推理引擎全链路剖析", section 五 (expert banks per
+ * quantisation format, a global LRU expert cache), and the benchmark guide
+ * "FreeToken MoE 离线推理基准完全指南", sections 一 (hit experts compute from the
+ * slot cache, misses are copied over the host link), 4.1 (ensure_experts = LRU
+ * slot remap plus a gather of the bank rows), 4.2 (bank schemas; the cache is
+ * layout-agnostic and only moves rows), 4.3 (flat id space, prepared state,
+ * miss counts) and 4.4 (copy_MiB, per-layer source lists, a fused multi-bank
+ * copy with a per-bank path kept for A/B comparison).
+ *
+ * Conventions for every entry point:
+ *   - returns FTMOE_OK (0) or a negative FTMOE_ERR_* code; on error
+ *     ftmoe_last_error() gives a message (thread-local, valid until the next call
+ *     on the same thread);
+ *   - pointers named d_* are device pointers, h_* host pointers;
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream); work is enqueued on it and the call returns without waiting,
+ *     unless the entry point says it synchronises;
+ *   - errors found on the host return before anything is enqueued; errors found
+ *     on the device (an expert id out of range, more misses than free slots)
+ *     leave the cache state untouched, make the kernel write nothing else, and
+ *     are recorded in a sticky device status word read by
+ *     ftmoe_get_device_status. No kernel traps, asserts or spin-waits.
+ */
+#ifndef FTMOE_H
+#define FTMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define FTMOE_OK 0
+#define FTMOE_ERR_INVALID_ARG (-1) /* bad argument found on the host */
+#define FTMOE_ERR_CAPACITY (-2)    /* more distinct missing experts than evictable slots */
+#define FTMOE_ERR_ID_RANGE (-3)    /* a routed expert id outside [0, E) */
+#define FTMOE_ERR_CUDA (-4)        /* a CUDA runtime call failed */
+#define FTMOE_ERR_FORMAT (-5)      /* banks do not match the format's schema */
+#define FTMOE_ERR_STATE (-6)       /* inconsistent cache state, clock exhausted, call order */
+
+/* bank formats (schemas of the benchmark guide, section 4.2) */
+#define FTMOE_FMT_RAW 0   /* any banks; copy only, no FFN */
+#define FTMOE_FMT_BF16 1  /* banks: gate_up [2I, H] bf16, down [H, I] bf16 */
+#define FTMOE_FMT_NVFP4 2 /* banks: gate_up codes [2I, H/2] u8, scales [2I, H/16] e4m3,
+                             global [2I] f16, down codes [H, I/2], scales [H, I/16], global [H] */
+#define FTMOE_FMT_MXFP4 3 /* banks (transposed): gate_up blocks [H/2, 2I] u8, scales [H/32, 2I]
+                             e8m0, bias [2I] bf16, down blocks [I/2, H], scales [I/32, H], bias [H] */
+
+/* element types of a bank (informative; FFN formats check them against the schema) */
+#define FTMOE_DT_U8 0
+#define FTMOE_DT_BF16 1
+#define FTMOE_DT_F16 2
+#define FTMOE_DT_E4M3 3
+#define FTMOE_DT_E8M0 4
+
+/* copy_missing implementations (benchmark guide, section 4.4: the fused multi-bank
+ * copy is the main path; the per-bank path is kept for A/B comparison) */
+#define FTMOE_COPY_FUSED 0    /* one kernel for all banks (default) */
+#define FTMOE_COPY_PER_BANK 1 /* one kernel launch per bank */
+#define FTMOE_COPY_ENGINE 2   /* copy engines: reads the miss list back to the host
+                                 (synchronises the stream), then one cudaMemcpyAsync
+                                 per (miss, bank) */
+
+/* Limits of one cache. */
+#define FTMOE_MAX_BANKS 8
+#define FTMOE_MAX_EXPERTS 8192      /* E */
+#define FTMOE_MAX_SLOTS 8192        /* S */
+#define FTMOE_MAX_IDS_PER_CALL 65536 /* bs * topk of one ensure call */
+
+typedef struct ftmoe_cache ftmoe_cache_t;
+
+/* One bank of the per-expert weights.
+ *   rows, row_bytes : per-expert geometry as declared; one expert occupies
+ *                     rows * row_bytes bytes (a multiple of 16 is fastest);
+ *   host_src        : host array of L pointers; host_src[l] points at layer l's
+ *                     [E, rows * row_bytes] bytes in PAGE-LOCKED host memory
+ *                     (cudaHostAlloc, cudaHostRegister, torch pin_memory). NULL
+ *                     entries mark layers whose banks are not filled (ensure on
+ *                     such a layer fails with FTMOE_ERR_INVALID_ARG). Entries may
+ *                     alias. The array is copied at create; the memory it points
+ *                     at must outlive the cache and must not change while a copy
+ *                     reads it;
+ *   dev_slots       : device [S, rows * row_bytes] slot bank, caller-owned. */
+typedef struct {
+    const char *name;
+    int32_t dtype;
+    int64_t rows;
+    int64_t row_bytes;
+    const void *const *host_src;
+    void *dev_slots;
+} ftmoe_bank_spec;
+
+/* Bytes of device workspace a cache with these sizes needs (cache tables, miss
+ * list and FFN scratch for up to max_pairs = bs * topk routed pairs per FFN call;
+ * max_pairs = 0 disables the FFN). H and I are ignored for FTMOE_FMT_RAW. */
+int ftmoe_cache_workspace_bytes(int32_t format, int32_t num_banks, int32_t E, int32_t L,
+                                int32_t S, int32_t H, int32_t I, int32_t max_pairs,
+                                size_t *bytes);
+
+/* Create a cache over caller-owned banks and workspace (d_workspace: device,
+ * 256-byte aligned, at least ftmoe_cache_workspace_bytes). Maps every non-NULL host
+ * bank pointer for device access and initialises the state on `stream` to empty:
+ * every slot free, stamp 0, clock 0, status 0. format FTMOE_FMT_BF16/NVFP4/MXFP4
+ * checks the number of banks and each bank's per-expert bytes against the schema
+ * for (H, I) (FTMOE_ERR_FORMAT on mismatch; the declared rows/row_bytes may be any
+ * factorisation). The library owns only the returned host handle. */
+int ftmoe_cache_create(const ftmoe_bank_spec *banks, int32_t num_banks, int32_t format,
+                       int32_t E, int32_t L, int32_t S, int32_t H, int32_t I,
+                       int32_t max_pairs, void *d_workspace, size_t workspace_bytes,
+                       void *stream, ftmoe_cache_t **out);
+
+/* Destroy the host handle (the caller frees banks and workspace). NULL is a no-op. */
+int ftmoe_cache_destroy(ftmoe_cache_t *cache);
+
+/* ensure_experts (benchmark guide, section 4.1: "LRU slot remap"; architecture
+ * deep-dive, section 五: one global LRU for all layers) for the bs * topk routed
+ * local expert ids d_topk_ids[bs, topk] (int32, device) of `layer`:
+ *   1. clock += 1;
+ *   2. U = ascending distinct flat ids layer * E + id;
+ *   3. resident members of U (hits) get stamp = clock;
+ *   4. the misses, in ascending flat id, take the slots not hit in this call in
+ *      ascending (stamp, slot) order — least recently used first, lowest slot on
+ *      equal stamps; an evicted owner loses its slot, the new owner gets stamp =
+ *      clock;
+ *   5. d_slots_out[bs, topk] (int32, device) = slot of every routed position.
+ * The miss list (flat ids and slots, ascending id) stays on the device for
+ * ftmoe_copy_missing. One kernel, no host synchronisation. Device-detected errors
+ * (FTMOE_ERR_ID_RANGE, FTMOE_ERR_CAPACITY, clock exhausted = FTMOE_ERR_STATE) leave
+ * the state and clock untouched, fill d_slots_out with -1, empty the miss list and
+ * set the device status. bs * topk = 0 only advances the clock. */
+int ftmoe_ensure_experts(ftmoe_cache_t *cache, int32_t layer, const int32_t *d_topk_ids,
+                         int32_t bs, int32_t topk, int32_t *d_slots_out, void *stream);
+
+/* copy_missing (benchmark guide, sections 4.1, 4.2, 4.4): for every miss of the
+ * last ensure call and every bank b, copy the expert's rows * row_bytes bytes from
+ * host_src[layer] + expert * bytes to dev_slots + slot * bytes, unchanged. The
+ * miss count is read on the device: no host synchronisation (except in
+ * FTMOE_COPY_ENGINE mode). Must be stream-ordered after that ensure call;
+ * FTMOE_ERR_STATE if no ensure call was made yet. */
+int ftmoe_copy_missing(ftmoe_cache_t *cache, void *stream);
+
+/* Expert FFN over resolved slots (architecture deep-dive, section 五; benchmark
+ * guide, section 一: hit experts compute from the slot cache). For every token t
+ * and routed position j with slot s = d_slots[t, j]:
+ *     gu = W_gu[s] x_t (+ b_gu), h = silu(gu[0:I]) * gu[I:2I],
+ *     o  = W_d[s] h (+ b_d),     y_t = sum_j d_weights[t, j] * o
+ * with fp32 accumulation and one final round to bf16. d_x_bf16 [bs, H] bf16,
+ * d_slots [bs, topk] int32, d_weights [bs, topk] fp32, d_y_bf16 [bs, H] bf16 (all
+ * device). Slots must be in [0, S) and bs * topk <= max_pairs of create. Uses the
+ * FFN scratch of the cache workspace, so FFN calls on one cache must not overlap. */
+int ftmoe_expert_ffn(ftmoe_cache_t *cache, const void *d_x_bf16, int32_t bs,
+                     const int32_t *d_slots, const float *d_weights, int32_t topk,
+                     void *d_y_bf16, void *stream);
+
+/* Select the copy_missing implementation (FTMOE_COPY_*). */
+int ftmoe_set_copy_mode(ftmoe_cache_t *cache, int32_t mode);
+
+/* Read the state into host arrays h_owner[S] (flat id or -1), h_stamp[S], *h_clock.
+ * Synchronises the stream. */
+int ftmoe_cache_get_state(ftmoe_cache_t *cache, int32_t *h_owner, uint32_t *h_stamp,
+                          uint32_t *h_clock, void *stream);
+
+/* Replace the state from host arrays (owner flat ids in [-1, L*E), no id twice,
+ * stamps <= clock); id2slot is rebuilt on the device. FTMOE_ERR_STATE if the arrays
+ * are inconsistent. The host arrays may be reused when the call returns. */
+int ftmoe_cache_set_state(ftmoe_cache_t *cache, const int32_t *h_owner,
+                          const uint32_t *h_stamp, uint32_t clock, void *stream);
+
+/* Read the last ensure call's miss list into host arrays h_ids[], h_slots[] (room
+ * for min(E, S) entries) and *h_m. Synchronises the stream. */
+int ftmoe_get_miss_list(ftmoe_cache_t *cache, int32_t *h_ids, int32_t *h_slots,
+                        int32_t *h_m, void *stream);
+
+/* Read and clear the sticky device status word (FTMOE_OK or the first device error
+ * since the last read). Synchronises the stream. */
+int ftmoe_get_device_status(ftmoe_cache_t *cache, int32_t *h_status, void *stream);
+
+/* Linear copy of `bytes` from page-locked host memory to device memory by SM loads
+ * of the mapped host pointer (the copy kernel's data path without the cache; used to
+ * measure the host-to-device link ceiling, as the pinned-to-device copy ceiling of
+ * the benchmark guide, section 5.2). */
+int ftmoe_h2d_stream_copy(void *d_dst, const void *h_src, size_t bytes, void *stream);
+
+/* Message of the last failing call on this thread. */
+const char *ftmoe_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
