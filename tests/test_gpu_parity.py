@@ -153,6 +153,13 @@ def test_link_probe_copy():
 # ------------------------------------------------------------------ workload points
 
 
+def install_hits(cache, r):
+    """The prepared state's resident experts (slots 0..h-1) get their bytes."""
+    for i, e in enumerate(sorted(int(v) for v in r.hits)):
+        for b in range(cache.nb):
+            cache.slots[b][i].copy_(cache.host[b][0][e])
+
+
 def _run_point(cache, cfg, bs, mr, modes=(F.COPY_FUSED, F.COPY_PER_BANK, F.COPY_ENGINE), ffn_tokens=None):
     r = wl.make_route(cfg, bs, mr)
     orc = oracle.Cache(cfg.E, cfg.L, cfg.S, r.owner, r.stamp, r.clock)
@@ -161,6 +168,7 @@ def _run_point(cache, cfg, bs, mr, modes=(F.COPY_FUSED, F.COPY_PER_BANK, F.COPY_
     d_ids = to_dev(r.topk_ids)
     d_slots = torch.empty_like(d_ids)
     snapshots = []
+    install_hits(cache, r)
     for mode in modes:
         cache.set_state(r.owner, r.stamp, r.clock)
         for b in range(cache.nb):
