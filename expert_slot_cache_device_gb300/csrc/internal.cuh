@@ -82,4 +82,7 @@ struct FfnParams {
 };
 cudaError_t launch_ffn(const FfnParams &p, int num_sms, cudaStream_t st);
 
+// Record `msg` as the thread's last error message and return `code`.
+int report_error(int code, const char *msg);
+
 }  // namespace ftmoe

@@ -28,8 +28,9 @@ EXPORTS = [
     "ftmoe_cache_workspace_bytes", "ftmoe_cache_create", "ftmoe_cache_destroy", "ftmoe_ensure_experts",
     "ftmoe_copy_missing", "ftmoe_expert_ffn", "ftmoe_set_copy_mode", "ftmoe_cache_get_state",
     "ftmoe_cache_set_state", "ftmoe_get_miss_list", "ftmoe_get_device_status", "ftmoe_h2d_stream_copy",
-    "ftmoe_last_error",
+    "ftmoe_last_error", "ftmoe_expert_ffn_noalloc",
 ]
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class FtmoeError(RuntimeError):
@@ -75,6 +76,7 @@ def lib() -> ctypes.CDLL:
         "ftmoe_get_miss_list": [P, P, P, P, P],
         "ftmoe_get_device_status": [P, P, P],
         "ftmoe_h2d_stream_copy": [P, P, sz, P],
+        "ftmoe_expert_ffn_noalloc": [i32, ctypes.POINTER(P), i32, i32, i32, i32, P, i32, P, P, i32, P, P],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -165,3 +167,11 @@ def ftmoe_get_device_status(cache: int, h_status: int, stream: int) -> None:
 
 def ftmoe_h2d_stream_copy(d_dst: int, h_src: int, nbytes: int, stream: int) -> None:
     _check(lib().ftmoe_h2d_stream_copy(d_dst, h_src, nbytes, stream))
+
+
+def ftmoe_expert_ffn_noalloc(fmt: int, d_slot_banks, S: int, H: int, I: int, d_x: int, bs: int, d_slots: int,
+                             d_weights: int, topk: int, d_y: int, stream: int) -> None:
+    """Allocation-free expert FFN (fixed device scratch inside the library)."""
+    banks = (ctypes.c_void_p * len(d_slot_banks))(*d_slot_banks)
+    _check(lib().ftmoe_expert_ffn_noalloc(fmt, banks, len(d_slot_banks), S, H, I, d_x, bs, d_slots, d_weights,
+                                          topk, d_y, stream))

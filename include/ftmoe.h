@@ -199,6 +199,33 @@ int ftmoe_get_device_status(ftmoe_cache_t *cache, int32_t *h_status, void *strea
  * the benchmark guide, section 5.2). */
 int ftmoe_h2d_stream_copy(void *d_dst, const void *h_src, size_t bytes, void *stream);
 
+/* Bytes of the fixed device scratch behind ftmoe_expert_ffn_noalloc (16 MiB). */
+#define FTMOE_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* Expert FFN that allocates nothing. The FreeToken pages have no counterpart of this
+ * call; it is for callers that cannot call cudaMalloc: code embedded in a host runtime
+ * that already owns all of the GPU's memory (a serving engine that reserved HBM for its
+ * weights and KV cache up front, where an allocation would fail or break its
+ * accounting), and code on a latency-critical path that must not pay for
+ * cudaMalloc/cudaFree and the device synchronisation they can cause.
+ *
+ * Computes exactly what ftmoe_expert_ffn computes, without a cache handle: the caller
+ * passes its slot banks d_slot_banks[num_banks] (device [S, per-expert bytes] each, in
+ * the schema order of `format`, FTMOE_FMT_BF16/NVFP4/MXFP4), the activations, slots,
+ * router weights and the output, with the same layouts as ftmoe_expert_ffn. The
+ * routing tables and fp32 intermediates live in one file-scope device array of
+ * FTMOE_NOALLOC_SCRATCH_BYTES that every GPU loading the library reserves until the
+ * process exits; calls needing more (about bs * topk * (H + I) * 4 bytes) fail with
+ * FTMOE_ERR_INVALID_ARG. The first call on a device looks up that array's device
+ * address (cudaGetSymbolAddress); make that first call before any stream capture.
+ * All calls share the array and it keeps the previous call's contents: calls that
+ * overlap on the GPU race on it and must be serialised by the caller. A slot outside
+ * [0, S) leaves d_y_bf16 unwritten (there is no status to read back). */
+int ftmoe_expert_ffn_noalloc(int32_t format, const void *const *d_slot_banks, int32_t num_banks,
+                             int32_t S, int32_t H, int32_t I, const void *d_x_bf16, int32_t bs,
+                             const int32_t *d_slots, const float *d_weights, int32_t topk,
+                             void *d_y_bf16, void *stream);
+
 /* Message of the last failing call on this thread. */
 const char *ftmoe_last_error(void);
 
