@@ -7,15 +7,18 @@
 // take the slots not hit in this call in ascending (stamp, slot) order.
 //
 // One CTA of 1024 threads does the whole call so that the miss list is ready on
-// the device for the copy kernel without a host round trip:
+// the device for the copy kernel without a host round trip. Every independent
+// global load (ids, the layer's id2slot row, stamps, owners, clock) is issued
+// up front, so a call costs about one memory latency plus the sort:
 //   1. mark the routed local ids in a shared table over E (dedup; scanning the
 //      table in index order yields the distinct ids already ascending);
 //   2. probe id2slot for every distinct id; hits mark their slot as used;
 //   3. block-wide prefix sum over the miss flags gives every miss its rank;
-//   4. 64-bit keys (stamp << 32 | slot) of the unused slots are sorted in shared
-//      memory (bitonic network: shuffles inside a warp, shared memory across
-//      warps); the j-th smallest key is the j-th victim — exactly the
-//      lowest-(stamp, slot) rule;
+//   4. 64-bit keys (stamp << 32 | slot) of the unused slots are sorted by a
+//      bitonic network (one key per thread in registers for S <= 1024: warp
+//      shuffles for distances below 32, shared memory above; a shared-memory
+//      network for larger S); the j-th smallest key is the j-th victim —
+//      exactly the lowest-(stamp, slot) rule;
 //   5. tables are updated and every routed position gets its slot.
 // Errors (id out of range, clock exhausted, too many misses) write only the
 // status word, -1 slots and an empty miss list.
@@ -53,7 +56,7 @@ __device__ __forceinline__ int block_excl_scan(int flag, int *warp_tot, int *tot
 }
 
 // In-place ascending bitonic sort of n (power of two) keys in shared memory.
-__device__ void bitonic_sort(uint64_t *keys, int n) {
+__device__ void bitonic_sort_smem(uint64_t *keys, int n) {
     for (int k = 2; k <= n; k <<= 1) {
         for (int j = k >> 1; j > 0; j >>= 1) {
             for (int i = threadIdx.x; i < (n >> 1); i += blockDim.x) {
@@ -71,17 +74,57 @@ __device__ void bitonic_sort(uint64_t *keys, int n) {
     }
 }
 
+// Ascending bitonic sort of n <= blockDim.x keys, one per thread (thread i ends with
+// the i-th smallest). Exchange distances below 32 use warp shuffles, larger ones go
+// through shared memory `xbuf` (blockDim.x entries). Every thread must call it.
+__device__ uint64_t bitonic_sort_regs(uint64_t key, int n, uint64_t *xbuf) {
+    const int i = threadIdx.x;
+    for (int k = 2; k <= n; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            uint64_t other;
+            if (j >= 32) {
+                xbuf[i] = key;
+                __syncthreads();
+                other = xbuf[i ^ j];
+                __syncthreads();
+            } else {
+                other = __shfl_xor_sync(0xffffffffu, key, j);
+            }
+            const bool keep_min = ((i & j) == 0) == ((i & k) == 0);
+            key = keep_min ? (other < key ? other : key) : (other > key ? other : key);
+        }
+    }
+    return key;
+}
+
+constexpr int kPerThread = (FTMOE_MAX_SLOTS + kThreads - 1) / kThreads;  // 8 (also covers E)
+
 __global__ void __launch_bounds__(kThreads) ensure_kernel(EnsureParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
-    uint64_t *keys = reinterpret_cast<uint64_t *>(smem);          // [Spad]
-    int32_t *s_slot = reinterpret_cast<int32_t *>(keys + p.Spad);  // [E]: -2 absent, -1 miss, >=0 slot
+    const int xn = p.Spad > kThreads ? p.Spad : kThreads;
+    uint64_t *keys = reinterpret_cast<uint64_t *>(smem);          // [max(Spad, blockDim)]
+    int32_t *s_slot = reinterpret_cast<int32_t *>(keys + xn);      // [E]: -2 absent, -1 miss, >=0 slot
     int32_t *s_miss = s_slot + p.E;                               // [maxm] flat ids by rank
-    unsigned char *s_hit = reinterpret_cast<unsigned char *>(s_miss + p.maxm);  // [S]
+    int32_t *s_owner = s_miss + p.maxm;                           // [S]
+    unsigned char *s_hit = reinterpret_cast<unsigned char *>(s_owner + p.S);  // [S]
     __shared__ int warp_tot[32];
     __shared__ int s_bad_id, s_m, s_h, s_tmp;
 
     const int tid = threadIdx.x, nt = blockDim.x;
     const int E = p.E, S = p.S;
+    // Prologue: issue every independent global load before the first use, so the
+    // call pays about one memory latency instead of one per step.
+    const int32_t *row = p.t.id2slot + (int64_t)p.layer * E;
+    int32_t rowv[kPerThread];
+    uint32_t stampv[kPerThread];
+#pragma unroll
+    for (int k = 0; k < kPerThread; k++) {
+        const int e = tid + k * nt, s = tid + k * nt;
+        rowv[k] = e < E ? row[e] : -1;
+        stampv[k] = s < S ? p.t.stamp[s] : 0u;
+        if (s < S) s_owner[s] = p.t.owner[s];
+    }
+    const uint32_t clock = *p.t.clock;
     if (tid == 0) {
         s_bad_id = 0;
         s_h = 0;
@@ -98,26 +141,23 @@ __global__ void __launch_bounds__(kThreads) ensure_kernel(EnsureParams p) {
         else
             s_slot[id] = -1;
     }
-    const uint32_t clock = *p.t.clock;
     __syncthreads();
 
     int err = s_bad_id ? FTMOE_ERR_ID_RANGE : (clock == 0xFFFFFFFFu ? FTMOE_ERR_STATE : 0);
     if (err == 0) {
-        // 2. probe
-        const int32_t *row = p.t.id2slot + (int64_t)p.layer * E;
+        // 2. probe (the row was prefetched; each thread handles the ids it loaded)
         int hits = 0;
-        for (int e = tid; e < E; e += nt) {
-            if (s_slot[e] == -1) {
-                int s = row[e];
-                if (s >= 0) {
-                    s_slot[e] = s;
-                    s_hit[s] = 1;
-                    hits++;
-                }
+#pragma unroll
+        for (int k = 0; k < kPerThread; k++) {
+            const int e = tid + k * nt;
+            if (e < E && s_slot[e] == -1 && rowv[k] >= 0) {
+                s_slot[e] = rowv[k];
+                s_hit[rowv[k]] = 1;
+                hits++;
             }
         }
         if (hits) atomicAdd(&s_h, hits);
-        // 3. miss ranks in ascending id (s_slot writes above are read only by their writer)
+        // 3. miss ranks in ascending id (each s_slot entry is read by the thread that wrote it)
         int base = 0;
         for (int e0 = 0; e0 < E; e0 += nt) {
             int e = e0 + tid;
@@ -143,21 +183,31 @@ __global__ void __launch_bounds__(kThreads) ensure_kernel(EnsureParams p) {
 
     const int m = s_m;
     const uint32_t now = clock + 1;
-    // 4. victims: m smallest (stamp, slot) keys among the slots not hit in this call
+    // 4. victims: the m smallest (stamp, slot) keys among the slots not hit in this call
+    uint64_t victim = ~0ull;
     if (m > 0) {
-        for (int s = tid; s < p.Spad; s += nt)
-            keys[s] = (s < S && !s_hit[s]) ? ((uint64_t)p.t.stamp[s] << 32) | (uint32_t)s : ~0ull;
-        __syncthreads();
-        bitonic_sort(keys, p.Spad);
+        if (p.Spad <= nt) {
+            const uint64_t key = (tid < S && !s_hit[tid]) ? ((uint64_t)stampv[0] << 32) | (uint32_t)tid : ~0ull;
+            victim = bitonic_sort_regs(key, p.Spad, keys);
+        } else {
+#pragma unroll
+            for (int k = 0; k < kPerThread; k++) {
+                const int s = tid + k * nt;
+                if (s < p.Spad) keys[s] = (s < S && !s_hit[s]) ? ((uint64_t)stampv[k] << 32) | (uint32_t)s : ~0ull;
+            }
+            __syncthreads();
+            bitonic_sort_smem(keys, p.Spad);
+        }
     }
     // 5. update: hit stamps, then victims (hit and victim slots are disjoint; an
     //    evicted owner is never one of this call's misses, whose id2slot is -1)
     for (int s = tid; s < S; s += nt)
         if (s_hit[s]) p.t.stamp[s] = now;
     for (int j = tid; j < m; j += nt) {
-        int s = (int)(uint32_t)(keys[j] & 0xffffffffu);
+        const uint64_t key = p.Spad <= nt ? victim : keys[j];
+        int s = (int)(uint32_t)(key & 0xffffffffu);
         int f = s_miss[j];
-        int old = p.t.owner[s];
+        int old = s_owner[s];
         if (old >= 0) p.t.id2slot[old] = -1;
         p.t.owner[s] = f;
         p.t.id2slot[f] = s;
@@ -206,7 +256,8 @@ __global__ void scatter_owner_kernel(Tables t, int S) {
 }  // namespace
 
 size_t ensure_smem_bytes(int E, int S, int Spad, int maxm) {
-    size_t b = (size_t)Spad * 8 + (size_t)E * 4 + (size_t)maxm * 4 + (size_t)S;
+    const size_t xn = Spad > kThreads ? Spad : kThreads;
+    size_t b = xn * 8 + (size_t)E * 4 + (size_t)maxm * 4 + (size_t)S * 4 + (size_t)S;
     return (b + 15) & ~(size_t)15;
 }
 

@@ -27,13 +27,13 @@
 // decoded in registers (cvt e2m1x2 -> f16x2), the block scales are applied to
 // per-block partial sums, and all accumulation is fp32. Nothing is atomic, so
 // results are bitwise reproducible.
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
-
+#include "ffn_common.cuh"
 #include "internal.cuh"
 
 namespace ftmoe {
 namespace {
+
+using namespace ffn;
 
 constexpr int kThreads = 256;  // 8 warps
 constexpr int kRowsTgMax = 4;  // tokens per pass, row-major kernels
@@ -42,81 +42,6 @@ constexpr int kColsDnTgMax = 4;  // tokens per pass, transposed down kernel
 constexpr int kGuNeurons = 16; // gate_up rows kernel: neurons per CTA (2 per warp)
 constexpr int kDnRows = 32;    // down rows kernel: output rows per CTA
 constexpr int kColTile = 128;  // transposed kernels: columns per CTA (4 per lane)
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-__device__ __forceinline__ uint4 ldg_stream(const void *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
-__device__ __forceinline__ uint32_t ldg_stream32(const void *p) {
-    uint32_t v;
-    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
-    return v;
-}
-
-// Four bytes of packed e2m1 codes -> eight floats (low nibble of each byte first).
-__device__ __forceinline__ void e2m1x8(uint32_t w, float (&f)[8]) {
-    uint32_t h0, h1, h2, h3;
-    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-        : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
-        : "r"(w));
-    float2 a = __half22float2(*reinterpret_cast<__half2 *>(&h0));
-    float2 b = __half22float2(*reinterpret_cast<__half2 *>(&h1));
-    float2 c = __half22float2(*reinterpret_cast<__half2 *>(&h2));
-    float2 d = __half22float2(*reinterpret_cast<__half2 *>(&h3));
-    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
-    f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
-}
-
-// One byte of packed e2m1 codes -> two floats (low nibble first).
-__device__ __forceinline__ float2 e2m1x2(uint32_t byte) {
-    uint32_t h;
-    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-        "mov.b32 {b0, b1, b2, b3}, %1;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t}"
-        : "=r"(h)
-        : "r"(byte));
-    return __half22float2(*reinterpret_cast<__half2 *>(&h));
-}
-
-// OCP e4m3fn byte -> float: bias 7, 3 mantissa bits, subnormals, S.1111.111 = NaN.
-__device__ __forceinline__ float e4m3_to_f(uint32_t b) {
-    const uint32_t sgn = (b & 0x80u) << 24, ex = (b >> 3) & 15u, man = b & 7u;
-    float v = ex ? __uint_as_float(((ex + 120u) << 23) | (man << 20)) : (float)man * 0.001953125f;
-    if (ex == 15u && man == 7u) v = __uint_as_float(0x7fc00000u);
-    return __uint_as_float(__float_as_uint(v) | sgn);
-}
-
-// e8m0 byte -> 2^(b - 127); 0xFF is NaN.
-__device__ __forceinline__ float e8m0_to_f(uint32_t b) {
-    b &= 0xffu;
-    if (b == 0xffu) return __uint_as_float(0x7fc00000u);
-    return b == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(b << 23);
-}
-
-__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
-
-__device__ __forceinline__ void unpack_bf16x8(uint4 v, float (&f)[8]) {
-    f[0] = bf_lo(v.x); f[1] = bf_hi(v.x); f[2] = bf_lo(v.y); f[3] = bf_hi(v.y);
-    f[4] = bf_lo(v.z); f[5] = bf_hi(v.z); f[6] = bf_lo(v.w); f[7] = bf_hi(v.w);
-}
 
 // ------------------------------------------------------------------------ route
 
@@ -152,6 +77,7 @@ __global__ void __launch_bounds__(1024) ffn_route_kernel(FfnParams p) {
     __shared__ int warp_tot[32];
     __shared__ int s_bad, s_tot_u, s_tot_c;
     const int tid = threadIdx.x, nt = blockDim.x;
+    asm volatile("griddepcontrol.launch_dependents;" :::);
     if (tid == 0) s_bad = 0;
     for (int s = tid; s < p.S; s += nt) cnt[s] = 0;
     __syncthreads();
@@ -700,6 +626,7 @@ __global__ void __launch_bounds__(kThreads, 2) ffn_down_cols_kernel(FfnParams p,
 // --------------------------------------------------------------------- combine
 
 __global__ void __launch_bounds__(kThreads) ffn_combine_kernel(FfnParams p) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // o comes from the down kernel
     if (*p.s.n_unique < 0) return;  // a bad slot: y is left untouched
     const int t = blockIdx.y;
     const int n4 = blockIdx.x * kThreads + threadIdx.x;  // 4 outputs per thread
@@ -742,7 +669,6 @@ cudaError_t launch_dyn(K kernel, int grid, size_t smem, cudaStream_t st, const F
 }  // namespace
 
 cudaError_t launch_ffn(const FfnParams &p, int num_sms, cudaStream_t st) {
-    (void)num_sms;
     cudaError_t e;
     size_t route_smem = (size_t)p.S * sizeof(int);
     if (route_smem > 48 * 1024) {
@@ -754,7 +680,11 @@ cudaError_t launch_ffn(const FfnParams &p, int num_sms, cudaStream_t st) {
 
     const int umax = p.P < p.S ? p.P : p.S;  // distinct slots at most
     const size_t budget = 64 * 1024;
-    if (p.fmt == FTMOE_FMT_BF16 || p.fmt == FTMOE_FMT_NVFP4) {
+    bool pdl_combine = false;
+    if (num_sms > 0 && ffn_rows_tma_supported(p)) {
+        if ((e = launch_ffn_rows_tma(p, num_sms, st)) != cudaSuccess) return e;
+        pdl_combine = true;
+    } else if (p.fmt == FTMOE_FMT_BF16 || p.fmt == FTMOE_FMT_NVFP4) {
         const int tiles_gu = (p.I + kGuNeurons - 1) / kGuNeurons;
         const int tg_gu = pick_tg(kRowsTgMax, (size_t)p.H * 2, 0, budget);
         const int tiles_dn = (p.H + kDnRows - 1) / kDnRows;
@@ -787,9 +717,16 @@ cudaError_t launch_ffn(const FfnParams &p, int num_sms, cudaStream_t st) {
                        tiles_dn, tg_dn);
         if (e != cudaSuccess) return e;
     }
-    dim3 cg((p.H / 4 + kThreads - 1) / kThreads, p.bs);
-    ffn_combine_kernel<<<cg, kThreads, 0, st>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((p.H / 4 + kThreads - 1) / kThreads, p.bs);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_combine ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, ffn_combine_kernel, p);
 }
 
 }  // namespace ftmoe

@@ -1,0 +1,503 @@
+// Row-major expert FFN phases (bf16 and nvfp4 banks) as a persistent,
+// warp-specialised bulk-copy pipeline.
+//
+// Decode batches make the FFN a grouped GEMV that must stream every used expert's
+// weights from HBM exactly once. Here each CTA owns a contiguous range of work items
+// (distinct slot u, tile of R output rows), so neighbouring CTAs read neighbouring
+// rows. One producer thread fills a ring of shared-memory stages with 1-D bulk
+// asynchronous copies (cp.async.bulk, completion counted on an mbarrier): the item's
+// weight rows (gate and up rows of R neurons, or R down rows, plus the nvfp4 block
+// scales) and the token vectors the item needs (bf16 activations for gate_up, fp32
+// h rows for down). It also writes a small stage header (slot, rows, tokens). Eight
+// consumer warps wait on the stage's mbarrier, compute from shared memory (a warp
+// per row, lanes over 16-byte chunks, warp-shuffle reductions, fp32 accumulation,
+// nvfp4 decoded in registers) and release the stage. Several stages stay in flight
+// per SM, so the HBM stream never waits on a CTA's start-up latency; weight copies
+// carry an L2 evict-first policy because they are read once.
+//
+// The kernels are chained with programmatic dependent launch: gate_up waits for the
+// routing kernel, down's producer starts streaming its weights while gate_up drains
+// and waits only before it copies the h rows gate_up writes.
+//
+// Every mbarrier wait is bounded: on expiry the waiting thread records
+// FTMOE_ERR_STATE in the status word and leaves, and the producer waits (again
+// bounded) for its own copies in flight before it exits.
+#include "ffn_common.cuh"
+#include "internal.cuh"
+
+namespace ftmoe {
+namespace {
+
+using namespace ffn;
+
+constexpr int kConsumerWarps = 8;
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kTmaThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMaxStages = 4;
+constexpr int kMaxTok = 4;  // tokens per stage
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any healthy wait
+
+enum { kGateUp = 0, kDown = 1 };
+
+struct StageHdr {
+    int32_t slot, n0, rows, ntok, done, pad0, pad1, pad2;
+    int32_t pairs[kMaxTok];
+    int32_t pad3[4];
+};
+
+struct TmaCfg {
+    int32_t R;           // rows (gate_up: neurons) per item
+    int32_t tiles;       // items per distinct slot
+    int32_t stages;
+    int32_t stage_bytes;
+    int32_t tok_off;     // offset of the token vectors inside a stage
+    int32_t tok_bytes;   // bytes of one token vector
+    int32_t tg;          // tokens per stage (<= kMaxTok)
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait for the phase with the given parity; false if the limit expired.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    const uint32_t a = smem_u32(bar);
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 0;; i++) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(a), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if ((i & 255) == 255 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                         uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s_plain(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ uint64_t evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
+// Bytes of the weight segments of an item with `rows` rows (R rows reserve the layout).
+template <int FMT, int PHASE>
+struct Seg {
+    // per-row bytes of the code/weight matrix and of the scale matrix
+    __device__ __host__ static int64_t wrow(int H, int I) {
+        const int64_t K = PHASE == kGateUp ? H : I;
+        return FMT == FTMOE_FMT_BF16 ? 2 * K : K / 2;
+    }
+    __device__ __host__ static int64_t srow(int H, int I) {
+        const int64_t K = PHASE == kGateUp ? H : I;
+        return FMT == FTMOE_FMT_BF16 ? 0 : K / 16;
+    }
+    static constexpr int mats = PHASE == kGateUp ? 2 : 1;  // gate + up, or down
+    __device__ __host__ static int64_t bytes(int rows, int H, int I) {
+        return (int64_t)mats * rows * (wrow(H, I) + srow(H, I));
+    }
+};
+
+// ---------------------------------------------------------------- consumers
+
+template <int FMT, int NT>
+__device__ __forceinline__ void gu_consume(const FfnParams &p, const TmaCfg &c, const unsigned char *st,
+                                           const StageHdr &h) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H = p.H, I = p.I, R = c.R;
+    const int64_t wr = Seg<FMT, kGateUp>::wrow(H, I), sr = Seg<FMT, kGateUp>::srow(H, I);
+    const uint4 *xs = reinterpret_cast<const uint4 *>(st + c.tok_off);
+    const int nxv = H >> 3;  // 16-byte vectors per token (8 bf16)
+    for (int j = warp; j < h.rows; j += kConsumerWarps) {
+        const int n = h.n0 + j;
+        float g[NT], u[NT];
+#pragma unroll
+        for (int t = 0; t < NT; t++) g[t] = u[t] = 0.f;
+        float gg = 1.f, gu = 1.f;
+        if (FMT == FTMOE_FMT_NVFP4) {  // per-row globals: plain loads issued early
+            const unsigned char *gl = p.bank[2] + (int64_t)h.slot * p.bank_bytes[2];
+            gg = __half2float(*reinterpret_cast<const __half *>(gl + 2 * (int64_t)n));
+            gu = __half2float(*reinterpret_cast<const __half *>(gl + 2 * ((int64_t)I + n)));
+        }
+        if (FMT == FTMOE_FMT_BF16) {
+            const uint4 *wg = reinterpret_cast<const uint4 *>(st + j * wr);
+            const uint4 *wu = reinterpret_cast<const uint4 *>(st + (R + j) * wr);
+            const int nch = H >> 3;
+#pragma unroll 2
+            for (int ch = lane; ch < nch; ch += 32) {
+                float fa[8], fb[8];
+                unpack_bf16x8(wg[ch], fa);
+                unpack_bf16x8(wu[ch], fb);
+#pragma unroll
+                for (int t = 0; t < NT; t++) {
+                    float fx[8];
+                    unpack_bf16x8(xs[t * nxv + ch], fx);
+#pragma unroll
+                    for (int i = 0; i < 8; i++) {
+                        g[t] = fmaf(fa[i], fx[i], g[t]);
+                        u[t] = fmaf(fb[i], fx[i], u[t]);
+                    }
+                }
+            }
+        } else {
+            // lane step = one 32-bit word of codes (8 consecutive k, inside one 16-block):
+            // code, scale and x reads are contiguous (or broadcast) across lanes
+            const uint32_t *cg = reinterpret_cast<const uint32_t *>(st + j * wr);
+            const uint32_t *cu = reinterpret_cast<const uint32_t *>(st + (R + j) * wr);
+            const unsigned char *sg = st + 2 * R * wr + j * sr, *su = st + 2 * R * wr + (R + j) * sr;
+            const int nw = H >> 3;
+#pragma unroll 2
+            for (int w = lane; w < nw; w += 32) {
+                float fa[8], fb[8];
+                e2m1x8(cg[w], fa);
+                e2m1x8(cu[w], fb);
+                const float scg = e4m3_to_f(sg[w >> 1]), scu = e4m3_to_f(su[w >> 1]);
+#pragma unroll
+                for (int t = 0; t < NT; t++) {
+                    float fx[8];
+                    unpack_bf16x8(xs[t * nxv + w], fx);
+                    float pg = 0.f, pu = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 8; i++) {
+                        pg = fmaf(fa[i], fx[i], pg);
+                        pu = fmaf(fb[i], fx[i], pu);
+                    }
+                    g[t] = fmaf(pg, scg, g[t]);
+                    u[t] = fmaf(pu, scu, u[t]);
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < NT; t++) {
+            const float gs = warp_sum(g[t]) * gg, us = warp_sum(u[t]) * gu;
+            if (lane == t) p.s.h[(int64_t)h.pairs[t] * I + n] = silu(gs) * us;
+        }
+    }
+}
+
+template <int FMT, int NT>
+__device__ __forceinline__ void dn_consume(const FfnParams &p, const TmaCfg &c, const unsigned char *st,
+                                           const StageHdr &h) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H = p.H, I = p.I, R = c.R;
+    const int64_t wr = Seg<FMT, kDown>::wrow(H, I), sr = Seg<FMT, kDown>::srow(H, I);
+    const float4 *hs = reinterpret_cast<const float4 *>(st + c.tok_off);
+    const int nh4 = I >> 2;
+    constexpr int RR = 4;  // rows sharing each h read
+    for (int j0 = warp * RR; j0 < h.rows; j0 += kConsumerWarps * RR) {
+        const int nr = h.rows - j0 < RR ? h.rows - j0 : RR;
+        float o[RR][NT];
+#pragma unroll
+        for (int r = 0; r < RR; r++)
+#pragma unroll
+            for (int t = 0; t < NT; t++) o[r][t] = 0.f;
+        if (FMT == FTMOE_FMT_BF16) {
+            // lane step = 4 consecutive k: 8-byte weight reads and 16-byte h reads are
+            // contiguous across lanes (no bank conflicts)
+            for (int q = lane; q < nh4; q += 32) {
+                float fa[RR][4];
+#pragma unroll
+                for (int r = 0; r < RR; r++) {
+                    const int jr = r < nr ? j0 + r : j0;
+                    const uint2 v = *reinterpret_cast<const uint2 *>(st + jr * wr + 8 * q);
+                    fa[r][0] = bf_lo(v.x); fa[r][1] = bf_hi(v.x); fa[r][2] = bf_lo(v.y); fa[r][3] = bf_hi(v.y);
+                }
+#pragma unroll
+                for (int t = 0; t < NT; t++) {
+                    const float4 hv = hs[t * nh4 + q];
+#pragma unroll
+                    for (int r = 0; r < RR; r++) {
+                        o[r][t] = fmaf(fa[r][0], hv.x, o[r][t]);
+                        o[r][t] = fmaf(fa[r][1], hv.y, o[r][t]);
+                        o[r][t] = fmaf(fa[r][2], hv.z, o[r][t]);
+                        o[r][t] = fmaf(fa[r][3], hv.w, o[r][t]);
+                    }
+                }
+            }
+        } else {
+            // lane step = one 32-bit word of codes (8 consecutive k inside one 16-block)
+            const int nw = I >> 3;
+            for (int w = lane; w < nw; w += 32) {
+                float fa[RR][8], sc[RR];
+#pragma unroll
+                for (int r = 0; r < RR; r++) {
+                    const int jr = r < nr ? j0 + r : j0;
+                    e2m1x8(*reinterpret_cast<const uint32_t *>(st + jr * wr + 4 * w), fa[r]);
+                    sc[r] = e4m3_to_f(st[R * wr + jr * sr + (w >> 1)]);
+                }
+#pragma unroll
+                for (int t = 0; t < NT; t++) {
+                    const float4 h0 = hs[t * nh4 + 2 * w], h1 = hs[t * nh4 + 2 * w + 1];
+                    const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+#pragma unroll
+                    for (int r = 0; r < RR; r++) {
+                        float part = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 8; i++) part = fmaf(fa[r][i], hv[i], part);
+                        o[r][t] = fmaf(part, sc[r], o[r][t]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < RR; r++) {
+            if (r >= nr) break;
+            const int n = h.n0 + j0 + r;
+            float gl = 1.f;
+            if (FMT == FTMOE_FMT_NVFP4)
+                gl = __half2float(*reinterpret_cast<const __half *>(p.bank[5] + (int64_t)h.slot * p.bank_bytes[5] +
+                                                                    2 * (int64_t)n));
+#pragma unroll
+            for (int t = 0; t < NT; t++) {
+                const float v = warp_sum(o[r][t]) * gl;
+                if (lane == t) p.s.o[(int64_t)h.pairs[t] * H + n] = v;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- kernel
+
+template <int FMT, int PHASE>
+__global__ void __launch_bounds__(kTmaThreads, 1) ffn_rows_tma_kernel(FfnParams p, TmaCfg c) {
+    extern __shared__ __align__(128) unsigned char sm[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm);
+    uint64_t *empty = full + kMaxStages;
+    StageHdr *hdr = reinterpret_cast<StageHdr *>(sm + 128);
+    unsigned char *stage0 = sm + 128 + kMaxStages * sizeof(StageHdr);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < c.stages; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (PHASE == kGateUp) griddep_wait();  // routing tables come from the previous kernel
+    griddep_launch();
+
+    if (warp == kProducerWarp) {
+        if (lane != 0) return;
+        // Work items [first, last) of this CTA.
+        const int nu = *p.s.n_unique;
+        const int items = nu > 0 ? nu * c.tiles : 0;
+        const int first = (int)((int64_t)blockIdx.x * items / gridDim.x);
+        const int last = (int)((int64_t)(blockIdx.x + 1) * items / gridDim.x);
+        const uint64_t pol = evict_first_policy();
+        const int H = p.H, I = p.I, R = c.R;
+        const int nout = PHASE == kGateUp ? I : H;
+        const int64_t wr = Seg<FMT, PHASE>::wrow(H, I), sr = Seg<FMT, PHASE>::srow(H, I);
+        bool waited = PHASE == kGateUp, ok = true;
+        int issued = 0;
+        for (int it = first; it < last && ok; it++) {
+            const int u = it / c.tiles, tile = it - u * c.tiles;
+            int slot = p.s.uslot[u];
+            slot = slot < 0 ? 0 : (slot >= p.S ? p.S - 1 : slot);
+            const int cnt = p.s.ucnt[u], off = p.s.uoff[u];
+            const int n0 = tile * R, rows = nout - n0 < R ? nout - n0 : R;
+            for (int g0 = 0; g0 < cnt && ok; g0 += c.tg) {
+                const int ntok = cnt - g0 < c.tg ? cnt - g0 : c.tg;
+                const int s = issued % c.stages;
+                const uint32_t ph = (issued / c.stages) & 1;
+                if (!mbar_wait(&empty[s], ph ^ 1)) {
+                    ok = false;
+                    break;
+                }
+                StageHdr &hh = hdr[s];
+                hh.slot = slot; hh.n0 = n0; hh.rows = rows; hh.ntok = ntok; hh.done = 0;
+                for (int i = 0; i < ntok; i++) hh.pairs[i] = p.s.upairs[off + g0 + i];
+                const uint32_t wbytes = (uint32_t)Seg<FMT, PHASE>::bytes(rows, H, I);
+                mbar_expect_tx(&full[s], wbytes + (uint32_t)(ntok * c.tok_bytes));
+                unsigned char *st = stage0 + (size_t)s * c.stage_bytes;
+                if (PHASE == kGateUp) {
+                    const unsigned char *wb = p.bank[0] + (int64_t)slot * p.bank_bytes[0];
+                    bulk_g2s(st, wb + n0 * wr, (uint32_t)(rows * wr), &full[s], pol);
+                    bulk_g2s(st + R * wr, wb + ((int64_t)I + n0) * wr, (uint32_t)(rows * wr), &full[s], pol);
+                    if (FMT == FTMOE_FMT_NVFP4) {
+                        const unsigned char *sb = p.bank[1] + (int64_t)slot * p.bank_bytes[1];
+                        bulk_g2s(st + 2 * R * wr, sb + n0 * sr, (uint32_t)(rows * sr), &full[s], pol);
+                        bulk_g2s(st + 2 * R * wr + R * sr, sb + ((int64_t)I + n0) * sr, (uint32_t)(rows * sr),
+                                 &full[s], pol);
+                    }
+                } else {
+                    const int wb_i = FMT == FTMOE_FMT_BF16 ? 1 : 3;
+                    const unsigned char *wb = p.bank[wb_i] + (int64_t)slot * p.bank_bytes[wb_i];
+                    bulk_g2s(st, wb + n0 * wr, (uint32_t)(rows * wr), &full[s], pol);
+                    if (FMT == FTMOE_FMT_NVFP4) {
+                        const unsigned char *sb = p.bank[4] + (int64_t)slot * p.bank_bytes[4];
+                        bulk_g2s(st + R * wr, sb + n0 * sr, (uint32_t)(rows * sr), &full[s], pol);
+                    }
+                }
+                if (!waited) {  // h rows are written by the gate_up kernel
+                    griddep_wait();
+                    waited = true;
+                }
+                for (int i = 0; i < ntok; i++) {
+                    const int q = hh.pairs[i];
+                    const void *src = PHASE == kGateUp
+                                          ? static_cast<const void *>(p.x + (int64_t)(q / p.topk) * H)
+                                          : static_cast<const void *>(p.s.h + (int64_t)q * I);
+                    bulk_g2s_plain(st + c.tok_off + i * c.tok_bytes, src, (uint32_t)c.tok_bytes, &full[s]);
+                }
+                issued++;
+            }
+        }
+        if (ok) {  // end marker
+            const int s = issued % c.stages;
+            if (mbar_wait(&empty[s], ((issued / c.stages) & 1) ^ 1)) {
+                hdr[s].done = 1;
+                mbar_arrive(&full[s]);
+            } else {
+                ok = false;
+            }
+        }
+        if (!ok) {
+            atomicCAS(p.status, 0, FTMOE_ERR_STATE);
+            // wait (bounded) until the copies already issued have landed
+            for (int j = issued - c.stages < 0 ? 0 : issued - c.stages; j < issued; j++)
+                mbar_wait(&full[j % c.stages], (j / c.stages) & 1);
+        }
+        return;
+    }
+
+    // consumers
+    for (int k = 0;; k++) {
+        const int s = k % c.stages;
+        if (!mbar_wait(&full[s], (k / c.stages) & 1)) {
+            if (lane == 0) atomicCAS(p.status, 0, FTMOE_ERR_STATE);
+            return;
+        }
+        const StageHdr h = hdr[s];
+        if (h.done) return;
+        const unsigned char *st = stage0 + (size_t)s * c.stage_bytes;
+        if (PHASE == kGateUp) {
+            switch (h.ntok) {
+                case 1: gu_consume<FMT, 1>(p, c, st, h); break;
+                case 2: gu_consume<FMT, 2>(p, c, st, h); break;
+                case 3: gu_consume<FMT, 3>(p, c, st, h); break;
+                default: gu_consume<FMT, 4>(p, c, st, h); break;
+            }
+        } else {
+            switch (h.ntok) {
+                case 1: dn_consume<FMT, 1>(p, c, st, h); break;
+                case 2: dn_consume<FMT, 2>(p, c, st, h); break;
+                case 3: dn_consume<FMT, 3>(p, c, st, h); break;
+                default: dn_consume<FMT, 4>(p, c, st, h); break;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+}
+
+constexpr size_t kSmemHeader = 128 + kMaxStages * sizeof(StageHdr);
+constexpr size_t kSmemCap = 200 * 1024;
+
+template <int FMT, int PHASE>
+bool make_cfg(const FfnParams &p, TmaCfg &c) {
+    const int H = p.H, I = p.I;
+    const int nout = PHASE == kGateUp ? I : H;
+    c.tok_bytes = PHASE == kGateUp ? 2 * H : 4 * I;
+    const int rmax = PHASE == kGateUp ? 16 : 32;
+    for (int tg = kMaxTok; tg >= 1; tg >>= 1) {
+        for (int R = rmax; R >= 1; R >>= 1) {
+            const int64_t wb = Seg<FMT, PHASE>::bytes(R, H, I);
+            if (wb > 72 * 1024) continue;
+            const int64_t stage = ((wb + 127) & ~(int64_t)127) + (int64_t)tg * c.tok_bytes;
+            const int64_t stages = (int64_t)((kSmemCap - kSmemHeader) / (size_t)stage);
+            if (stages < 2) continue;
+            c.R = R;
+            c.tiles = (nout + R - 1) / R;
+            c.tg = tg;
+            c.tok_off = (int32_t)((wb + 127) & ~(int64_t)127);
+            c.stage_bytes = (int32_t)((stage + 127) & ~(int64_t)127);
+            c.stages = stages > kMaxStages ? kMaxStages : (int32_t)stages;
+            return true;
+        }
+    }
+    return false;
+}
+
+template <int FMT, int PHASE>
+cudaError_t launch_one(const FfnParams &p, int num_sms, cudaStream_t st) {
+    TmaCfg c;
+    if (!make_cfg<FMT, PHASE>(p, c)) return cudaErrorInvalidValue;
+    const size_t smem = kSmemHeader + (size_t)c.stages * c.stage_bytes;
+    auto kern = ffn_rows_tma_kernel<FMT, PHASE>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms);
+    cfg.blockDim = dim3(kTmaThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p, c);
+}
+
+}  // namespace
+
+bool ffn_rows_tma_supported(const FfnParams &p) {
+    if (p.fmt == FTMOE_FMT_BF16) return p.H % 8 == 0 && p.I % 8 == 0;
+    if (p.fmt == FTMOE_FMT_NVFP4) return p.H % 256 == 0 && p.I % 256 == 0;
+    return false;
+}
+
+cudaError_t launch_ffn_rows_tma(const FfnParams &p, int num_sms, cudaStream_t st) {
+    cudaError_t e;
+    if (p.fmt == FTMOE_FMT_BF16) {
+        if ((e = launch_one<FTMOE_FMT_BF16, kGateUp>(p, num_sms, st)) != cudaSuccess) return e;
+        return launch_one<FTMOE_FMT_BF16, kDown>(p, num_sms, st);
+    }
+    if ((e = launch_one<FTMOE_FMT_NVFP4, kGateUp>(p, num_sms, st)) != cudaSuccess) return e;
+    return launch_one<FTMOE_FMT_NVFP4, kDown>(p, num_sms, st);
+}
+
+}  // namespace ftmoe

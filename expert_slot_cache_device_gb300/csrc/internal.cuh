@@ -81,6 +81,9 @@ struct FfnParams {
     int32_t fmt, H, I, S, bs, topk, P;
 };
 cudaError_t launch_ffn(const FfnParams &p, int num_sms, cudaStream_t st);
+// Persistent bulk-copy pipeline for the row-major formats (bf16; nvfp4 with H, I multiples of 256).
+bool ffn_rows_tma_supported(const FfnParams &p);
+cudaError_t launch_ffn_rows_tma(const FfnParams &p, int num_sms, cudaStream_t st);
 
 // Record `msg` as the thread's last error message and return `code`.
 int report_error(int code, const char *msg);
