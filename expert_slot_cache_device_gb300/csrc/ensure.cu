@@ -79,15 +79,16 @@ __device__ void bitonic_sort_smem(uint64_t *keys, int n) {
 // through shared memory `xbuf` (blockDim.x entries). Every thread must call it.
 __device__ uint64_t bitonic_sort_regs(uint64_t key, int n, uint64_t *xbuf) {
     const int i = threadIdx.x;
+    const bool active = (i & ~31) < n;  // whole warps past the sort width only join the barriers
     for (int k = 2; k <= n; k <<= 1) {
         for (int j = k >> 1; j > 0; j >>= 1) {
-            uint64_t other;
+            uint64_t other = key;
             if (j >= 32) {
-                xbuf[i] = key;
+                if (active) xbuf[i] = key;
                 __syncthreads();
-                other = xbuf[i ^ j];
+                if (active) other = xbuf[i ^ j];
                 __syncthreads();
-            } else {
+            } else if (active) {
                 other = __shfl_xor_sync(0xffffffffu, key, j);
             }
             const bool keep_min = ((i & j) == 0) == ((i & k) == 0);

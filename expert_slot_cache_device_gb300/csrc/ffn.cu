@@ -633,14 +633,30 @@ __global__ void __launch_bounds__(kThreads) ffn_combine_kernel(FfnParams p) {
     const int H = p.H;
     if (4 * n4 >= H) return;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < p.topk; j++) {
-        const int q = t * p.topk + j;
-        const float w = p.weights[q];
-        const float4 o = reinterpret_cast<const float4 *>(p.s.o + (int64_t)q * H)[n4];
-        acc.x = fmaf(w, o.x, acc.x);
-        acc.y = fmaf(w, o.y, acc.y);
-        acc.z = fmaf(w, o.z, acc.z);
-        acc.w = fmaf(w, o.w, acc.w);
+    const float4 *o4 = reinterpret_cast<const float4 *>(p.s.o);
+    const int64_t h4 = H >> 2;
+    // load a group of routed positions before using any of them (independent L2 reads)
+    for (int j0 = 0; j0 < p.topk; j0 += 8) {
+        float4 ov[8];
+        float wv[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; jj++) {
+            const int j = j0 + jj;
+            if (j < p.topk) {
+                const int q = t * p.topk + j;
+                wv[jj] = p.weights[q];
+                ov[jj] = o4[(int64_t)q * h4 + n4];
+            }
+        }
+#pragma unroll
+        for (int jj = 0; jj < 8; jj++) {
+            if (j0 + jj < p.topk) {
+                acc.x = fmaf(wv[jj], ov[jj].x, acc.x);
+                acc.y = fmaf(wv[jj], ov[jj].y, acc.y);
+                acc.z = fmaf(wv[jj], ov[jj].z, acc.z);
+                acc.w = fmaf(wv[jj], ov[jj].w, acc.w);
+            }
+        }
     }
     __nv_bfloat16 b0 = __float2bfloat16_rn(acc.x), b1 = __float2bfloat16_rn(acc.y);
     __nv_bfloat16 b2 = __float2bfloat16_rn(acc.z), b3 = __float2bfloat16_rn(acc.w);

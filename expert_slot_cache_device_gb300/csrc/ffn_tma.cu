@@ -442,20 +442,25 @@ bool make_cfg(const FfnParams &p, TmaCfg &c) {
     const int nout = PHASE == kGateUp ? I : H;
     c.tok_bytes = PHASE == kGateUp ? 2 * H : 4 * I;
     const int rmax = PHASE == kGateUp ? 16 : 32;
-    for (int tg = kMaxTok; tg >= 1; tg >>= 1) {
-        for (int R = rmax; R >= 1; R >>= 1) {
-            const int64_t wb = Seg<FMT, PHASE>::bytes(R, H, I);
-            if (wb > 72 * 1024) continue;
-            const int64_t stage = ((wb + 127) & ~(int64_t)127) + (int64_t)tg * c.tok_bytes;
-            const int64_t stages = (int64_t)((kSmemCap - kSmemHeader) / (size_t)stage);
-            if (stages < 2) continue;
-            c.R = R;
-            c.tiles = (nout + R - 1) / R;
-            c.tg = tg;
-            c.tok_off = (int32_t)((wb + 127) & ~(int64_t)127);
-            c.stage_bytes = (int32_t)((stage + 127) & ~(int64_t)127);
-            c.stages = stages > kMaxStages ? kMaxStages : (int32_t)stages;
-            return true;
+    // Prefer enough rows per item to keep all consumer warps busy (gate_up: one neuron per
+    // warp; down: four rows per warp), then as many token slots as fit.
+    const int rmin_busy = PHASE == kGateUp ? kConsumerWarps : 4 * kConsumerWarps;
+    for (int pass = 0; pass < 2; pass++) {
+        for (int tg = kMaxTok; tg >= 1; tg >>= 1) {
+            for (int R = rmax; R >= (pass == 0 ? rmin_busy : 1); R >>= 1) {
+                const int64_t wb = Seg<FMT, PHASE>::bytes(R, H, I);
+                if (wb > 72 * 1024) continue;
+                const int64_t stage = ((wb + 127) & ~(int64_t)127) + (int64_t)tg * c.tok_bytes;
+                const int64_t stages = (int64_t)((kSmemCap - kSmemHeader) / (size_t)stage);
+                if (stages < 2) continue;
+                c.R = R;
+                c.tiles = (nout + R - 1) / R;
+                c.tg = tg;
+                c.tok_off = (int32_t)((wb + 127) & ~(int64_t)127);
+                c.stage_bytes = (int32_t)((stage + 127) & ~(int64_t)127);
+                c.stages = stages > kMaxStages ? kMaxStages : (int32_t)stages;
+                return true;
+            }
         }
     }
     return false;
