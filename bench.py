@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--copy-mode", default="fused", choices=["fused", "per_bank", "engine"])
+    ap.add_argument("--experts", type=int, default=0, help="override E (smaller profiling cases)")
+    ap.add_argument("--slots", type=int, default=0, help="override S (smaller profiling cases)")
     return ap.parse_args()
 
 
@@ -299,6 +301,8 @@ def run_gpu(args):
     dev = torch.cuda.current_device()
     stream = torch.cuda.Stream()
     cfg = wl.CONFIGS[args.config]
+    if args.experts or args.slots:
+        cfg = wl.scaled(cfg, E=args.experts or cfg.E, S=args.slots or cfg.S)
     bs, mr = args.bs, args.miss_rate
     r = wl.make_route(cfg, bs, mr)
     B = cfg.bytes_per_expert

@@ -35,7 +35,7 @@ size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct Layout {
     size_t hdr, id2slot, owner, stamp, miss_ids, miss_slots;
-    size_t n_unique, uslot, ucnt, uoff, upairs, h, o;
+    size_t n_unique, uslot, ucnt, uoff, upairs, h, o, x16, xexp, hmax, upoff;
     size_t total;
     bool ffn;
 };
@@ -100,6 +100,10 @@ Layout make_layout(int fmt, int E, int L, int S, int H, int I, int max_pairs) {
         l.upairs = off; off += align256(P * 4);
         l.h = off; off += align256(P * (size_t)I * 4);
         l.o = off; off += align256(P * (size_t)H * 4);
+        l.x16 = off; off += align256(P * (size_t)H * 2);
+        l.xexp = off; off += align256(P * 4);
+        l.hmax = off; off += align256(P * 4);
+        l.upoff = off; off += align256(P * 4);
     }
     l.total = off;
     return l;
@@ -139,6 +143,7 @@ struct ftmoe_cache {
     Tables t;
     FfnScratch s;
     bool ffn;
+    MxTmaMaps mx;
 };
 
 extern "C" {
@@ -244,6 +249,16 @@ int ftmoe_cache_create(const ftmoe_bank_spec *banks, int32_t num_banks, int32_t 
         c->s.upairs = reinterpret_cast<int32_t *>(ws + lay.upairs);
         c->s.h = reinterpret_cast<float *>(ws + lay.h);
         c->s.o = reinterpret_cast<float *>(ws + lay.o);
+        c->s.x16 = reinterpret_cast<uint16_t *>(ws + lay.x16);
+        c->s.xexp = reinterpret_cast<int32_t *>(ws + lay.xexp);
+        c->s.hmax = reinterpret_cast<uint32_t *>(ws + lay.hmax);
+        c->s.upoff = reinterpret_cast<int32_t *>(ws + lay.upoff);
+        c->s.n_passes = c->s.n_unique + 1;  // second word of the 256-byte n_unique block
+    }
+    if (format == FTMOE_FMT_MXFP4 && lay.ffn) {
+        const unsigned char *sb[6];
+        for (int b = 0; b < 6; b++) sb[b] = c->dev_slots[b];
+        make_mx_tma_maps(c->mx, sb, S, H, I);  // on failure the FFN uses the register path
     }
     e = launch_init_state(c->t, E, L, S, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
@@ -376,7 +391,7 @@ int ftmoe_expert_ffn(ftmoe_cache_t *c, const void *d_x_bf16, int32_t bs, const i
     p.y = static_cast<uint16_t *>(d_y_bf16);
     p.status = c->t.status;
     p.fmt = c->fmt; p.H = c->H; p.I = c->I; p.S = c->S; p.bs = bs; p.topk = topk; p.P = (int)P;
-    CK(launch_ffn(p, c->num_sms, static_cast<cudaStream_t>(stream)), "ffn kernels");
+    CK(launch_ffn(p, c->num_sms, static_cast<cudaStream_t>(stream), &c->mx), "ffn kernels");
     return FTMOE_OK;
 }
 

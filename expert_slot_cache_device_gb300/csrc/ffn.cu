@@ -72,14 +72,51 @@ __device__ int block_scan_sum(int v, int *warp_tot, int *total) {
     return r;
 }
 
+// CTA 0 groups the routed pairs by slot (and clears the per-pair max |h| words). CTAs
+// 1..bs (launched only when the fp4 activation copy is wanted) convert token
+// t = blockIdx.x - 1 to f16 with a power-of-two scale 2^-e chosen so that
+// max|x_t| * 2^-e < 2^10: bf16 values (8 significant bits) land exactly in f16 except
+// below the f16 normal range, and the f16 partial sums of the fp4 dot products (four
+// products of |e2m1| <= 6) stay below 2^15.
 __global__ void __launch_bounds__(1024) ffn_route_kernel(FfnParams p) {
     extern __shared__ int cnt[];  // [S], later the placement cursor
     __shared__ int warp_tot[32];
     __shared__ int s_bad, s_tot_u, s_tot_c;
+    __shared__ float s_wmax[32];
     const int tid = threadIdx.x, nt = blockDim.x;
     asm volatile("griddepcontrol.launch_dependents;" :::);
+    if (blockIdx.x > 0) {
+        const int t = blockIdx.x - 1;
+        const uint16_t *xr = p.x + (int64_t)t * p.H;
+        float m = 0.f;
+        for (int k = tid; k < p.H; k += nt) m = fmaxf(m, fabsf(__uint_as_float((uint32_t)xr[k] << 16)));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if ((tid & 31) == 0) s_wmax[tid >> 5] = m;
+        __syncthreads();
+        if (tid < 32) {
+            float v = tid < (nt >> 5) ? s_wmax[tid] : 0.f;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+            if (tid == 0) s_wmax[0] = v;
+        }
+        __syncthreads();
+        int e = 0;
+        if (s_wmax[0] > 0.f && s_wmax[0] < INFINITY) {
+            frexpf(s_wmax[0], &e);  // max < 2^e
+            e -= p.x16_emax;
+        }
+        const float sc = ldexpf(1.f, -e);
+        uint16_t *dst = p.s.x16 + (int64_t)t * p.H;
+        for (int k = tid; k < p.H; k += nt)
+            dst[k] = __half_as_ushort(__float2half_rn(__uint_as_float((uint32_t)xr[k] << 16) * sc));
+        if (tid == 0) p.s.xexp[t] = e;
+        return;
+    }
     if (tid == 0) s_bad = 0;
     for (int s = tid; s < p.S; s += nt) cnt[s] = 0;
+    if (p.s.hmax)
+        for (int q = tid; q < p.P; q += nt) p.s.hmax[q] = 0u;
     __syncthreads();
     for (int q = tid; q < p.P; q += nt) {
         int s = p.slots[q];
@@ -96,23 +133,28 @@ __global__ void __launch_bounds__(1024) ffn_route_kernel(FfnParams p) {
         }
         return;
     }
-    int base_u = 0, base_c = 0;
+    int base_u = 0, base_c = 0, base_p = 0;
+    __shared__ int s_tot_p;
     for (int s0 = 0; s0 < p.S; s0 += nt) {
         int s = s0 + tid;
         int c = s < p.S ? cnt[s] : 0;
         int ru = block_scan_sum(c > 0, warp_tot, &s_tot_u);
         int rc = block_scan_sum(c, warp_tot, &s_tot_c);
+        int rp = block_scan_sum((c + kPassTokens - 1) / kPassTokens, warp_tot, &s_tot_p);
         if (c > 0) {
             int u = base_u + ru;
             p.s.uslot[u] = s;
             p.s.ucnt[u] = c;
             p.s.uoff[u] = base_c + rc;
+            if (p.s.upoff) p.s.upoff[u] = base_p + rp;
             cnt[s] = base_c + rc;
         }
         base_u += s_tot_u;
         base_c += s_tot_c;
+        base_p += s_tot_p;
         __syncthreads();
     }
+    if (tid == 0 && p.s.n_passes) *p.s.n_passes = base_p;
     for (int q = tid; q < p.P; q += nt) {
         int pos = atomicAdd(&cnt[p.slots[q]], 1);
         p.s.upairs[pos] = q;
@@ -684,21 +726,29 @@ cudaError_t launch_dyn(K kernel, int grid, size_t smem, cudaStream_t st, const F
 
 }  // namespace
 
-cudaError_t launch_ffn(const FfnParams &p, int num_sms, cudaStream_t st) {
+cudaError_t launch_ffn(const FfnParams &p_in, int num_sms, cudaStream_t st, const MxTmaMaps *mx) {
+    FfnParams p = p_in;
     cudaError_t e;
     size_t route_smem = (size_t)p.S * sizeof(int);
     if (route_smem > 48 * 1024) {
         e = cudaFuncSetAttribute(ffn_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)route_smem);
         if (e != cudaSuccess) return e;
     }
-    ffn_route_kernel<<<1, 1024, route_smem, st>>>(p);
+    const bool fp4_rows_tma = num_sms > 0 && ffn_rows_tma_supported(p);
+    const bool mx_tma = num_sms > 0 && ffn_mx_tma_supported(p, mx);
+    const bool want_x16 = (fp4_rows_tma && p.fmt == FTMOE_FMT_NVFP4) || mx_tma;
+    p.x16_emax = p.fmt == FTMOE_FMT_MXFP4 ? 9 : 10;
+    ffn_route_kernel<<<1 + (want_x16 ? p.bs : 0), 1024, route_smem, st>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
     const int umax = p.P < p.S ? p.P : p.S;  // distinct slots at most
     const size_t budget = 64 * 1024;
     bool pdl_combine = false;
-    if (num_sms > 0 && ffn_rows_tma_supported(p)) {
+    if (fp4_rows_tma) {
         if ((e = launch_ffn_rows_tma(p, num_sms, st)) != cudaSuccess) return e;
+        pdl_combine = true;
+    } else if (mx_tma) {
+        if ((e = launch_ffn_mx_tma(p, *mx, num_sms, st)) != cudaSuccess) return e;
         pdl_combine = true;
     } else if (p.fmt == FTMOE_FMT_BF16 || p.fmt == FTMOE_FMT_NVFP4) {
         const int tiles_gu = (p.I + kGuNeurons - 1) / kGuNeurons;

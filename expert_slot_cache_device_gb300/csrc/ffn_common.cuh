@@ -85,5 +85,105 @@ __device__ __forceinline__ void unpack_bf16x8(uint4 v, float (&f)[8]) {
     f[4] = bf_lo(v.z); f[5] = bf_hi(v.z); f[6] = bf_lo(v.w); f[7] = bf_hi(v.w);
 }
 
+// Eight packed e2m1 codes (one 32-bit word) -> four f16x2 registers, low nibble first.
+// e2m1 values are exact in f16.
+__device__ __forceinline__ void e2m1x8_h2(uint32_t w, uint32_t (&h)[4]) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w));
+}
+
+// acc + w.lo * x.lo + w.hi * x.hi: f16 multiplicands, exact products, fp32 accumulation.
+__device__ __forceinline__ float fma2_f16(uint32_t w2, uint32_t x2, float acc) {
+    asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\t"
+        "mov.b32 {a0, a1}, %1;\n\t"
+        "mov.b32 {b0, b1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, a0, b0, %0;\n\t"
+        "fma.rn.f32.f16 %0, a1, b1, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(w2), "r"(x2));
+    return acc;
+}
+
+// Packed fp32 fused multiply-add: (a.x * b.x + c.x, a.y * b.y + c.y).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    uint64_t d;
+    asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+        "mov.b64 ra, {%1, %2};\n\t"
+        "mov.b64 rb, {%3, %4};\n\t"
+        "mov.b64 rc, {%5, %6};\n\t"
+        "fma.rn.f32x2 %0, ra, rb, rc;\n\t}"
+        : "=l"(d)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
+    return r;
+}
+
+__device__ __forceinline__ float2 h2_to_f2(uint32_t h) { return __half22float2(*reinterpret_cast<__half2 *>(&h)); }
+
+// Two e4m3 bytes (low byte first) -> float2 via the f16x2 conversion (exact).
+__device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t two_bytes) {
+    uint32_t h;
+    asm("{\n\t.reg .b16 s;\n\t"
+        "cvt.u16.u32 s, %1;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, s;\n\t}"
+        : "=r"(h)
+        : "r"(two_bytes & 0xffffu));
+    return h2_to_f2(h);
+}
+
+// Dot product of one packed word of eight e2m1 codes with eight f16 activations
+// (four f16x2 registers): products are exact in f16 (2 x 8 significant bits at most);
+// each half accumulates four of them with f16 additions, then the two halves are
+// summed in fp32. Callers keep |x| < 2^10 so no partial can overflow.
+__device__ __forceinline__ float dot8_e2m1_f16(const uint32_t (&w)[4], const uint32_t (&x)[4]) {
+    __half2 acc = __hmul2(*reinterpret_cast<const __half2 *>(&w[0]), *reinterpret_cast<const __half2 *>(&x[0]));
+    acc = __hfma2(*reinterpret_cast<const __half2 *>(&w[1]), *reinterpret_cast<const __half2 *>(&x[1]), acc);
+    acc = __hfma2(*reinterpret_cast<const __half2 *>(&w[2]), *reinterpret_cast<const __half2 *>(&x[2]), acc);
+    acc = __hfma2(*reinterpret_cast<const __half2 *>(&w[3]), *reinterpret_cast<const __half2 *>(&x[3]), acc);
+    const float2 f = __half22float2(acc);
+    return f.x + f.y;
+}
+
+// Dot product of one 16-element block: sixteen e2m1 codes (eight f16x2 registers) with
+// sixteen f16 activations. Each f16 half sums eight exact products (|x| < 2^10 keeps
+// every partial below 8 * 6 * 2^10 = 49152 < 65504); the halves are added in fp32.
+__device__ __forceinline__ float dot16_e2m1_f16(const uint32_t (&w)[8], const uint32_t (&x)[8]) {
+    __half2 acc = __hmul2(*reinterpret_cast<const __half2 *>(&w[0]), *reinterpret_cast<const __half2 *>(&x[0]));
+#pragma unroll
+    for (int i = 1; i < 8; i++)
+        acc = __hfma2(*reinterpret_cast<const __half2 *>(&w[i]), *reinterpret_cast<const __half2 *>(&x[i]), acc);
+    const float2 f = __half22float2(acc);
+    return f.x + f.y;
+}
+
+// Eight fp32 values scaled by `sc` (a power of two) -> four f16x2 registers.
+__device__ __forceinline__ void f32x8_to_h2(const float (&v)[8], float sc, uint32_t (&h)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const __half2 t = __floats2half2_rn(v[2 * i] * sc, v[2 * i + 1] * sc);
+        h[i] = *reinterpret_cast<const uint32_t *>(&t);
+    }
+}
+
+// Distinct slot u owning pass `pi`: the largest u with upoff[u] <= pi (upoff ascending).
+__device__ __forceinline__ int pass_owner(const int32_t *upoff, int nu, int pi) {
+    int lo = 0, hi = nu - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (upoff[mid] <= pi)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
 }  // namespace ffn
 }  // namespace ftmoe

@@ -42,7 +42,7 @@ enum { kGateUp = 0, kDown = 1 };
 struct StageHdr {
     int32_t slot, n0, rows, ntok, done, pad0, pad1, pad2;
     int32_t pairs[kMaxTok];
-    int32_t pad3[4];
+    int32_t texp[kMaxTok];  // per-token exponent of the f16 activations (nvfp4 gate_up)
 };
 
 struct TmaCfg {
@@ -181,37 +181,39 @@ __device__ __forceinline__ void gu_consume(const FfnParams &p, const TmaCfg &c, 
                 }
             }
         } else {
-            // lane step = one 32-bit word of codes (8 consecutive k, inside one 16-block):
-            // code, scale and x reads are contiguous (or broadcast) across lanes
-            const uint32_t *cg = reinterpret_cast<const uint32_t *>(st + j * wr);
-            const uint32_t *cu = reinterpret_cast<const uint32_t *>(st + (R + j) * wr);
+            // lane step = one 16-element scale block (two 32-bit code words): codes ->
+            // exact f16x2, sixteen exact f16 products summed in two f16 halves of eight,
+            // then fp32 (block scale, accumulation over blocks)
+            const uint2 *cg = reinterpret_cast<const uint2 *>(st + j * wr);
+            const uint2 *cu = reinterpret_cast<const uint2 *>(st + (R + j) * wr);
             const unsigned char *sg = st + 2 * R * wr + j * sr, *su = st + 2 * R * wr + (R + j) * sr;
-            const int nw = H >> 3;
-#pragma unroll 2
-            for (int w = lane; w < nw; w += 32) {
-                float fa[8], fb[8];
-                e2m1x8(cg[w], fa);
-                e2m1x8(cu[w], fb);
-                const float scg = e4m3_to_f(sg[w >> 1]), scu = e4m3_to_f(su[w >> 1]);
+            const int nb = H >> 4;
+            for (int b = lane; b < nb; b += 32) {
+                const uint2 ca = cg[b], cb = cu[b];
+                uint32_t fa[8], fb[8];
+                e2m1x8_h2(ca.x, *reinterpret_cast<uint32_t(*)[4]>(&fa[0]));
+                e2m1x8_h2(ca.y, *reinterpret_cast<uint32_t(*)[4]>(&fa[4]));
+                e2m1x8_h2(cb.x, *reinterpret_cast<uint32_t(*)[4]>(&fb[0]));
+                e2m1x8_h2(cb.y, *reinterpret_cast<uint32_t(*)[4]>(&fb[4]));
+                const float2 sc = e4m3x2_to_f2((uint32_t)sg[b] | ((uint32_t)su[b] << 8));
 #pragma unroll
                 for (int t = 0; t < NT; t++) {
-                    float fx[8];
-                    unpack_bf16x8(xs[t * nxv + w], fx);
-                    float pg = 0.f, pu = 0.f;
-#pragma unroll
-                    for (int i = 0; i < 8; i++) {
-                        pg = fmaf(fa[i], fx[i], pg);
-                        pu = fmaf(fb[i], fx[i], pu);
-                    }
-                    g[t] = fmaf(pg, scg, g[t]);
-                    u[t] = fmaf(pu, scu, u[t]);
+                    const uint4 x0 = xs[t * nxv + 2 * b], x1 = xs[t * nxv + 2 * b + 1];
+                    const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                    g[t] = fmaf(dot16_e2m1_f16(fa, xw), sc.x, g[t]);
+                    u[t] = fmaf(dot16_e2m1_f16(fb, xw), sc.y, u[t]);
                 }
             }
         }
 #pragma unroll
         for (int t = 0; t < NT; t++) {
-            const float gs = warp_sum(g[t]) * gg, us = warp_sum(u[t]) * gu;
-            if (lane == t) p.s.h[(int64_t)h.pairs[t] * I + n] = silu(gs) * us;
+            const float xs_t = FMT == FTMOE_FMT_NVFP4 ? ldexpf(1.f, h.texp[t]) : 1.f;
+            const float gs = warp_sum(g[t]) * gg * xs_t, us = warp_sum(u[t]) * gu * xs_t;
+            if (lane == t) {
+                const float hv = silu(gs) * us;
+                p.s.h[(int64_t)h.pairs[t] * I + n] = hv;
+                if (FMT == FTMOE_FMT_NVFP4) atomicMax(&p.s.hmax[h.pairs[t]], __float_as_uint(fabsf(hv)));
+            }
         }
     }
 }
@@ -256,27 +258,41 @@ __device__ __forceinline__ void dn_consume(const FfnParams &p, const TmaCfg &c, 
                 }
             }
         } else {
-            // lane step = one 32-bit word of codes (8 consecutive k inside one 16-block)
-            const int nw = I >> 3;
-            for (int w = lane; w < nw; w += 32) {
-                float fa[RR][8], sc[RR];
+            // lane step = one 16-element scale block (two code words); h is converted once
+            // per block and token to f16 with the token's power-of-two scale (max |h| <
+            // 2^10), shared by the RR rows; products summed as in gate_up
+            const int nb = I >> 4;
+            float hsc[NT];
 #pragma unroll
-                for (int r = 0; r < RR; r++) {
-                    const int jr = r < nr ? j0 + r : j0;
-                    e2m1x8(*reinterpret_cast<const uint32_t *>(st + jr * wr + 4 * w), fa[r]);
-                    sc[r] = e4m3_to_f(st[R * wr + jr * sr + (w >> 1)]);
+            for (int t = 0; t < NT; t++) hsc[t] = ldexpf(1.f, -h.texp[t]);
+            for (int b = lane; b < nb; b += 32) {
+                uint32_t fa[RR][8];
+                float sc[RR];
+#pragma unroll
+                for (int r = 0; r < RR; r += 2) {
+                    const int j1 = r < nr ? j0 + r : j0, j2 = r + 1 < nr ? j0 + r + 1 : j0;
+                    const uint2 c1 = *reinterpret_cast<const uint2 *>(st + j1 * wr + 8 * b);
+                    const uint2 c2 = *reinterpret_cast<const uint2 *>(st + j2 * wr + 8 * b);
+                    e2m1x8_h2(c1.x, *reinterpret_cast<uint32_t(*)[4]>(&fa[r][0]));
+                    e2m1x8_h2(c1.y, *reinterpret_cast<uint32_t(*)[4]>(&fa[r][4]));
+                    e2m1x8_h2(c2.x, *reinterpret_cast<uint32_t(*)[4]>(&fa[r + 1][0]));
+                    e2m1x8_h2(c2.y, *reinterpret_cast<uint32_t(*)[4]>(&fa[r + 1][4]));
+                    const float2 s2 = e4m3x2_to_f2((uint32_t)st[R * wr + j1 * sr + b] |
+                                                   ((uint32_t)st[R * wr + j2 * sr + b] << 8));
+                    sc[r] = s2.x;
+                    sc[r + 1] = s2.y;
                 }
 #pragma unroll
                 for (int t = 0; t < NT; t++) {
-                    const float4 h0 = hs[t * nh4 + 2 * w], h1 = hs[t * nh4 + 2 * w + 1];
-                    const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+                    const float4 *hp = hs + t * nh4 + 4 * b;
+                    const float4 h0 = hp[0], h1 = hp[1], h2 = hp[2], h3 = hp[3];
+                    const float hv0[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+                    const float hv1[8] = {h2.x, h2.y, h2.z, h2.w, h3.x, h3.y, h3.z, h3.w};
+                    uint32_t hh2[8];
+                    f32x8_to_h2(hv0, hsc[t], *reinterpret_cast<uint32_t(*)[4]>(&hh2[0]));
+                    f32x8_to_h2(hv1, hsc[t], *reinterpret_cast<uint32_t(*)[4]>(&hh2[4]));
 #pragma unroll
-                    for (int r = 0; r < RR; r++) {
-                        float part = 0.f;
-#pragma unroll
-                        for (int i = 0; i < 8; i++) part = fmaf(fa[r][i], hv[i], part);
-                        o[r][t] = fmaf(part, sc[r], o[r][t]);
-                    }
+                    for (int r = 0; r < RR; r++) o[r][t] = fmaf(dot16_e2m1_f16(fa[r], hh2), sc[r], o[r][t]);
                 }
             }
         }
@@ -290,7 +306,7 @@ __device__ __forceinline__ void dn_consume(const FfnParams &p, const TmaCfg &c, 
                                                                     2 * (int64_t)n));
 #pragma unroll
             for (int t = 0; t < NT; t++) {
-                const float v = warp_sum(o[r][t]) * gl;
+                const float v = warp_sum(o[r][t]) * gl * (FMT == FTMOE_FMT_NVFP4 ? ldexpf(1.f, h.texp[t]) : 1.f);
                 if (lane == t) p.s.o[(int64_t)h.pairs[t] * H + n] = v;
             }
         }
@@ -323,7 +339,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1) ffn_rows_tma_kernel(FfnParams 
         if (lane != 0) return;
         // Work items [first, last) of this CTA.
         const int nu = *p.s.n_unique;
-        const int items = nu > 0 ? nu * c.tiles : 0;
+        const int npass = nu > 0 ? *p.s.n_passes : 0;
+        const int items = npass * c.tiles;
         const int first = (int)((int64_t)blockIdx.x * items / gridDim.x);
         const int last = (int)((int64_t)(blockIdx.x + 1) * items / gridDim.x);
         const uint64_t pol = evict_first_policy();
@@ -332,11 +349,15 @@ __global__ void __launch_bounds__(kTmaThreads, 1) ffn_rows_tma_kernel(FfnParams 
         const int64_t wr = Seg<FMT, PHASE>::wrow(H, I), sr = Seg<FMT, PHASE>::srow(H, I);
         bool waited = PHASE == kGateUp, ok = true;
         int issued = 0;
+        int u = items > first ? pass_owner(p.s.upoff, nu, first / c.tiles) : 0;
         for (int it = first; it < last && ok; it++) {
-            const int u = it / c.tiles, tile = it - u * c.tiles;
+            const int pi = it / c.tiles, tile = it - pi * c.tiles;
+            while (u + 1 < nu && p.s.upoff[u + 1] <= pi) u++;  // contiguous items: walk forward
             int slot = p.s.uslot[u];
             slot = slot < 0 ? 0 : (slot >= p.S ? p.S - 1 : slot);
-            const int cnt = p.s.ucnt[u], off = p.s.uoff[u];
+            const int pbase = (pi - p.s.upoff[u]) * kPassTokens;
+            const int pcnt = p.s.ucnt[u] - pbase < kPassTokens ? p.s.ucnt[u] - pbase : kPassTokens;
+            const int off = p.s.uoff[u] + pbase, cnt = pcnt;
             const int n0 = tile * R, rows = nout - n0 < R ? nout - n0 : R;
             for (int g0 = 0; g0 < cnt && ok; g0 += c.tg) {
                 const int ntok = cnt - g0 < c.tg ? cnt - g0 : c.tg;
@@ -348,7 +369,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1) ffn_rows_tma_kernel(FfnParams 
                 }
                 StageHdr &hh = hdr[s];
                 hh.slot = slot; hh.n0 = n0; hh.rows = rows; hh.ntok = ntok; hh.done = 0;
-                for (int i = 0; i < ntok; i++) hh.pairs[i] = p.s.upairs[off + g0 + i];
+                for (int i = 0; i < ntok; i++) {
+                    hh.pairs[i] = p.s.upairs[off + g0 + i];
+                    hh.texp[i] = (PHASE == kGateUp && FMT == FTMOE_FMT_NVFP4) ? p.s.xexp[hh.pairs[i] / p.topk] : 0;
+                }
                 const uint32_t wbytes = (uint32_t)Seg<FMT, PHASE>::bytes(rows, H, I);
                 mbar_expect_tx(&full[s], wbytes + (uint32_t)(ntok * c.tok_bytes));
                 unsigned char *st = stage0 + (size_t)s * c.stage_bytes;
@@ -375,10 +399,23 @@ __global__ void __launch_bounds__(kTmaThreads, 1) ffn_rows_tma_kernel(FfnParams 
                     griddep_wait();
                     waited = true;
                 }
+                if (PHASE == kDown && FMT == FTMOE_FMT_NVFP4) {
+                    // power-of-two exponent for the f16 copy of each h row (max |h| < 2^10)
+                    for (int i = 0; i < ntok; i++) {
+                        const float m = __uint_as_float(p.s.hmax[hh.pairs[i]]);
+                        int e = 0;
+                        if (m > 0.f && m < INFINITY) {
+                            frexpf(m, &e);
+                            e -= 10;
+                        }
+                        hh.texp[i] = e;
+                    }
+                }
                 for (int i = 0; i < ntok; i++) {
                     const int q = hh.pairs[i];
+                    const uint16_t *xsrc = FMT == FTMOE_FMT_NVFP4 ? p.s.x16 : p.x;
                     const void *src = PHASE == kGateUp
-                                          ? static_cast<const void *>(p.x + (int64_t)(q / p.topk) * H)
+                                          ? static_cast<const void *>(xsrc + (int64_t)(q / p.topk) * H)
                                           : static_cast<const void *>(p.s.h + (int64_t)q * I);
                     bulk_g2s_plain(st + c.tok_off + i * c.tok_bytes, src, (uint32_t)c.tok_bytes, &full[s]);
                 }
@@ -490,8 +527,9 @@ cudaError_t launch_one(const FfnParams &p, int num_sms, cudaStream_t st) {
 }  // namespace
 
 bool ffn_rows_tma_supported(const FfnParams &p) {
+    if (!p.s.upoff || !p.s.n_passes) return false;
     if (p.fmt == FTMOE_FMT_BF16) return p.H % 8 == 0 && p.I % 8 == 0;
-    if (p.fmt == FTMOE_FMT_NVFP4) return p.H % 256 == 0 && p.I % 256 == 0;
+    if (p.fmt == FTMOE_FMT_NVFP4) return p.H % 256 == 0 && p.I % 256 == 0 && p.s.x16 && p.s.xexp && p.s.hmax;
     return false;
 }
 

@@ -66,7 +66,16 @@ struct FfnScratch {
     int32_t *upairs;    // [P] pair indices t * topk + j grouped by slot
     float *h;           // [P, I] SiLU(gate) * up per pair
     float *o;           // [P, H] down output per pair
+    uint16_t *x16;      // [bs, H] activations as f16, scaled by 2^-xexp[t] (nullptr: not prepared)
+    int32_t *xexp;      // [bs] per-token power-of-two exponent of x16
+    uint32_t *hmax;     // [P] bit pattern of max |h| per pair (order-independent atomicMax)
+    int32_t *upoff;     // [P] first pass (group of kPassTokens pairs) of each distinct slot
+    int32_t *n_passes;  // [1] passes over all distinct slots
 };
+
+// Pipelined FFN kernels split each slot's routed pairs into passes of this many tokens;
+// every (pass, tile) is a separate work item so hot experts spread over the SMs.
+constexpr int kPassTokens = 4;
 
 struct FfnParams {
     FfnScratch s;
@@ -79,11 +88,25 @@ struct FfnParams {
     uint16_t *y;            // [bs, H] bf16
     int32_t *status;
     int32_t fmt, H, I, S, bs, topk, P;
+    int32_t x16_emax;  // f16 activation copy keeps max |x| < 2^x16_emax
 };
-cudaError_t launch_ffn(const FfnParams &p, int num_sms, cudaStream_t st);
+
+// Tensor maps (CUtensorMap, 128 bytes each) over the transposed mxfp4 slot banks.
+struct MxTmaMaps {
+    alignas(128) unsigned char gu_blocks[128];
+    alignas(128) unsigned char gu_scales[128];
+    alignas(128) unsigned char dn_blocks[128];
+    alignas(128) unsigned char dn_scales[128];
+    bool valid = false;
+};
+bool make_mx_tma_maps(MxTmaMaps &m, const unsigned char *const *banks, int S, int H, int I);
+cudaError_t launch_ffn(const FfnParams &p, int num_sms, cudaStream_t st, const MxTmaMaps *mx = nullptr);
 // Persistent bulk-copy pipeline for the row-major formats (bf16; nvfp4 with H, I multiples of 256).
 bool ffn_rows_tma_supported(const FfnParams &p);
 cudaError_t launch_ffn_rows_tma(const FfnParams &p, int num_sms, cudaStream_t st);
+// 2-D tensor-map pipeline for the transposed mxfp4 format.
+bool ffn_mx_tma_supported(const FfnParams &p, const MxTmaMaps *maps);
+cudaError_t launch_ffn_mx_tma(const FfnParams &p, const MxTmaMaps &maps, int num_sms, cudaStream_t st);
 
 // Record `msg` as the thread's last error message and return `code`.
 int report_error(int code, const char *msg);
