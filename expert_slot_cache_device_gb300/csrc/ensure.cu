@@ -98,11 +98,11 @@ __device__ uint64_t bitonic_sort_regs(uint64_t key, int n, uint64_t *xbuf) {
     return key;
 }
 
-constexpr int kPerThread = (FTMOE_MAX_SLOTS + kThreads - 1) / kThreads;  // 8 (also covers E)
+constexpr int kPerThread = 8;  // slots and experts per thread: 8 x blockDim covers S and E
 
 __global__ void __launch_bounds__(kThreads) ensure_kernel(EnsureParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
-    const int xn = p.Spad > kThreads ? p.Spad : kThreads;
+    const int xn = p.Spad > (int)blockDim.x ? p.Spad : (int)blockDim.x;
     uint64_t *keys = reinterpret_cast<uint64_t *>(smem);          // [max(Spad, blockDim)]
     int32_t *s_slot = reinterpret_cast<int32_t *>(keys + xn);      // [E]: -2 absent, -1 miss, >=0 slot
     int32_t *s_miss = s_slot + p.E;                               // [maxm] flat ids by rank
@@ -256,8 +256,19 @@ __global__ void scatter_owner_kernel(Tables t, int S) {
 
 }  // namespace
 
+// Smallest power-of-two block (256..1024) whose threads cover the sort width, S and E / 8.
+int ensure_threads(int E, int S, int Spad) {
+    int need = Spad > S ? Spad : S;
+    const int e8 = (E + kPerThread - 1) / kPerThread;
+    if (e8 > need) need = e8;
+    int nt = 256;
+    while (nt < need && nt < kThreads) nt <<= 1;
+    return nt;
+}
+
 size_t ensure_smem_bytes(int E, int S, int Spad, int maxm) {
-    const size_t xn = Spad > kThreads ? Spad : kThreads;
+    const int nt = ensure_threads(E, S, Spad);
+    const size_t xn = Spad > nt ? Spad : nt;
     size_t b = xn * 8 + (size_t)E * 4 + (size_t)maxm * 4 + (size_t)S * 4 + (size_t)S;
     return (b + 15) & ~(size_t)15;
 }
@@ -268,7 +279,7 @@ cudaError_t launch_ensure(const EnsureParams &p, cudaStream_t st) {
         cudaError_t e = cudaFuncSetAttribute(ensure_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    ensure_kernel<<<1, kThreads, smem, st>>>(p);
+    ensure_kernel<<<1, ensure_threads(p.E, p.S, p.Spad), smem, st>>>(p);
     return cudaGetLastError();
 }
 
