@@ -49,6 +49,8 @@ def lib() -> ctypes.CDLL:
         P = ctypes.c_void_p
         L.orc_ensure.argtypes = [i32, i32, i32, P, P, P, P, i32, P, i32, P, P, P, P]
         L.orc_ensure.restype = ctypes.c_int
+        L.orc_ensure_hybrid.argtypes = [i32, i32, i32, P, P, P, P, i32, P, i32, i32, ctypes.c_float, P, P, P, P, P]
+        L.orc_ensure_hybrid.restype = ctypes.c_int
         L.orc_rebuild_id2slot.argtypes = [i32, i32, i32, P, P]
         L.orc_rebuild_id2slot.restype = ctypes.c_int
         L.orc_copy_missing.argtypes = [i32, P, P, P, i32, P, P, i32]
@@ -103,6 +105,23 @@ class Cache:
                               _p(self.clock), layer, _p(ids) if n else 0, n, _p(slots), _p(mid), _p(msl), _p(m))
         k = int(m[0])
         return rc, slots[:n].reshape(np.shape(topk_ids)), mid[:k].copy(), msl[:k].copy()
+
+    def ensure_hybrid(self, layer: int, topk_ids: np.ndarray, max_fetch: int, fetch_fraction: float = 0.0):
+        """Returns (rc, slots, miss_ids, miss_slots, (num_indices, num_missing_full))."""
+        ids = np.ascontiguousarray(topk_ids, dtype=np.int32).reshape(-1)
+        n = ids.size
+        slots = np.empty(max(n, 1), np.int32)
+        cap = max(min(self.E, n), 1)
+        mid = np.empty(cap, np.int32)
+        msl = np.empty(cap, np.int32)
+        m = np.zeros(1, np.int32)
+        counts = np.zeros(2, np.int32)
+        rc = lib().orc_ensure_hybrid(self.E, self.L, self.S, _p(self.owner), _p(self.stamp), _p(self.id2slot),
+                                     _p(self.clock), layer, _p(ids) if n else 0, n, int(max_fetch),
+                                     float(fetch_fraction), _p(slots), _p(mid), _p(msl), _p(m), _p(counts))
+        k = int(m[0])
+        return (rc, slots[:n].reshape(np.shape(topk_ids)), mid[:k].copy(), msl[:k].copy(),
+                (int(counts[0]), int(counts[1])))
 
 
 def copy_missing(bank_bytes: Sequence[int], host_layer: Sequence, slots: Sequence, E: int,

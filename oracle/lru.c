@@ -15,7 +15,10 @@
  *     equal stamps; empty slots keep stamp 0 and therefore go first;
  *   - more misses than untouched slots is a capacity error that leaves the
  *     state untouched.
+ * Hybrid variant ([BENCH] section 5.4): only the first `cap` misses in ascending
+ * flat id are fetched; the overflow keeps slot -1 for the CPU executor.
  */
+#include <math.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -50,10 +53,21 @@ static void fail_outputs(int32_t n, int32_t *slots_out, int32_t *num_miss) {
     *num_miss = 0;
 }
 
-int orc_ensure(int32_t E, int32_t L, int32_t S, int32_t *owner, uint32_t *stamp,
-               int32_t *id2slot, uint32_t *clock, int32_t layer, const int32_t *topk_ids,
-               int32_t n, int32_t *slots_out, int32_t *miss_ids, int32_t *miss_slots,
-               int32_t *num_miss) {
+/* Fetch cap of the hybrid rule (see oracle.h); the product is formed in binary32. */
+static int32_t hybrid_cap(int32_t misses, int32_t max_fetch, float fetch_fraction) {
+    if (max_fetch >= 0) return max_fetch;
+    if (fetch_fraction > 0.0f) {
+        float want = (float)misses * fetch_fraction;
+        return (int32_t)rintf(want);
+    }
+    return 1;
+}
+
+static int ensure_core(int32_t E, int32_t L, int32_t S, int32_t *owner, uint32_t *stamp,
+                       int32_t *id2slot, uint32_t *clock, int32_t layer, const int32_t *topk_ids,
+                       int32_t n, int hybrid, int32_t max_fetch, float fetch_fraction,
+                       int32_t *slots_out, int32_t *miss_ids, int32_t *miss_slots,
+                       int32_t *num_miss, int32_t *counts) {
     if (E <= 0 || L <= 0 || S <= 0 || n < 0 || layer < 0 || layer >= L) {
         fail_outputs(n < 0 ? 0 : n, slots_out, num_miss);
         return ORC_ERR_INVALID_ARG;
@@ -100,6 +114,12 @@ int orc_ensure(int32_t E, int32_t L, int32_t S, int32_t *owner, uint32_t *stamp,
     }
     qsort(cand, (size_t)nc, sizeof(cand_t), cand_cmp);
 
+    int32_t m_full = m;
+    if (hybrid) {
+        int32_t cap = hybrid_cap(m_full, max_fetch, fetch_fraction);
+        if (cap < 0) cap = 0;
+        if (m > cap) m = cap; /* the first `cap` misses in ascending id are fetched */
+    }
     int rc = ORC_OK;
     if (m > nc) {
         fail_outputs(n, slots_out, num_miss);
@@ -122,14 +142,35 @@ int orc_ensure(int32_t E, int32_t L, int32_t S, int32_t *owner, uint32_t *stamp,
         miss_slots[j] = s;
     }
     *num_miss = m;
+    if (counts) {
+        counts[0] = m;
+        counts[1] = m_full;
+    }
 
-    /* 6. slot of every routed (token, j) position */
+    /* 6. slot of every routed (token, j) position (-1 for misses left to the CPU) */
     for (int32_t t = 0; t < n; t++) slots_out[t] = id2slot[layer * E + topk_ids[t]];
 
 done:
+    if (rc != ORC_OK && counts) counts[0] = counts[1] = 0;
     free(present);
     free(hit_slot);
     free(misses);
     free(cand);
     return rc;
+}
+
+int orc_ensure(int32_t E, int32_t L, int32_t S, int32_t *owner, uint32_t *stamp,
+               int32_t *id2slot, uint32_t *clock, int32_t layer, const int32_t *topk_ids,
+               int32_t n, int32_t *slots_out, int32_t *miss_ids, int32_t *miss_slots,
+               int32_t *num_miss) {
+    return ensure_core(E, L, S, owner, stamp, id2slot, clock, layer, topk_ids, n, 0, -1, 0.0f,
+                       slots_out, miss_ids, miss_slots, num_miss, NULL);
+}
+
+int orc_ensure_hybrid(int32_t E, int32_t L, int32_t S, int32_t *owner, uint32_t *stamp,
+                      int32_t *id2slot, uint32_t *clock, int32_t layer, const int32_t *topk_ids,
+                      int32_t n, int32_t max_fetch, float fetch_fraction, int32_t *slots_out,
+                      int32_t *miss_ids, int32_t *miss_slots, int32_t *num_miss, int32_t *counts) {
+    return ensure_core(E, L, S, owner, stamp, id2slot, clock, layer, topk_ids, n, 1, max_fetch,
+                       fetch_fraction, slots_out, miss_ids, miss_slots, num_miss, counts);
 }

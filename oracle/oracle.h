@@ -60,6 +60,17 @@ int orc_ensure(int32_t E, int32_t L, int32_t S, int32_t *owner, uint32_t *stamp,
                int32_t n, int32_t *slots_out, int32_t *miss_ids, int32_t *miss_slots,
                int32_t *num_miss);
 
+/* Hybrid ensure_experts (benchmark guide, section 5.4): as orc_ensure, but only the
+ * first `cap` misses in ascending flat id get slots; the others keep slot -1 and leave
+ * the cache untouched. cap = max_fetch when max_fetch >= 0; otherwise the fetch share
+ * of the measured bandwidths, round-half-even(float(misses) * fetch_fraction) computed
+ * in binary32, when fetch_fraction > 0; otherwise 1. counts[0] = misses fetched
+ * (num_indices), counts[1] = misses before the cap (num_missing_full). */
+int orc_ensure_hybrid(int32_t E, int32_t L, int32_t S, int32_t *owner, uint32_t *stamp,
+                      int32_t *id2slot, uint32_t *clock, int32_t layer, const int32_t *topk_ids,
+                      int32_t n, int32_t max_fetch, float fetch_fraction, int32_t *slots_out,
+                      int32_t *miss_ids, int32_t *miss_slots, int32_t *num_miss, int32_t *counts);
+
 /* Rebuild id2slot[L*E] from owner[S]; returns ORC_ERR_STATE on duplicate / bad owners. */
 int orc_rebuild_id2slot(int32_t E, int32_t L, int32_t S, const int32_t *owner, int32_t *id2slot);
 
