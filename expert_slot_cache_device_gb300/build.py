@@ -1,7 +1,7 @@
 """Build libftmoe.so (sm_103a) in-tree with nvcc.
 
-Every translation unit under csrc/ is compiled in parallel for
-``-gencode arch=compute_103a,code=sm_103a`` and linked into
+Every CUDA translation unit under csrc/ is compiled in parallel for
+``-gencode arch=compute_103a,code=sm_103a`` (host C++ units with g++) and linked into
 ``expert_slot_cache_device_gb300/libftmoe.so`` against the shared CUDA runtime.
 """
 from __future__ import annotations
@@ -31,8 +31,18 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
+CXX_FLAGS = ["-O3", "-std=c++17", "-fPIC", "-pthread", "-I", INCLUDE]
+
+
 def sources():
-    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
+    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cpp")))
+
+
+def cxx() -> str:
+    for cand in (os.environ.get("CXX"), shutil.which("g++"), shutil.which("c++")):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("no C++ compiler found")
 
 
 def _deps():
@@ -56,7 +66,10 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-        cmd = [cc, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
+        if src.endswith(".cpp"):
+            cmd = [cxx(), *CXX_FLAGS, "-c", src, "-o", obj]
+        else:
+            cmd = [cc, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
@@ -67,7 +80,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     with ThreadPoolExecutor(max(1, min(8, os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, sources()))
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [cc, "-shared", "-cudart", "shared", *ARCH, "-o", tmp, *objs,
+    cmd = [cc, "-shared", "-cudart", "shared", *ARCH, "-o", tmp, *objs, "-lpthread",
            "-Xlinker", "-rpath=/usr/local/cuda/lib64"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:

@@ -282,8 +282,9 @@ int ftmoe_set_copy_mode(ftmoe_cache_t *c, int32_t mode) {
     return FTMOE_OK;
 }
 
-int ftmoe_ensure_experts(ftmoe_cache_t *c, int32_t layer, const int32_t *d_topk_ids, int32_t bs, int32_t topk,
-                         int32_t *d_slots_out, void *stream) {
+static int ensure_impl(ftmoe_cache_t *c, int32_t layer, const int32_t *d_topk_ids, int32_t bs, int32_t topk,
+                       int32_t *d_slots_out, int hybrid, int32_t max_fetch, float fetch_fraction, int32_t *d_counts,
+                       void *stream) {
     if (!c) return fail(FTMOE_ERR_INVALID_ARG, "cache is NULL");
     if (layer < 0 || layer >= c->L) return fail(FTMOE_ERR_INVALID_ARG, "layer %d outside [0, %d)", layer, c->L);
     if (bs < 0 || topk < 0) return fail(FTMOE_ERR_INVALID_ARG, "bs and topk must be >= 0");
@@ -302,9 +303,35 @@ int ftmoe_ensure_experts(ftmoe_cache_t *c, int32_t layer, const int32_t *d_topk_
     while (spad < c->S) spad <<= 1;
     p.Spad = spad;
     p.maxm = c->E < c->S ? c->E : c->S;
+    p.hybrid = hybrid;
+    p.max_fetch = max_fetch;
+    p.fetch_fraction = fetch_fraction;
+    p.counts = d_counts;
     cudaError_t e = launch_ensure(p, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "ensure kernel");
     c->last_layer = layer;
+    return FTMOE_OK;
+}
+
+int ftmoe_ensure_experts(ftmoe_cache_t *c, int32_t layer, const int32_t *d_topk_ids, int32_t bs, int32_t topk,
+                         int32_t *d_slots_out, void *stream) {
+    return ensure_impl(c, layer, d_topk_ids, bs, topk, d_slots_out, 0, -1, 0.f, nullptr, stream);
+}
+
+int ftmoe_ensure_experts_hybrid(ftmoe_cache_t *c, int32_t layer, const int32_t *d_topk_ids, int32_t bs,
+                                int32_t topk, int32_t max_fetch, float fetch_fraction, int32_t *d_slots_out,
+                                int32_t *d_counts, void *stream) {
+    return ensure_impl(c, layer, d_topk_ids, bs, topk, d_slots_out, 1, max_fetch, fetch_fraction, d_counts, stream);
+}
+
+int ftmoe_hybrid_fetch_fraction(double pcie_gbps, double cpu_gbps, float *out) {
+    if (!out) return fail(FTMOE_ERR_INVALID_ARG, "out is NULL");
+    if (!(pcie_gbps > 0.0) || !(cpu_gbps > 0.0))
+        *out = 0.f;
+    else if (cpu_gbps <= pcie_gbps)
+        *out = 1.f;
+    else
+        *out = (float)(pcie_gbps / cpu_gbps);
     return FTMOE_OK;
 }
 
@@ -368,6 +395,12 @@ int ftmoe_copy_missing(ftmoe_cache_t *c, void *stream) {
 
 int ftmoe_expert_ffn(ftmoe_cache_t *c, const void *d_x_bf16, int32_t bs, const int32_t *d_slots,
                      const float *d_weights, int32_t topk, void *d_y_bf16, void *stream) {
+    return ftmoe_expert_ffn_hybrid(c, d_x_bf16, bs, d_slots, d_weights, topk, nullptr, d_y_bf16, stream);
+}
+
+int ftmoe_expert_ffn_hybrid(ftmoe_cache_t *c, const void *d_x_bf16, int32_t bs, const int32_t *d_slots,
+                            const float *d_weights, int32_t topk, const float *d_addend, void *d_y_bf16,
+                            void *stream) {
     if (!c) return fail(FTMOE_ERR_INVALID_ARG, "cache is NULL");
     if (c->fmt == FTMOE_FMT_RAW) return fail(FTMOE_ERR_FORMAT, "a raw-format cache has no FFN");
     if (!c->ffn) return fail(FTMOE_ERR_INVALID_ARG, "cache created with max_pairs = 0");
@@ -376,8 +409,8 @@ int ftmoe_expert_ffn(ftmoe_cache_t *c, const void *d_x_bf16, int32_t bs, const i
     if (P > c->max_pairs) return fail(FTMOE_ERR_INVALID_ARG, "bs*topk=%lld above max_pairs=%d", (long long)P, c->max_pairs);
     if (P == 0) return FTMOE_OK;
     if (!d_x_bf16 || !d_slots || !d_weights || !d_y_bf16) return fail(FTMOE_ERR_INVALID_ARG, "NULL FFN argument");
-    if (((uintptr_t)d_x_bf16 | (uintptr_t)d_y_bf16) % 16)
-        return fail(FTMOE_ERR_INVALID_ARG, "x and y must be 16-byte aligned");
+    if (((uintptr_t)d_x_bf16 | (uintptr_t)d_y_bf16 | (uintptr_t)d_addend) % 16)
+        return fail(FTMOE_ERR_INVALID_ARG, "x, y and the addend must be 16-byte aligned");
     FfnParams p;
     memset(&p, 0, sizeof p);
     p.s = c->s;
@@ -388,6 +421,7 @@ int ftmoe_expert_ffn(ftmoe_cache_t *c, const void *d_x_bf16, int32_t bs, const i
     p.x = static_cast<const uint16_t *>(d_x_bf16);
     p.slots = d_slots;
     p.weights = d_weights;
+    p.addend = d_addend;
     p.y = static_cast<uint16_t *>(d_y_bf16);
     p.status = c->t.status;
     p.fmt = c->fmt; p.H = c->H; p.I = c->I; p.S = c->S; p.bs = bs; p.topk = topk; p.P = (int)P;

@@ -1,0 +1,212 @@
+// Host CPU expert executor of the hybrid decode path.
+//
+// FreeToken benchmark guide, section 5.4: in hybrid mode the misses beyond the fetch
+// cap are not copied to the GPU; their routed positions get slot -1 and a CPU MoE
+// executor computes those experts from the page-locked host banks while the GPU
+// computes the resident and fetched ones (architecture deep-dive, section 五: the CPU
+// side runs a GEMV over the host expert banks). This is that executor for the bf16,
+// nvfp4 and transposed mxfp4 bank schemas: plain C++ with fp32 accumulation, written
+// so the compiler can vectorise the inner loops for the host's SIMD units, and split
+// over std::thread workers (gate_up + SiLU * up for every CPU pair, then down).
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <thread>
+#include <vector>
+
+#include "ftmoe.h"
+
+namespace {
+
+float bf16_to_f(uint16_t b) {
+    const uint32_t u = static_cast<uint32_t>(b) << 16;
+    float f;
+    std::memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+float f16_to_f(uint16_t h) {
+    const int s = (h >> 15) & 1, e = (h >> 10) & 31, m = h & 1023;
+    float v;
+    if (e == 0)
+        v = std::ldexp(static_cast<float>(m), -24);
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = std::ldexp(static_cast<float>(1024 + m), e - 25);
+    return s ? -v : v;
+}
+
+struct Tables {
+    float e2m1[16];
+    float e4m3[256];
+    Tables() {
+        for (int c = 0; c < 16; c++) {
+            const int mag = c & 7;
+            const float v = mag < 2 ? 0.5f * mag : std::ldexp(1.0f + 0.5f * (mag & 1), (mag >> 1) - 1);
+            e2m1[c] = (c & 8) ? -v : v;
+        }
+        for (int b = 0; b < 256; b++) {
+            const int e = (b >> 3) & 15, m = b & 7;
+            float v = e == 0 ? std::ldexp(static_cast<float>(m), -9) : std::ldexp(1.0f + m / 8.0f, e - 7);
+            if (e == 15 && m == 7) v = NAN;
+            e4m3[b] = (b & 0x80) ? -v : v;
+        }
+    }
+};
+
+const Tables &tables() {
+    static const Tables t;
+    return t;
+}
+
+float silu(float z) { return z / (1.0f + std::exp(-z)); }
+
+template <typename F>
+void parallel_for(int64_t n, int threads, F &&fn) {
+    if (n <= 0) return;
+    const int nt = static_cast<int>(std::min<int64_t>(threads, n));
+    if (nt <= 1) {
+        fn(0, n);
+        return;
+    }
+    std::vector<std::thread> pool;
+    pool.reserve(nt);
+    for (int i = 0; i < nt; i++) {
+        const int64_t a = n * i / nt, b = n * (i + 1) / nt;
+        pool.emplace_back([&fn, a, b] { fn(a, b); });
+    }
+    for (auto &th : pool) th.join();
+}
+
+// Dot product of output row n of a row-major expert matrix (bf16 or nvfp4) with v[K].
+float row_dot(int fmt, const uint8_t *const *b, int which, int64_t n, int64_t K, const float *v) {
+    const Tables &T = tables();
+    if (fmt == FTMOE_FMT_BF16) {
+        const uint16_t *w = reinterpret_cast<const uint16_t *>(b[which]) + n * K;
+        float acc = 0.f;
+        for (int64_t k = 0; k < K; k++) acc += bf16_to_f(w[k]) * v[k];
+        return acc;
+    }
+    const uint8_t *codes = b[3 * which] + n * (K / 2);
+    const uint8_t *sc = b[3 * which + 1] + n * (K / 16);
+    const uint16_t g = reinterpret_cast<const uint16_t *>(b[3 * which + 2])[n];
+    float acc = 0.f;
+    for (int64_t blk = 0; blk < K / 16; blk++) {
+        float part = 0.f;
+        for (int i = 0; i < 8; i++) {
+            const uint8_t c = codes[blk * 8 + i];
+            part += T.e2m1[c & 15] * v[blk * 16 + 2 * i] + T.e2m1[c >> 4] * v[blk * 16 + 2 * i + 1];
+        }
+        acc += part * T.e4m3[sc[blk]];
+    }
+    return acc * f16_to_f(g);
+}
+
+// Columns [n0, n1) of a transposed mxfp4 matrix (blocks [K/2, N], scales [K/32, N],
+// bias [N]) against v[K]: out[n] = sum_k w(n, k) v[k] + bias[n].
+void cols_dot(const uint8_t *const *b, int which, int64_t N, int64_t K, const float *v, int64_t n0, int64_t n1,
+              float *out) {
+    const Tables &T = tables();
+    const uint8_t *blocks = b[3 * which], *scales = b[3 * which + 1];
+    const uint16_t *bias = reinterpret_cast<const uint16_t *>(b[3 * which + 2]);
+    std::vector<float> part(static_cast<size_t>(n1 - n0));
+    for (int64_t n = n0; n < n1; n++) out[n - n0] = 0.f;
+    for (int64_t blk = 0; blk < K / 32; blk++) {
+        std::fill(part.begin(), part.end(), 0.f);
+        for (int64_t i = blk * 16; i < blk * 16 + 16; i++) {
+            const uint8_t *row = blocks + i * N;
+            const float x0 = v[2 * i], x1 = v[2 * i + 1];
+            for (int64_t n = n0; n < n1; n++) {
+                const uint8_t c = row[n];
+                part[n - n0] += T.e2m1[c & 15] * x0 + T.e2m1[c >> 4] * x1;
+            }
+        }
+        const uint8_t *srow = scales + blk * N;
+        for (int64_t n = n0; n < n1; n++) out[n - n0] += part[n - n0] * std::ldexp(1.0f, static_cast<int>(srow[n]) - 127);
+    }
+    for (int64_t n = n0; n < n1; n++) out[n - n0] += bf16_to_f(bias[n]);
+}
+
+}  // namespace
+
+extern "C" int ftmoe_cpu_expert_ffn(int32_t format, int32_t H, int32_t I, int32_t bs, int32_t topk,
+                                    const int32_t *h_topk_ids, const int32_t *h_slots,
+                                    const void *const *h_layer_banks, const int64_t *bank_bytes,
+                                    const uint16_t *h_x, const float *h_weights, float *h_y,
+                                    int32_t threads) {
+    if (format != FTMOE_FMT_BF16 && format != FTMOE_FMT_NVFP4 && format != FTMOE_FMT_MXFP4) return FTMOE_ERR_FORMAT;
+    if (H <= 0 || I <= 0 || bs < 0 || topk <= 0 || !h_topk_ids || !h_slots || !h_layer_banks || !bank_bytes ||
+        !h_x || !h_weights || !h_y)
+        return FTMOE_ERR_INVALID_ARG;
+    const int q = format == FTMOE_FMT_BF16 ? 8 : 32;
+    if (H % q || I % q) return FTMOE_ERR_FORMAT;
+    const int nb = format == FTMOE_FMT_BF16 ? 2 : 6;
+    if (threads <= 0) threads = static_cast<int>(std::max(1u, std::thread::hardware_concurrency()));
+
+    // pairs computed here: routed positions whose slot is -1
+    std::vector<int> pairs;
+    for (int64_t p = 0; p < (int64_t)bs * topk; p++)
+        if (h_slots[p] == -1) pairs.push_back(static_cast<int>(p));
+    std::fill(h_y, h_y + (int64_t)bs * H, 0.f);
+    if (pairs.empty()) return FTMOE_OK;
+    const int64_t np = static_cast<int64_t>(pairs.size());
+    std::vector<const uint8_t *> eb(static_cast<size_t>(np * nb));
+    for (int64_t i = 0; i < np; i++) {
+        const int e = h_topk_ids[pairs[i]];
+        if (e < 0) return FTMOE_ERR_ID_RANGE;
+        for (int b = 0; b < nb; b++)
+            eb[i * nb + b] = static_cast<const uint8_t *>(h_layer_banks[b]) + (int64_t)e * bank_bytes[b];
+    }
+    std::vector<float> xs(static_cast<size_t>(np * H)), hs(static_cast<size_t>(np * I)),
+        os(static_cast<size_t>(np * H));
+    for (int64_t i = 0; i < np; i++) {
+        const int64_t t = pairs[i] / topk;
+        for (int64_t k = 0; k < H; k++) xs[i * H + k] = bf16_to_f(h_x[t * H + k]);
+    }
+    if (format == FTMOE_FMT_MXFP4) {
+        // gate_up: columns split over the workers, in chunks of 64 columns per pair
+        const int64_t chunk = 64, nch = (I + chunk - 1) / chunk;
+        parallel_for(np * nch, threads, [&](int64_t a, int64_t b) {
+            std::vector<float> g(chunk), u(chunk);
+            for (int64_t w = a; w < b; w++) {
+                const int64_t i = w / nch, c0 = (w % nch) * chunk, c1 = std::min<int64_t>(I, c0 + chunk);
+                const uint8_t *const *bk = &eb[i * nb];
+                cols_dot(bk, 0, 2 * (int64_t)I, H, &xs[i * H], c0, c1, g.data());
+                cols_dot(bk, 0, 2 * (int64_t)I, H, &xs[i * H], I + c0, I + c1, u.data());
+                for (int64_t n = c0; n < c1; n++) hs[i * I + n] = silu(g[n - c0]) * u[n - c0];
+            }
+        });
+        const int64_t nchd = (H + chunk - 1) / chunk;
+        parallel_for(np * nchd, threads, [&](int64_t a, int64_t b) {
+            for (int64_t w = a; w < b; w++) {
+                const int64_t i = w / nchd, c0 = (w % nchd) * chunk, c1 = std::min<int64_t>(H, c0 + chunk);
+                cols_dot(&eb[i * nb], 1, H, I, &hs[i * I], c0, c1, &os[i * H + c0]);
+            }
+        });
+    } else {
+        parallel_for(np * I, threads, [&](int64_t a, int64_t b) {
+            for (int64_t w = a; w < b; w++) {
+                const int64_t i = w / I, n = w % I;
+                const uint8_t *const *bk = &eb[i * nb];
+                const float g = row_dot(format, bk, 0, n, H, &xs[i * H]);
+                const float u = row_dot(format, bk, 0, I + n, H, &xs[i * H]);
+                hs[i * I + n] = silu(g) * u;
+            }
+        });
+        parallel_for(np * H, threads, [&](int64_t a, int64_t b) {
+            for (int64_t w = a; w < b; w++) {
+                const int64_t i = w / H, n = w % H;
+                os[i * H + n] = row_dot(format, &eb[i * nb], 1, n, I, &hs[i * I]);
+            }
+        });
+    }
+    // combine in routed order (fixed summation order)
+    for (int64_t i = 0; i < np; i++) {
+        const int64_t p = pairs[i], t = p / topk;
+        const float w = h_weights[p];
+        for (int64_t n = 0; n < H; n++) h_y[t * H + n] += w * os[i * H + n];
+    }
+    return FTMOE_OK;
+}

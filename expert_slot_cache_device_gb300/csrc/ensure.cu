@@ -20,6 +20,8 @@
 //      network for larger S); the j-th smallest key is the j-th victim —
 //      exactly the lowest-(stamp, slot) rule;
 //   5. tables are updated and every routed position gets its slot.
+// The hybrid variant (benchmark guide, section 5.4) fetches only the first `cap`
+// misses in ascending flat id; the overflow keeps slot -1 for the CPU executor.
 // Errors (id out of range, clock exhausted, too many misses) write only the
 // status word, -1 slots and an empty miss list.
 #include "internal.cuh"
@@ -109,7 +111,7 @@ __global__ void __launch_bounds__(kThreads) ensure_kernel(EnsureParams p) {
     int32_t *s_owner = s_miss + p.maxm;                           // [S]
     unsigned char *s_hit = reinterpret_cast<unsigned char *>(s_owner + p.S);  // [S]
     __shared__ int warp_tot[32];
-    __shared__ int s_bad_id, s_m, s_h, s_tmp;
+    __shared__ int s_bad_id, s_m, s_mfull, s_h, s_tmp;
 
     const int tid = threadIdx.x, nt = blockDim.x;
     const int E = p.E, S = p.S;
@@ -169,7 +171,17 @@ __global__ void __launch_bounds__(kThreads) ensure_kernel(EnsureParams p) {
             base += s_tmp;  // every thread reads the same total (synchronised in the scan)
             __syncthreads();
         }
-        if (tid == 0) s_m = base;
+        if (tid == 0) {
+            s_mfull = base;
+            int m = base;
+            if (p.hybrid) {  // fetch only the first `cap` misses (ascending flat id)
+                int cap = p.max_fetch >= 0 ? p.max_fetch
+                                           : (p.fetch_fraction > 0.f ? (int)rintf((float)base * p.fetch_fraction) : 1);
+                if (cap < 0) cap = 0;
+                if (m > cap) m = cap;
+            }
+            s_m = m;
+        }
         __syncthreads();
         if (s_m > S - s_h) err = FTMOE_ERR_CAPACITY;
     }
@@ -177,6 +189,7 @@ __global__ void __launch_bounds__(kThreads) ensure_kernel(EnsureParams p) {
         for (int t = tid; t < p.n; t += nt) p.slots_out[t] = -1;
         if (tid == 0) {
             *p.t.num_miss = 0;
+            if (p.counts) p.counts[0] = p.counts[1] = 0;
             set_status(p.t.status, err);
         }
         return;
@@ -222,6 +235,10 @@ __global__ void __launch_bounds__(kThreads) ensure_kernel(EnsureParams p) {
     if (tid == 0) {
         *p.t.clock = now;
         *p.t.num_miss = m;
+        if (p.counts) {
+            p.counts[0] = m;
+            p.counts[1] = s_mfull;
+        }
     }
 }
 

@@ -120,6 +120,7 @@ __global__ void __launch_bounds__(1024) ffn_route_kernel(FfnParams p) {
     __syncthreads();
     for (int q = tid; q < p.P; q += nt) {
         int s = p.slots[q];
+        if (s == -1) continue;  // computed elsewhere (hybrid CPU executor)
         if ((unsigned)s >= (unsigned)p.S)
             s_bad = 1;
         else
@@ -156,7 +157,9 @@ __global__ void __launch_bounds__(1024) ffn_route_kernel(FfnParams p) {
     }
     if (tid == 0 && p.s.n_passes) *p.s.n_passes = base_p;
     for (int q = tid; q < p.P; q += nt) {
-        int pos = atomicAdd(&cnt[p.slots[q]], 1);
+        const int s = p.slots[q];
+        if (s < 0) continue;
+        int pos = atomicAdd(&cnt[s], 1);
         p.s.upairs[pos] = q;
     }
     if (tid == 0) *p.s.n_unique = base_u;
@@ -678,16 +681,21 @@ __global__ void __launch_bounds__(kThreads) ffn_combine_kernel(FfnParams p) {
     const float4 *o4 = reinterpret_cast<const float4 *>(p.s.o);
     const int64_t h4 = H >> 2;
     // load a group of routed positions before using any of them (independent L2 reads)
+    if (p.addend) acc = reinterpret_cast<const float4 *>(p.addend + (int64_t)t * H)[n4];
     for (int j0 = 0; j0 < p.topk; j0 += 8) {
         float4 ov[8];
         float wv[8];
 #pragma unroll
         for (int jj = 0; jj < 8; jj++) {
             const int j = j0 + jj;
+            wv[jj] = 0.f;
+            ov[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (j < p.topk) {
                 const int q = t * p.topk + j;
-                wv[jj] = p.weights[q];
-                ov[jj] = o4[(int64_t)q * h4 + n4];
+                if (p.slots[q] >= 0) {  // slot -1: the pair is computed elsewhere
+                    wv[jj] = p.weights[q];
+                    ov[jj] = o4[(int64_t)q * h4 + n4];
+                }
             }
         }
 #pragma unroll

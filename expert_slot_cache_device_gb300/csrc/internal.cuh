@@ -30,6 +30,12 @@ struct EnsureParams {
     int32_t E, L, S, layer, n;
     int32_t Spad;         // power of two >= S (bitonic sort width)
     int32_t maxm;         // min(E, S)
+    // hybrid fetch cap: hybrid = 0 fetches every miss; otherwise cap = max_fetch when
+    // max_fetch >= 0, else rint(float(misses) * fetch_fraction) when fetch_fraction > 0,
+    // else 1. counts (nullable): [fetched, misses before the cap].
+    int32_t hybrid, max_fetch;
+    float fetch_fraction;
+    int32_t *counts;
 };
 size_t ensure_smem_bytes(int E, int S, int Spad, int maxm);
 cudaError_t launch_ensure(const EnsureParams &p, cudaStream_t st);
@@ -85,6 +91,7 @@ struct FfnParams {
     const uint16_t *x;      // [bs, H] bf16
     const int32_t *slots;   // [P]
     const float *weights;   // [P]
+    const float *addend;    // [bs, H] fp32 added before the final round (nullable)
     uint16_t *y;            // [bs, H] bf16
     int32_t *status;
     int32_t fmt, H, I, S, bs, topk, P;

@@ -28,7 +28,8 @@ EXPORTS = [
     "ftmoe_cache_workspace_bytes", "ftmoe_cache_create", "ftmoe_cache_destroy", "ftmoe_ensure_experts",
     "ftmoe_copy_missing", "ftmoe_expert_ffn", "ftmoe_set_copy_mode", "ftmoe_cache_get_state",
     "ftmoe_cache_set_state", "ftmoe_get_miss_list", "ftmoe_get_device_status", "ftmoe_h2d_stream_copy",
-    "ftmoe_last_error", "ftmoe_expert_ffn_noalloc",
+    "ftmoe_last_error", "ftmoe_expert_ffn_noalloc", "ftmoe_ensure_experts_hybrid", "ftmoe_hybrid_fetch_fraction",
+    "ftmoe_expert_ffn_hybrid", "ftmoe_cpu_expert_ffn",
 ]
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -77,6 +78,10 @@ def lib() -> ctypes.CDLL:
         "ftmoe_get_device_status": [P, P, P],
         "ftmoe_h2d_stream_copy": [P, P, sz, P],
         "ftmoe_expert_ffn_noalloc": [i32, ctypes.POINTER(P), i32, i32, i32, i32, P, i32, P, P, i32, P, P],
+        "ftmoe_ensure_experts_hybrid": [P, i32, P, i32, i32, i32, ctypes.c_float, P, P, P],
+        "ftmoe_hybrid_fetch_fraction": [ctypes.c_double, ctypes.c_double, P],
+        "ftmoe_expert_ffn_hybrid": [P, P, i32, P, P, i32, P, P, P],
+        "ftmoe_cpu_expert_ffn": [i32, i32, i32, i32, i32, P, P, P, P, P, P, P, i32],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -175,3 +180,29 @@ def ftmoe_expert_ffn_noalloc(fmt: int, d_slot_banks, S: int, H: int, I: int, d_x
     banks = (ctypes.c_void_p * len(d_slot_banks))(*d_slot_banks)
     _check(lib().ftmoe_expert_ffn_noalloc(fmt, banks, len(d_slot_banks), S, H, I, d_x, bs, d_slots, d_weights,
                                           topk, d_y, stream))
+
+
+def ftmoe_ensure_experts_hybrid(cache: int, layer: int, d_topk_ids: int, bs: int, topk: int, max_fetch: int,
+                                fetch_fraction: float, d_slots_out: int, d_counts: int, stream: int) -> None:
+    _check(lib().ftmoe_ensure_experts_hybrid(cache, layer, d_topk_ids, bs, topk, max_fetch, fetch_fraction,
+                                             d_slots_out, d_counts, stream))
+
+
+def ftmoe_hybrid_fetch_fraction(pcie_gbps: float, cpu_gbps: float) -> float:
+    out = ctypes.c_float(0.0)
+    _check(lib().ftmoe_hybrid_fetch_fraction(pcie_gbps, cpu_gbps, ctypes.byref(out)))
+    return out.value
+
+
+def ftmoe_expert_ffn_hybrid(cache: int, d_x: int, bs: int, d_slots: int, d_weights: int, topk: int, d_addend: int,
+                            d_y: int, stream: int) -> None:
+    _check(lib().ftmoe_expert_ffn_hybrid(cache, d_x, bs, d_slots, d_weights, topk, d_addend, d_y, stream))
+
+
+def ftmoe_cpu_expert_ffn(fmt: int, H: int, I: int, bs: int, topk: int, h_topk_ids: int, h_slots: int,
+                         h_layer_banks, bank_bytes, h_x: int, h_weights: int, h_y: int, threads: int = 0) -> None:
+    """Host CPU executor of the hybrid path (all pointers are host addresses)."""
+    banks = (ctypes.c_void_p * len(h_layer_banks))(*h_layer_banks)
+    bb = (ctypes.c_int64 * len(bank_bytes))(*bank_bytes)
+    _check(lib().ftmoe_cpu_expert_ffn(fmt, H, I, bs, topk, h_topk_ids, h_slots, banks, bb, h_x, h_weights, h_y,
+                                      threads))

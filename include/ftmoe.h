@@ -164,11 +164,60 @@ int ftmoe_copy_missing(ftmoe_cache_t *cache, void *stream);
  *     o  = W_d[s] h (+ b_d),     y_t = sum_j d_weights[t, j] * o
  * with fp32 accumulation and one final round to bf16. d_x_bf16 [bs, H] bf16,
  * d_slots [bs, topk] int32, d_weights [bs, topk] fp32, d_y_bf16 [bs, H] bf16 (all
- * device). Slots must be in [0, S) and bs * topk <= max_pairs of create. Uses the
- * FFN scratch of the cache workspace, so FFN calls on one cache must not overlap. */
+ * device). Slots must be in [0, S), or -1 for a position computed elsewhere (the hybrid
+ * CPU executor), which then contributes nothing; any other slot is a device error
+ * (y left unwritten, status FTMOE_ERR_INVALID_ARG). bs * topk <= max_pairs of create.
+ * Uses the FFN scratch of the cache workspace, so FFN calls on one cache must not
+ * overlap. */
 int ftmoe_expert_ffn(ftmoe_cache_t *cache, const void *d_x_bf16, int32_t bs,
                      const int32_t *d_slots, const float *d_weights, int32_t topk,
                      void *d_y_bf16, void *stream);
+
+/* Hybrid ensure_experts (benchmark guide, section 5.4: in hybrid mode only a capped
+ * number of misses is fetched per step; the overflow is rewritten to -1 and computed by
+ * the CPU executor; num_indices and num_missing_full count the capped and the uncapped
+ * misses). As ftmoe_ensure_experts, except that only the first `cap` misses in
+ * ascending flat id get slots (and are copied by the next ftmoe_copy_missing); the
+ * other misses leave the cache untouched and their routed positions get slot -1.
+ *   cap = max_fetch                                     if max_fetch >= 0,
+ *       = rint(float(misses) * fetch_fraction) (binary32, half to even)
+ *                                                       if max_fetch < 0 and fetch_fraction > 0,
+ *       = 1                                             otherwise (no bandwidth profile).
+ * d_counts (device int32[2], may be NULL) receives {fetched, misses before the cap}. */
+int ftmoe_ensure_experts_hybrid(ftmoe_cache_t *cache, int32_t layer, const int32_t *d_topk_ids,
+                                int32_t bs, int32_t topk, int32_t max_fetch, float fetch_fraction,
+                                int32_t *d_slots_out, int32_t *d_counts, void *stream);
+
+/* Fetch share of the hybrid split (benchmark guide, section 5.4: PCIe-fetched experts :
+ * CPU-computed experts = pcie_bw : (cpu_bw - pcie_bw), i.e. pcie_bw / cpu_bw of the
+ * misses are fetched). *out = pcie_gbps / cpu_gbps when cpu_gbps > pcie_gbps > 0, 1 when
+ * 0 < cpu_gbps <= pcie_gbps (the link is the faster path), 0 when either is <= 0 (no
+ * profile: ftmoe_ensure_experts_hybrid then falls back to a cap of 1). Host only. */
+int ftmoe_hybrid_fetch_fraction(double pcie_gbps, double cpu_gbps, float *out);
+
+/* Expert FFN of the hybrid path: as ftmoe_expert_ffn (which is this call with
+ * d_addend = NULL), plus an optional device fp32 [bs, H] addend (the CPU executor's
+ * partial output) added to every token's sum before the single round to bf16. Routed
+ * positions with slot -1 contribute nothing here. */
+int ftmoe_expert_ffn_hybrid(ftmoe_cache_t *cache, const void *d_x_bf16, int32_t bs,
+                            const int32_t *d_slots, const float *d_weights, int32_t topk,
+                            const float *d_addend, void *d_y_bf16, void *stream);
+
+/* CPU expert executor of the hybrid path (benchmark guide, section 5.4; architecture
+ * deep-dive, section 五: the CPU side computes experts by GEMV from the host banks).
+ * Host-side, synchronous, multi-threaded (threads <= 0: all hardware threads). For every
+ * routed position (t, j) with h_slots[t, j] == -1 it computes the expert FFN of expert
+ * h_topk_ids[t, j] from the layer's host banks and accumulates it into h_y:
+ *     h_y[t, :] = sum over those j of h_weights[t, j] * down(silu(gate) * up)(x_t)
+ * in fp32 (h_y [bs, H] fp32 is overwritten; tokens without CPU pairs get 0).
+ * h_layer_banks[b] points at the layer's [E, bank_bytes[b]] host bank b in the schema
+ * order of `format` (FTMOE_FMT_BF16 / NVFP4 / MXFP4); h_x is bf16 [bs, H]. All pointers
+ * are host pointers. */
+int ftmoe_cpu_expert_ffn(int32_t format, int32_t H, int32_t I, int32_t bs, int32_t topk,
+                         const int32_t *h_topk_ids, const int32_t *h_slots,
+                         const void *const *h_layer_banks, const int64_t *bank_bytes,
+                         const uint16_t *h_x, const float *h_weights, float *h_y,
+                         int32_t threads);
 
 /* Select the copy_missing implementation (FTMOE_COPY_*). */
 int ftmoe_set_copy_mode(ftmoe_cache_t *cache, int32_t mode);

@@ -1,0 +1,70 @@
+"""The hybrid path's CPU expert executor (host code of libftmoe) against the oracle.
+
+FreeToken benchmark guide, section 5.4: misses beyond the fetch cap get slot -1 and are
+computed by a CPU executor from the host banks. This runs on the CPU only: for every
+format, the executor's fp32 partial output over the -1 positions must match the fp64
+oracle FFN restricted to those positions.
+"""
+import numpy as np
+import pytest
+
+from expert_slot_cache_device_gb300 import build as B
+from expert_slot_cache_device_gb300 import ftmoe as F
+from expert_slot_cache_device_gb300 import workload as wl
+
+CASES = [("bf16", dict(E=6, H=264, I=72)), ("nvfp4", dict(E=5, H=320, I=96)), ("mxfp4", dict(E=5, H=160, I=96)),
+         ("mxfp4", dict(E=4, H=576, I=320))]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return F.lib()
+
+
+@pytest.mark.parametrize("fmt,geo", CASES)
+def test_cpu_executor_matches_oracle(lib, orc, fmt, geo):
+    base = {"bf16": "c2", "nvfp4": "c3", "mxfp4": "c4"}[fmt]
+    cfg = wl.scaled(wl.CONFIGS[base], topk=3, L=2, S=4, **geo)
+    banks = wl.make_banks(cfg)
+    rng = np.random.default_rng(geo["H"])
+    bs = 5
+    ids = np.stack([rng.choice(cfg.E, cfg.topk, replace=False) for _ in range(bs)]).astype(np.int32)
+    slots = rng.integers(0, cfg.S, ids.shape).astype(np.int32)
+    cpu_mask = rng.random(ids.shape) < 0.6
+    cpu_mask[0, :] = True
+    slots[cpu_mask] = -1
+    w = rng.random(ids.shape).astype(np.float32)
+    x = wl.f32_to_bf16_bits(rng.standard_normal((bs, cfg.H)).astype(np.float32))
+    y = np.empty((bs, cfg.H), np.float32)
+    F.ftmoe_cpu_expert_ffn(F.FORMATS[fmt], cfg.H, cfg.I, bs, cfg.topk, ids.ctypes.data, slots.ctypes.data,
+                           [b.ctypes.data for b in banks], [b.shape[1] for b in banks], x.ctypes.data, w.ctypes.data,
+                           y.ctypes.data, 4)
+    w_cpu = np.where(cpu_mask, w, 0.0).astype(np.float32)
+    pairs = [[b[int(e)] for b in banks] for e in ids.reshape(-1)]
+    ref = orc.expert_ffn(fmt, cfg.H, cfg.I, pairs, x, w_cpu)
+    err = np.abs(y - ref).max()
+    l2 = np.linalg.norm(y - ref) / np.linalg.norm(ref)
+    assert err <= 1e-4 and l2 <= 1e-5, (err, l2)  # fp32 accumulation against fp64
+
+
+def test_cpu_executor_no_cpu_pairs_gives_zero(lib):
+    cfg = wl.scaled(wl.CONFIGS["c2"], E=2, H=64, I=32, topk=1)
+    banks = wl.make_banks(cfg)
+    ids = np.zeros((2, 1), np.int32)
+    slots = np.zeros((2, 1), np.int32)
+    x = np.zeros((2, 64), np.uint16)
+    w = np.ones((2, 1), np.float32)
+    y = np.full((2, 64), 7.0, np.float32)
+    F.ftmoe_cpu_expert_ffn(F.FMT_BF16, 64, 32, 2, 1, ids.ctypes.data, slots.ctypes.data,
+                           [b.ctypes.data for b in banks], [b.shape[1] for b in banks], x.ctypes.data, w.ctypes.data,
+                           y.ctypes.data, 2)
+    assert (y == 0).all()
+
+
+def test_fetch_fraction_helper(lib):
+    assert F.ftmoe_hybrid_fetch_fraction(200.0, 800.0) == pytest.approx(0.25)
+    assert F.ftmoe_hybrid_fetch_fraction(200.0, 150.0) == 1.0
+    assert F.ftmoe_hybrid_fetch_fraction(0.0, 800.0) == 0.0
+    with pytest.raises(F.FtmoeError):
+        F.ftmoe_cpu_expert_ffn(9, 64, 32, 1, 1, 0, 0, [0, 0], [1, 1], 0, 0, 0, 1)
