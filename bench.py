@@ -51,6 +51,7 @@ def parse():
     ap.add_argument("--repeat", type=int, default=25, help="repeats per sweep point (median)")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-hybrid", action="store_true", help="skip the hybrid-path measurements")
     ap.add_argument("--copy-mode", default="fused", choices=["fused", "per_bank", "engine"])
     ap.add_argument("--experts", type=int, default=0, help="override E (smaller profiling cases)")
     ap.add_argument("--slots", type=int, default=0, help="override S (smaller profiling cases)")
@@ -430,6 +431,8 @@ def run_gpu(args):
         }
         if not args.no_sweep:
             line["sweep"] = sweep(args, cfg, cache, stream, torch, F, wl)
+        if not args.no_hybrid:
+            line["hybrid"] = hybrid_probe(args, cfg, cache, stream, torch, F, wl, link, cpu_cores())
     cache.close()
     if rank == 0 and not args.no_cpu_baseline:
         hb = [cache.host[b][0].numpy() for b in range(cache.nb)]
@@ -446,6 +449,79 @@ def run_gpu(args):
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def hybrid_probe(args, cfg, cache, stream, torch, F, wl, link_gbps, cores):
+    """Hybrid path measurements (benchmark guide, section 5.2 and 5.4): the CPU expert
+    executor's weight bandwidth, the pages' decision rule (hybrid when the CPU MoE GB/s
+    exceed 2x the link's), the fetch fraction pcie/cpu, and timed steps of the hybrid path
+    (ensure_hybrid, then the copy overlapped with the CPU executor, then the GPU FFN with
+    the CPU partial as addend) for the recommended fraction and for an even split."""
+    import threading
+
+    s = stream.cuda_stream
+    B = cfg.bytes_per_expert
+    bank_ptrs = [cache.host_ptrs[b][0] for b in range(cache.nb)]
+    bank_bytes = [g.bytes for g in cache.schema]
+    fmt = F.FORMATS[cfg.fmt]
+    # CPU executor bandwidth: every routed pair of a 2-token batch on distinct experts
+    k = cfg.topk
+    ids = np.arange(2 * k, dtype=np.int32).reshape(2, k) % cfg.E
+    sl = np.full((2, k), -1, np.int32)
+    x = np.zeros((2, cfg.H), np.uint16)
+    w = np.ones((2, k), np.float32)
+    y = np.empty((2, cfg.H), np.float32)
+    times = []
+    for _ in range(3):
+        t0 = time.perf_counter()
+        F.ftmoe_cpu_expert_ffn(fmt, cfg.H, cfg.I, 2, k, ids.ctypes.data, sl.ctypes.data, bank_ptrs, bank_bytes,
+                               x.ctypes.data, w.ctypes.data, y.ctypes.data, cores)
+        times.append(time.perf_counter() - t0)
+    cpu_gbps = 2 * k * B / min(times) / 1e9
+    frac = F.ftmoe_hybrid_fetch_fraction(link_gbps, cpu_gbps)
+    out = {"cpu_moe_GBps": cpu_gbps, "link_GBps": link_gbps, "cores": cores,
+           "decision": "hybrid" if cpu_gbps > 2 * link_gbps else "offload", "fetch_fraction": frac}
+
+    r = wl.make_route(cfg, args.bs, args.miss_rate)
+    install_hits(cache, r)
+    d_ids = torch.from_numpy(r.topk_ids).cuda()
+    d_slots = torch.empty_like(d_ids)
+    d_counts = torch.zeros(2, dtype=torch.int32, device="cuda")
+    d_w = torch.from_numpy(r.weights).cuda()
+    d_x = torch.from_numpy(r.x.view(np.int16).copy()).view(torch.bfloat16).cuda()
+    d_y = torch.empty((args.bs, cfg.H), dtype=torch.bfloat16, device="cuda")
+    d_add = torch.zeros((args.bs, cfg.H), dtype=torch.float32, device="cuda")
+    h_add = torch.zeros((args.bs, cfg.H), dtype=torch.float32).pin_memory()
+
+    def run(max_fetch, fraction, reps=5):
+        best = None
+        for _ in range(reps):
+            cache.set_state(r.owner, r.stamp, r.clock, stream=s)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            F.ftmoe_ensure_experts_hybrid(cache.handle, 0, d_ids.data_ptr(), args.bs, cfg.topk, max_fetch, fraction,
+                                          d_slots.data_ptr(), d_counts.data_ptr(), s)
+            h_slots = d_slots.cpu().numpy()  # the host needs the CPU positions
+            F.ftmoe_copy_missing(cache.handle, s)  # the link copy runs while the CPU computes
+            F.ftmoe_cpu_expert_ffn(fmt, cfg.H, cfg.I, args.bs, cfg.topk, r.topk_ids.ctypes.data, h_slots.ctypes.data,
+                                   bank_ptrs, bank_bytes, r.x.ctypes.data, r.weights.ctypes.data,
+                                   h_add.data_ptr(), cores)
+            with torch.cuda.stream(stream):
+                d_add.copy_(h_add, non_blocking=True)
+            F.ftmoe_expert_ffn_hybrid(cache.handle, d_x.data_ptr(), args.bs, d_slots.data_ptr(), d_w.data_ptr(),
+                                      cfg.topk, d_add.data_ptr(), d_y.data_ptr(), s)
+            torch.cuda.synchronize()
+            dt = time.perf_counter() - t0
+            counts = d_counts.cpu().tolist()
+            if best is None or dt < best[0]:
+                best = (dt, counts)
+        return {"step_ms": best[0] * 1e3, "fetched": best[1][0], "misses": best[1][1]}
+
+    out["recommended"] = run(-1, frac)
+    out["half_split"] = run(max(0, r.misses // 2), 0.0)
+    out["offload"] = run(r.misses, 0.0)
+    assert cache.status() == F.OK
+    return out
 
 
 def sweep(args, cfg, cache, stream, torch, F, wl):

@@ -42,7 +42,8 @@ def test_hybrid_ensure_random_traces(seed):
         max_fetch = int(rng.integers(-1, 5))
         frac = float(rng.choice([0.0, 0.25, 0.5, 0.8]))
         rc, slots, mids, msl, counts = orc.ensure_hybrid(layer, ids, max_fetch, frac)
-        F.ftmoe_ensure_experts_hybrid(cache.handle, layer, to_dev(ids).data_ptr(), 2, k, max_fetch, frac,
+        d_ids = to_dev(ids)
+        F.ftmoe_ensure_experts_hybrid(cache.handle, layer, d_ids.data_ptr(), 2, k, max_fetch, frac,
                                       d_slots.data_ptr(), d_counts.data_ptr(), st)
         cache.copy_missing()
         assert cache.status() == rc
@@ -90,10 +91,14 @@ def test_hybrid_step_matches_oracle(key, geo, bs, mr, max_fetch):
                            h_slots.ctypes.data, [cache.host_ptrs[b][0] for b in range(cache.nb)],
                            [g.bytes for g in cache.schema], r.x.ctypes.data, r.weights.ctypes.data, y_cpu.ctypes.data,
                            0)
+    # keep every device tensor referenced until the kernels have run (a temporary's
+    # memory could be handed to the next allocation before the FFN reads it)
     d_add = torch.from_numpy(y_cpu).cuda()
+    d_x = x_dev(r.x)
+    d_w = to_dev(r.weights)
     d_y = torch.empty((bs, cfg.H), dtype=torch.bfloat16, device="cuda")
-    F.ftmoe_expert_ffn_hybrid(cache.handle, x_dev(r.x).data_ptr(), bs, d_slots.data_ptr(),
-                              to_dev(r.weights).data_ptr(), cfg.topk, d_add.data_ptr(), d_y.data_ptr(), st)
+    F.ftmoe_expert_ffn_hybrid(cache.handle, d_x.data_ptr(), bs, d_slots.data_ptr(), d_w.data_ptr(), cfg.topk,
+                              d_add.data_ptr(), d_y.data_ptr(), st)
     assert cache.status() == F.OK
     toks = list(range(min(bs, 4)))
     ref = oracle_ffn(cache, 0, r.topk_ids, r.weights, r.x, toks)
