@@ -163,6 +163,16 @@ __device__ __forceinline__ float dot16_e2m1_f16(const uint32_t (&w)[8], const ui
     return f.x + f.y;
 }
 
+// Four e2m1 codes (16 bits) -> two f16x2 registers (low nibble first).
+__device__ __forceinline__ void e2m1x4_h2(uint32_t v16, uint32_t (&h)[2]) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t}"
+        : "=r"(h[0]), "=r"(h[1])
+        : "r"(v16));
+}
+
 // Eight fp32 values scaled by `sc` (a power of two) -> four f16x2 registers.
 __device__ __forceinline__ void f32x8_to_h2(const float (&v)[8], float sc, uint32_t (&h)[4]) {
 #pragma unroll
@@ -171,6 +181,69 @@ __device__ __forceinline__ void f32x8_to_h2(const float (&v)[8], float sc, uint3
         h[i] = *reinterpret_cast<const uint32_t *>(&t);
     }
 }
+
+// Two e4m3 bytes (low byte first) -> f16x2 (exact: every e4m3 value is an f16 normal).
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t two_bytes) {
+    uint32_t h;
+    asm("{\n\t.reg .b16 s;\n\t"
+        "cvt.u16.u32 s, %1;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, s;\n\t}"
+        : "=r"(h)
+        : "r"(two_bytes & 0xffffu));
+    return h;
+}
+
+// Low / high f16 of a packed pair as a 16-bit register value.
+__device__ __forceinline__ uint16_t h2_lo(uint32_t h) { return static_cast<uint16_t>(h & 0xffffu); }
+__device__ __forceinline__ uint16_t h2_hi(uint32_t h) { return static_cast<uint16_t>(h >> 16); }
+
+// c + a.lo * s + a.hi * s with f16 multiplicands and fp32 addition (the f16 x f16
+// products are exact in fp32): applies a block scale to an f16x2 partial sum.
+__device__ __forceinline__ float fma_h2_scale(uint32_t a, uint16_t s, float c) {
+    asm("{\n\t.reg .f16 a0, a1;\n\t"
+        "mov.b32 {a0, a1}, %1;\n\t"
+        "fma.rn.f32.f16 %0, a0, %2, %0;\n\t"
+        "fma.rn.f32.f16 %0, a1, %2, %0;\n\t}"
+        : "+f"(c)
+        : "r"(a), "h"(s));
+    return c;
+}
+
+// Sixteen e2m1 codes (eight f16x2 registers) against sixteen f16 activations, left as
+// two f16 partial sums of eight exact products each (|x| < 2^10 keeps every partial
+// below 8 * 6 * 2^10 = 49152 < 65504).
+__device__ __forceinline__ uint32_t dot16_e2m1_h2(const uint32_t (&w)[8], const uint32_t (&x)[8]) {
+    __half2 acc = __hmul2(*reinterpret_cast<const __half2 *>(&w[0]), *reinterpret_cast<const __half2 *>(&x[0]));
+#pragma unroll
+    for (int i = 1; i < 8; i++)
+        acc = __hfma2(*reinterpret_cast<const __half2 *>(&w[i]), *reinterpret_cast<const __half2 *>(&x[i]), acc);
+    return *reinterpret_cast<const uint32_t *>(&acc);
+}
+
+// (x * s, y * s) -> f16x2 (x in the low half): one packed fp32 multiply, one conversion.
+__device__ __forceinline__ uint32_t f2_scale_to_h2(float x, float y, float s) {
+    uint32_t h;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t.reg .f32 lo, hi;\n\t"
+        "mov.b64 ra, {%1, %2};\n\t"
+        "mov.b64 rb, {%3, %3};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {lo, hi}, rd;\n\t"
+        "cvt.rn.f16x2.f32 %0, hi, lo;\n\t}"
+        : "=r"(h)
+        : "f"(x), "f"(y), "f"(s));
+    return h;
+}
+
+// Element layouts of the nvfp4 activation vectors staged in shared memory. A lane
+// handles one 16-element block b per step; storing some of its 16-byte groups in a
+// lane-dependent order makes the quarter-warp phases of 128-bit shared loads hit 32
+// distinct banks without any data-dependent register selection:
+//   f16 activations (32-byte blocks, two 16-byte halves): bit 3 of the element index
+//   is flipped when bit 6 is set, i.e. blocks with b & 4 store their halves swapped;
+//   fp32 h rows (64-byte blocks, four 16-byte quarters): quarter q of block b is stored
+//   at quarter q ^ ((b >> 1) & 3).
+__host__ __device__ __forceinline__ int swz_x16(int k) { return k ^ ((k >> 3) & 8); }
+__host__ __device__ __forceinline__ int swz_h32(int n) { return n ^ ((n >> 3) & 12); }
 
 // Distinct slot u owning pass `pi`: the largest u with upoff[u] <= pi (upoff ascending).
 __device__ __forceinline__ int pass_owner(const int32_t *upoff, int nu, int pi) {

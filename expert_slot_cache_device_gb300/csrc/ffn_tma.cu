@@ -183,11 +183,15 @@ __device__ __forceinline__ void gu_consume(const FfnParams &p, const TmaCfg &c, 
         } else {
             // lane step = one 16-element scale block (two 32-bit code words): codes ->
             // exact f16x2, sixteen exact f16 products summed in two f16 halves of eight,
-            // then fp32 (block scale, accumulation over blocks)
+            // then the block scale applied in fp32 (f16 x f16 products, fp32 sums). The
+            // activations are staged in the swz_x16 layout: this lane's first 16-byte
+            // half of block b sits at group 2b + rot, its second at 2b + (rot ^ 1).
             const uint2 *cg = reinterpret_cast<const uint2 *>(st + j * wr);
             const uint2 *cu = reinterpret_cast<const uint2 *>(st + (R + j) * wr);
             const unsigned char *sg = st + 2 * R * wr + j * sr, *su = st + 2 * R * wr + (R + j) * sr;
             const int nb = H >> 4;
+            const int rot = (lane >> 2) & 1;
+#pragma unroll 2
             for (int b = lane; b < nb; b += 32) {
                 const uint2 ca = cg[b], cb = cu[b];
                 uint32_t fa[8], fb[8];
@@ -195,13 +199,13 @@ __device__ __forceinline__ void gu_consume(const FfnParams &p, const TmaCfg &c, 
                 e2m1x8_h2(ca.y, *reinterpret_cast<uint32_t(*)[4]>(&fa[4]));
                 e2m1x8_h2(cb.x, *reinterpret_cast<uint32_t(*)[4]>(&fb[0]));
                 e2m1x8_h2(cb.y, *reinterpret_cast<uint32_t(*)[4]>(&fb[4]));
-                const float2 sc = e4m3x2_to_f2((uint32_t)sg[b] | ((uint32_t)su[b] << 8));
+                const uint32_t s2 = e4m3x2_to_h2((uint32_t)sg[b] | ((uint32_t)su[b] << 8));
 #pragma unroll
                 for (int t = 0; t < NT; t++) {
-                    const uint4 x0 = xs[t * nxv + 2 * b], x1 = xs[t * nxv + 2 * b + 1];
+                    const uint4 x0 = xs[t * nxv + 2 * b + rot], x1 = xs[t * nxv + 2 * b + (rot ^ 1)];
                     const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-                    g[t] = fmaf(dot16_e2m1_f16(fa, xw), sc.x, g[t]);
-                    u[t] = fmaf(dot16_e2m1_f16(fb, xw), sc.y, u[t]);
+                    g[t] = fma_h2_scale(dot16_e2m1_h2(fa, xw), h2_lo(s2), g[t]);
+                    u[t] = fma_h2_scale(dot16_e2m1_h2(fb, xw), h2_hi(s2), u[t]);
                 }
             }
         }
@@ -211,7 +215,7 @@ __device__ __forceinline__ void gu_consume(const FfnParams &p, const TmaCfg &c, 
             const float gs = warp_sum(g[t]) * gg * xs_t, us = warp_sum(u[t]) * gu * xs_t;
             if (lane == t) {
                 const float hv = silu(gs) * us;
-                p.s.h[(int64_t)h.pairs[t] * I + n] = hv;
+                p.s.h[(int64_t)h.pairs[t] * I + (FMT == FTMOE_FMT_NVFP4 ? swz_h32(n) : n)] = hv;
                 if (FMT == FTMOE_FMT_NVFP4) atomicMax(&p.s.hmax[h.pairs[t]], __float_as_uint(fabsf(hv)));
             }
         }
@@ -234,6 +238,14 @@ __device__ __forceinline__ void dn_consume(const FfnParams &p, const TmaCfg &c, 
         for (int r = 0; r < RR; r++)
 #pragma unroll
             for (int t = 0; t < NT; t++) o[r][t] = 0.f;
+        float gl[RR];  // per-row global scales (nvfp4), loaded before the row loop
+#pragma unroll
+        for (int r = 0; r < RR; r++) {
+            gl[r] = 1.f;
+            if (FMT == FTMOE_FMT_NVFP4 && r < nr)
+                gl[r] = __half2float(*reinterpret_cast<const __half *>(p.bank[5] + (int64_t)h.slot * p.bank_bytes[5] +
+                                                                       2 * (int64_t)(h.n0 + j0 + r)));
+        }
         if (FMT == FTMOE_FMT_BF16) {
             // lane step = 4 consecutive k: 8-byte weight reads and 16-byte h reads are
             // contiguous across lanes (no bank conflicts)
@@ -260,14 +272,16 @@ __device__ __forceinline__ void dn_consume(const FfnParams &p, const TmaCfg &c, 
         } else {
             // lane step = one 16-element scale block (two code words); h is converted once
             // per block and token to f16 with the token's power-of-two scale (max |h| <
-            // 2^10), shared by the RR rows; products summed as in gate_up
+            // 2^10), shared by the RR rows; products summed as in gate_up. The h rows are
+            // staged in the swz_h32 layout: quarter q of this lane's block sits at q ^ rot.
             const int nb = I >> 4;
+            const int rot = (lane >> 1) & 3;
             float hsc[NT];
 #pragma unroll
             for (int t = 0; t < NT; t++) hsc[t] = ldexpf(1.f, -h.texp[t]);
             for (int b = lane; b < nb; b += 32) {
                 uint32_t fa[RR][8];
-                float sc[RR];
+                uint32_t s2[RR / 2];
 #pragma unroll
                 for (int r = 0; r < RR; r += 2) {
                     const int j1 = r < nr ? j0 + r : j0, j2 = r + 1 < nr ? j0 + r + 1 : j0;
@@ -277,22 +291,23 @@ __device__ __forceinline__ void dn_consume(const FfnParams &p, const TmaCfg &c, 
                     e2m1x8_h2(c1.y, *reinterpret_cast<uint32_t(*)[4]>(&fa[r][4]));
                     e2m1x8_h2(c2.x, *reinterpret_cast<uint32_t(*)[4]>(&fa[r + 1][0]));
                     e2m1x8_h2(c2.y, *reinterpret_cast<uint32_t(*)[4]>(&fa[r + 1][4]));
-                    const float2 s2 = e4m3x2_to_f2((uint32_t)st[R * wr + j1 * sr + b] |
-                                                   ((uint32_t)st[R * wr + j2 * sr + b] << 8));
-                    sc[r] = s2.x;
-                    sc[r + 1] = s2.y;
+                    s2[r / 2] = e4m3x2_to_h2((uint32_t)st[R * wr + j1 * sr + b] |
+                                             ((uint32_t)st[R * wr + j2 * sr + b] << 8));
                 }
 #pragma unroll
                 for (int t = 0; t < NT; t++) {
-                    const float4 *hp = hs + t * nh4 + 4 * b;
-                    const float4 h0 = hp[0], h1 = hp[1], h2 = hp[2], h3 = hp[3];
-                    const float hv0[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-                    const float hv1[8] = {h2.x, h2.y, h2.z, h2.w, h3.x, h3.y, h3.z, h3.w};
-                    uint32_t hh2[8];
-                    f32x8_to_h2(hv0, hsc[t], *reinterpret_cast<uint32_t(*)[4]>(&hh2[0]));
-                    f32x8_to_h2(hv1, hsc[t], *reinterpret_cast<uint32_t(*)[4]>(&hh2[4]));
+                    uint32_t hh[8];
 #pragma unroll
-                    for (int r = 0; r < RR; r++) o[r][t] = fmaf(dot16_e2m1_f16(fa[r], hh2), sc[r], o[r][t]);
+                    for (int q = 0; q < 4; q++) {
+                        const float4 hv = hs[t * nh4 + 4 * b + (q ^ rot)];
+                        hh[2 * q] = f2_scale_to_h2(hv.x, hv.y, hsc[t]);
+                        hh[2 * q + 1] = f2_scale_to_h2(hv.z, hv.w, hsc[t]);
+                    }
+#pragma unroll
+                    for (int r = 0; r < RR; r++) {
+                        const uint32_t sr2 = s2[r / 2];
+                        o[r][t] = fma_h2_scale(dot16_e2m1_h2(fa[r], hh), (r & 1) ? h2_hi(sr2) : h2_lo(sr2), o[r][t]);
+                    }
                 }
             }
         }
@@ -300,13 +315,9 @@ __device__ __forceinline__ void dn_consume(const FfnParams &p, const TmaCfg &c, 
         for (int r = 0; r < RR; r++) {
             if (r >= nr) break;
             const int n = h.n0 + j0 + r;
-            float gl = 1.f;
-            if (FMT == FTMOE_FMT_NVFP4)
-                gl = __half2float(*reinterpret_cast<const __half *>(p.bank[5] + (int64_t)h.slot * p.bank_bytes[5] +
-                                                                    2 * (int64_t)n));
 #pragma unroll
             for (int t = 0; t < NT; t++) {
-                const float v = warp_sum(o[r][t]) * gl * (FMT == FTMOE_FMT_NVFP4 ? ldexpf(1.f, h.texp[t]) : 1.f);
+                const float v = warp_sum(o[r][t]) * gl[r] * (FMT == FTMOE_FMT_NVFP4 ? ldexpf(1.f, h.texp[t]) : 1.f);
                 if (lane == t) p.s.o[(int64_t)h.pairs[t] * H + n] = v;
             }
         }

@@ -96,6 +96,7 @@ struct FfnParams {
     int32_t *status;
     int32_t fmt, H, I, S, bs, topk, P;
     int32_t x16_emax;  // f16 activation copy keeps max |x| < 2^x16_emax
+    int32_t x16_swz;   // f16 activation copy stored in the swz_x16 layout (nvfp4 rows kernels)
 };
 
 // Tensor maps (CUtensorMap, 128 bytes each) over the transposed mxfp4 slot banks.
