@@ -1,21 +1,22 @@
-// Transposed mxfp4 expert FFN phases as a persistent, warp-specialised 2-D TMA pipeline.
+// Transposed mxfp4 expert FFN phases as a persistent, warp-specialised bulk-tensor (TMA) pipeline.
 //
 // mxfp4 banks are stored transposed (benchmark guide, section 4.2: "_blocks /
 // _scales / _bias"): blocks [K/2, N] (byte (i, n) holds k = 2i in the low nibble and
 // k = 2i + 1 in the high nibble of output column n), scales [K/32, N] e8m0, bias [N].
-// A work item is (distinct slot u, tile of 128 output columns); it streams the whole
-// reduction axis in stages of kKp = 128 k-pair rows. A producer thread loads each
-// stage with 2-D bulk tensor copies (cp.async.bulk.tensor, one box of 128 columns x
-// 128 rows per matrix plus the 8 matching scale rows, completion on an mbarrier) and
-// a 1-D bulk copy of the tokens' activations for those rows. Eight consumer warps each
-// take one 16-row scale block of the stage: a lane owns 4 adjacent columns, decodes
-// their code bytes to exact f16x2 (k even, k odd), and accumulates with packed f16
-// FMAs against the row's activation pair (a shared-memory broadcast): each f16 half
-// sums 16 exact products of |e2m1| <= 6 and |x| < 2^9, so it stays below 2^15. The
-// block's partial is scaled by 2^(e8m0 - 127) and accumulated in fp32. After the
-// last stage of an item the eight warps' partials meet in shared memory behind an
-// mbarrier (bounded wait), the bias is added, and gate_up writes h = silu(g) * u
-// while down writes o.
+// A work item is (distinct slot u, pass of up to four tokens, tile of 128 output
+// columns); it streams the whole reduction axis in stages of kKp = 256 k-pair rows. A
+// producer thread loads each stage with 3-D bulk tensor copies (cp.async.bulk.tensor
+// over [slot, row, column], one box of 128 columns x 256 rows per matrix plus the 16
+// matching scale rows, completion on an mbarrier; rows past the slot's end are
+// zero-filled) and a 1-D bulk copy of the tokens' activations for those rows. Sixteen
+// consumer warps each take one 16-row scale block of the stage: a lane owns 4 adjacent
+// columns, decodes their code bytes to exact f16x2 (k even, k odd), and accumulates
+// with packed f16 FMAs against the row's activation pair (a shared-memory broadcast):
+// each f16 half sums 16 exact products of |e2m1| <= 6 and |x| < 2^9, so it stays below
+// 2^15. The block's partial is scaled by 2^(e8m0 - 127) and accumulated in fp32. After
+// the last stage of an item each warp writes its partials over its own (consumed) code
+// block of that stage, the warps meet behind an mbarrier (bounded wait), the bias is
+// added, and gate_up writes h = silu(g) * u while down writes o.
 //
 // Activations: gate_up uses the f16 copy of x (per-token power-of-two scale, max
 // |x| < 2^9); down converts the fp32 h rows with the per-pair power-of-two scale
@@ -36,6 +37,7 @@ constexpr int kKp = 256;                    // k-pair rows per stage (16 blocks 
 constexpr int kCols = 128;                  // output columns per item
 constexpr int kMxStagesMax = 4;
 constexpr int kMxTokMax = 4;
+static_assert(kMxTokMax * kCols * 4 <= 16 * kCols, "a warp's partials fit its 16-row code block");
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 enum { kGU = 0, kDN = 1 };
@@ -47,7 +49,7 @@ struct MxHdr {
 };
 
 struct MxCfg {
-    int32_t tiles, kst, stages, stage_bytes, tok_off, tok_bytes, sc_off, tg, red_off;
+    int32_t tiles, kst, stages, stage_bytes, tok_off, tok_bytes, sc_off, tg;
 };
 
 __device__ __forceinline__ uint32_t su32(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
@@ -83,11 +85,11 @@ __device__ __forceinline__ bool bar_wait(uint64_t *b, uint32_t parity) {
     }
 }
 
-__device__ __forceinline__ void tma2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+__device__ __forceinline__ void tma3d(void *dst, const CUtensorMap *map, int x, int y, int z, uint64_t *bar) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-        "[%4];" ::"r"(su32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(su32(bar))
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(su32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(su32(bar))
         : "memory");
 }
 
@@ -165,7 +167,6 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     uint64_t *rbar = empty + kMxStagesMax;  // [2] consumer barriers around the reduction
     MxHdr *hdr = reinterpret_cast<MxHdr *>(sm + 256);
     unsigned char *stage0 = sm + 256 + kMxStagesMax * sizeof(MxHdr);
-    float *red = reinterpret_cast<float *>(sm + c.red_off);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = p.H, I = p.I;
     const int K2 = (PHASE == kGU ? H : I) / 2;  // k-pair rows
@@ -249,11 +250,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                     const uint32_t tb = (uint32_t)rows * (PHASE == kGU ? 4u : 8u);
                     bar_expect(&full[s], box_bytes + (uint32_t)ntok * tb);
                     unsigned char *st = stage0 + (size_t)s * c.stage_bytes;
-                    const int y = slot * K2 + ks * kKp, ys = slot * (K2 / 16) + ks * (kKp / 16);
+                    // rows past the slot's last k-pair row are zero-filled by the copy, not read
                     for (int m = 0; m < NM; m++) {
                         const int x = n0 + (m ? I : 0);
-                        tma2d(st + m * kKp * kCols, &blocks_map, x, y, &full[s]);
-                        tma2d(st + c.sc_off + m * (kKp / 16) * kCols, &scales_map, x, ys, &full[s]);
+                        tma3d(st + m * kKp * kCols, &blocks_map, x, ks * kKp, slot, &full[s]);
+                        tma3d(st + c.sc_off + m * (kKp / 16) * kCols, &scales_map, x, ks * (kKp / 16), slot, &full[s]);
                     }
                     for (int i = 0; i < ntok; i++) {
                         const int q = hh.pairs[i];
@@ -321,15 +322,19 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             continue;
         }
 
-        // item end: the warps' partial sums meet in shared memory; red layout
-        // [warp][m][t][kCols]. The stage (and its header) is released afterwards.
+        // item end: the warps' partial sums meet in shared memory. Each warp writes its
+        // partials [t][kCols] over its own 16-row code block of each matrix in this stage
+        // (16 x 128 bytes = kMxTokMax x kCols floats), which no other warp reads. The
+        // stage (and its header) is released afterwards.
 #pragma unroll
         for (int m = 0; m < NM; m++)
 #pragma unroll
             for (int t = 0; t < kMxTokMax; t++) {
                 if (t < ntok) {
                     float4 v = make_float4(acc[m][0][t], acc[m][1][t], acc[m][2][t], acc[m][3][t]);
-                    reinterpret_cast<float4 *>(red + ((warp * NM + m) * kMxTokMax + t) * kCols)[lane] = v;
+                    float *red = reinterpret_cast<float *>(const_cast<unsigned char *>(st) + m * kKp * kCols +
+                                                           warp * 16 * kCols);
+                    reinterpret_cast<float4 *>(red + t * kCols)[lane] = v;
                 }
 #pragma unroll
                 for (int cc = 0; cc < 4; cc++) acc[m][cc][t] = 0.f;
@@ -343,27 +348,36 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         const int bi = PHASE == kGU ? 2 : 5;
         const uint16_t *bias = reinterpret_cast<const uint16_t *>(p.bank[bi] + (int64_t)hs.slot * p.bank_bytes[bi]);
         const int n0 = hs.n0;
+        // ntok * kCols and the stride are multiples of 32, so a warp's 32 threads share
+        // one token t here and take the max |h| over their columns before a single
+        // atomic (every column doing its own atomic on the pair's word serialised on
+        // one L2 slice)
         for (int i = threadIdx.x; i < ntok * kCols; i += kCW * 32) {
             const int t = i / kCols, col = i - t * kCols;
             const int n = n0 + col;
-            if (n >= nout) continue;
+            const bool valid = n < nout;
             const float xs_t = ldexpf(1.f, hs.texp[t]);
             float v[NM];
 #pragma unroll
             for (int m = 0; m < NM; m++) {
                 float sum = 0.f;
 #pragma unroll
-                for (int w = 0; w < kCW; w++) sum += red[((w * NM + m) * kMxTokMax + t) * kCols + col];
+                for (int w = 0; w < kCW; w++)
+                    sum += reinterpret_cast<const float *>(st + m * kKp * kCols + w * 16 * kCols)[t * kCols + col];
                 v[m] = sum * xs_t;
             }
             const int q = hs.pairs[t];
             if (PHASE == kGU) {
-                const float g = v[0] + __uint_as_float((uint32_t)bias[n] << 16);
-                const float uu = v[NM - 1] + __uint_as_float((uint32_t)bias[I + n] << 16);
-                const float hv = silu(g) * uu;
-                p.s.h[(int64_t)q * I + n] = hv;
-                atomicMax(&p.s.hmax[q], __float_as_uint(fabsf(hv)));
-            } else {
+                float hv = 0.f;
+                if (valid) {
+                    const float g = v[0] + __uint_as_float((uint32_t)bias[n] << 16);
+                    const float uu = v[NM - 1] + __uint_as_float((uint32_t)bias[I + n] << 16);
+                    hv = silu(g) * uu;
+                    p.s.h[(int64_t)q * I + n] = hv;
+                }
+                const uint32_t wm = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv)));
+                if (lane == 0 && wm) atomicMax(&p.s.hmax[q], wm);
+            } else if (valid) {
                 p.s.o[(int64_t)q * H + n] = v[0] + __uint_as_float((uint32_t)bias[n] << 16);
             }
         }
@@ -392,14 +406,12 @@ bool make_mx_cfg(const FfnParams &p, int phase, MxCfg &c, size_t &smem) {
     c.tok_off = c.sc_off + NM * (kKp / 16) * kCols;
     c.stage_bytes = (c.tok_off + c.tg * c.tok_bytes + 127) & ~127;
     const size_t head = 256 + kMxStagesMax * sizeof(MxHdr);
-    const size_t red = (size_t)kCW * NM * kMxTokMax * kCols * 4;
-    const size_t cap = 220 * 1024;
+    const size_t cap = 226 * 1024;
     int stages = kMxStagesMax;
-    while (stages >= 2 && head + (size_t)stages * c.stage_bytes + red > cap) stages--;
+    while (stages >= 2 && head + (size_t)stages * c.stage_bytes > cap) stages--;
     if (stages < 2) return false;
     c.stages = stages;
-    c.red_off = (int32_t)(head + (size_t)stages * c.stage_bytes);
-    smem = head + (size_t)stages * c.stage_bytes + red;
+    smem = head + (size_t)stages * c.stage_bytes;
     return true;
 }
 
@@ -464,15 +476,18 @@ EncodeFn encode_fn() {
     return fn;
 }
 
-// 2-D u8 map over [rows, cols] bytes with a box of 128 columns x box_rows rows.
-bool encode_u8(void *out, const void *base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+// 3-D u8 map over [slots, rows, cols] bytes (one slot's rows contiguous, slots at a stride
+// of rows * cols) with a box of 128 columns x box_rows rows x 1 slot. Rows past a slot's
+// last row fall outside the map, so a ragged last box is zero-filled instead of reading
+// the next slot.
+bool encode_u8(void *out, const void *base, uint64_t cols, uint64_t rows, uint64_t slots, uint32_t box_rows) {
     EncodeFn fn = encode_fn();
     if (!fn || cols % 16 || ((uintptr_t)base % 16)) return false;
-    const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {cols};
-    const cuuint32_t box[2] = {(cuuint32_t)kCols, box_rows};
-    const cuuint32_t es[2] = {1, 1};
-    return fn(reinterpret_cast<CUtensorMap *>(out), CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims,
+    const cuuint64_t dims[3] = {cols, rows, slots};
+    const cuuint64_t strides[2] = {cols, cols * rows};
+    const cuuint32_t box[3] = {(cuuint32_t)kCols, box_rows, 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return fn(reinterpret_cast<CUtensorMap *>(out), CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims,
               strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -483,10 +498,10 @@ bool make_mx_tma_maps(MxTmaMaps &m, const unsigned char *const *banks, int S, in
     m.valid = false;
     if (H % 32 || I % 32) return false;
     const uint64_t ngu = 2ull * I, ndn = (uint64_t)H;
-    bool ok = encode_u8(m.gu_blocks, banks[0], ngu, (uint64_t)S * (H / 2), kKp) &&
-              encode_u8(m.gu_scales, banks[1], ngu, (uint64_t)S * (H / 32), kKp / 16) &&
-              encode_u8(m.dn_blocks, banks[3], ndn, (uint64_t)S * (I / 2), kKp) &&
-              encode_u8(m.dn_scales, banks[4], ndn, (uint64_t)S * (I / 32), kKp / 16);
+    bool ok = encode_u8(m.gu_blocks, banks[0], ngu, (uint64_t)(H / 2), (uint64_t)S, kKp) &&
+              encode_u8(m.gu_scales, banks[1], ngu, (uint64_t)(H / 32), (uint64_t)S, kKp / 16) &&
+              encode_u8(m.dn_blocks, banks[3], ndn, (uint64_t)(I / 2), (uint64_t)S, kKp) &&
+              encode_u8(m.dn_scales, banks[4], ndn, (uint64_t)(I / 32), (uint64_t)S, kKp / 16);
     m.valid = ok;
     return ok;
 }

@@ -141,9 +141,29 @@ struct Seg {
 
 // ---------------------------------------------------------------- consumers
 
+// Running max |h| of one pair, kept by lane t for the pair in token slot t: consecutive
+// items of a CTA mostly share their pairs, so the pair's max word is updated once per
+// run of items instead of once per row (per-row atomics on a handful of words
+// serialised on one L2 slice).
+struct HMax {
+    int pair = -1;
+    float m = 0.f;
+    __device__ __forceinline__ void flush(const FfnParams &p) {
+        if (pair >= 0 && m > 0.f) atomicMax(&p.s.hmax[pair], __float_as_uint(m));
+    }
+    __device__ __forceinline__ void add(const FfnParams &p, int q, float v) {
+        if (q != pair) {
+            flush(p);
+            pair = q;
+            m = 0.f;
+        }
+        m = fmaxf(m, v);
+    }
+};
+
 template <int FMT, int NT>
 __device__ __forceinline__ void gu_consume(const FfnParams &p, const TmaCfg &c, const unsigned char *st,
-                                           const StageHdr &h) {
+                                           const StageHdr &h, HMax &hm) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = p.H, I = p.I, R = c.R;
     const int64_t wr = Seg<FMT, kGateUp>::wrow(H, I), sr = Seg<FMT, kGateUp>::srow(H, I);
@@ -216,7 +236,7 @@ __device__ __forceinline__ void gu_consume(const FfnParams &p, const TmaCfg &c, 
             if (lane == t) {
                 const float hv = silu(gs) * us;
                 p.s.h[(int64_t)h.pairs[t] * I + (FMT == FTMOE_FMT_NVFP4 ? swz_h32(n) : n)] = hv;
-                if (FMT == FTMOE_FMT_NVFP4) atomicMax(&p.s.hmax[h.pairs[t]], __float_as_uint(fabsf(hv)));
+                if (FMT == FTMOE_FMT_NVFP4) hm.add(p, h.pairs[t], fabsf(hv));
             }
         }
     }
@@ -452,6 +472,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) ffn_rows_tma_kernel(FfnParams 
     }
 
     // consumers
+    HMax hm;
     for (int k = 0;; k++) {
         const int s = k % c.stages;
         if (!mbar_wait(&full[s], (k / c.stages) & 1)) {
@@ -459,14 +480,17 @@ __global__ void __launch_bounds__(kTmaThreads, 1) ffn_rows_tma_kernel(FfnParams 
             return;
         }
         const StageHdr h = hdr[s];
-        if (h.done) return;
+        if (h.done) {
+            hm.flush(p);
+            return;
+        }
         const unsigned char *st = stage0 + (size_t)s * c.stage_bytes;
         if (PHASE == kGateUp) {
             switch (h.ntok) {
-                case 1: gu_consume<FMT, 1>(p, c, st, h); break;
-                case 2: gu_consume<FMT, 2>(p, c, st, h); break;
-                case 3: gu_consume<FMT, 3>(p, c, st, h); break;
-                default: gu_consume<FMT, 4>(p, c, st, h); break;
+                case 1: gu_consume<FMT, 1>(p, c, st, h, hm); break;
+                case 2: gu_consume<FMT, 2>(p, c, st, h, hm); break;
+                case 3: gu_consume<FMT, 3>(p, c, st, h, hm); break;
+                default: gu_consume<FMT, 4>(p, c, st, h, hm); break;
             }
         } else {
             switch (h.ntok) {
