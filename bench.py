@@ -148,6 +148,44 @@ def install_hits(cache, r):
             cache.slots[b][i].copy_(cache.host[b][0][e])
 
 
+# Kernel sources whose DRAM traffic is recorded under profiles/ (one ncu capture of the
+# workload); a recorded figure is reported only while these sources are unchanged.
+TRAFFIC_SOURCES = {
+    "copy": ["copy.cu", "internal.cuh"],
+    "ffn": ["ffn_tma.cu", "ffn_common.cuh", "internal.cuh"],
+}
+
+
+def source_hash(kind: str) -> str:
+    """First 16 hex digits of the sha256 over the kernel sources of `kind`."""
+    import hashlib
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "expert_slot_cache_device_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in TRAFFIC_SOURCES[kind]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, kind: str):
+    """DRAM bytes (read + write) per launch of `kind` on `workload`, from the `traffic:`
+    lines of profiles/traffic_*.md, or None if none matches the current sources."""
+    pdir = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    cur = source_hash(kind)
+    for name in sorted(os.listdir(pdir)):
+        if not (name.startswith("traffic_") and name.endswith(".md")):
+            continue
+        with open(os.path.join(pdir, name)) as f:
+            for ln in f:
+                parts = ln.split()
+                if len(parts) == 6 and parts[0] == "traffic:" and parts[1] == workload and parts[2] == kind \
+                        and parts[3] == cur:
+                    return int(parts[4]) + int(parts[5])
+    return None
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -418,12 +456,14 @@ def run_gpu(args):
             "bw_GBps": r.misses * B / (time_ms / 1e3) / 1e9 if time_ms > 0 else 0.0,
             "tok_ms": time_ms * cfg.L, "ffn_us": ffn_s * 1e6,
             "roofline": {"bound": "host_link", "kernel": "copy_missing_kernel", "achieved": copy_ach, "peak": link,
-                         "unit": "GB/s", "frac": copy_ach / link if link else None, "traffic": None,
+                         "unit": "GB/s", "frac": copy_ach / link if link else None,
+                         "traffic": recorded_traffic(f"{cfg.name}/bs{bs}/mr{mr}", "copy"),
                          "peak_source": f"measured in this run: max(1 GiB pinned->device cudaMemcpyAsync "
                                         f"{links['memcpy']:.1f}, SM zero-copy read {links['sm_read']:.1f}) GB/s"},
             "roofline_ffn": {"bound": "hbm", "kernel": "expert FFN (route + gate_up + down + combine)",
                              "achieved": ffn_ach, "peak": hbm_peak, "unit": "GB/s", "frac": ffn_ach / hbm_peak,
-                             "traffic": None, "peak_source": hbm_src},
+                             "traffic": recorded_traffic(f"{cfg.name}/bs{bs}/mr{mr}", "ffn"),
+                             "peak_source": hbm_src},
             "link_peak_GBps": links,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
