@@ -134,8 +134,12 @@ struct Seg {
         return FMT == FTMOE_FMT_BF16 ? 0 : K / 16;
     }
     static constexpr int mats = PHASE == kGateUp ? 2 : 1;  // gate + up, or down
+    // offset of the nvfp4 per-row f16 globals (after the codes and scales of R rows)
+    __device__ __host__ static int64_t goff(int R, int H, int I) {
+        return (int64_t)mats * R * (wrow(H, I) + srow(H, I));
+    }
     __device__ __host__ static int64_t bytes(int rows, int H, int I) {
-        return (int64_t)mats * rows * (wrow(H, I) + srow(H, I));
+        return (int64_t)mats * rows * (wrow(H, I) + srow(H, I) + (FMT == FTMOE_FMT_NVFP4 ? 2 : 0));
     }
 };
 
@@ -175,10 +179,10 @@ __device__ __forceinline__ void gu_consume(const FfnParams &p, const TmaCfg &c, 
 #pragma unroll
         for (int t = 0; t < NT; t++) g[t] = u[t] = 0.f;
         float gg = 1.f, gu = 1.f;
-        if (FMT == FTMOE_FMT_NVFP4) {  // per-row globals: plain loads issued early
-            const unsigned char *gl = p.bank[2] + (int64_t)h.slot * p.bank_bytes[2];
-            gg = __half2float(*reinterpret_cast<const __half *>(gl + 2 * (int64_t)n));
-            gu = __half2float(*reinterpret_cast<const __half *>(gl + 2 * ((int64_t)I + n)));
+        if (FMT == FTMOE_FMT_NVFP4) {  // per-row f16 globals, staged after the scales
+            const __half *gl = reinterpret_cast<const __half *>(st + Seg<FMT, kGateUp>::goff(R, H, I));
+            gg = __half2float(gl[j]);
+            gu = __half2float(gl[R + j]);
         }
         if (FMT == FTMOE_FMT_BF16) {
             const uint4 *wg = reinterpret_cast<const uint4 *>(st + j * wr);
@@ -258,13 +262,12 @@ __device__ __forceinline__ void dn_consume(const FfnParams &p, const TmaCfg &c, 
         for (int r = 0; r < RR; r++)
 #pragma unroll
             for (int t = 0; t < NT; t++) o[r][t] = 0.f;
-        float gl[RR];  // per-row global scales (nvfp4), loaded before the row loop
+        float gl[RR];  // per-row f16 global scales (nvfp4), staged after the block scales
 #pragma unroll
         for (int r = 0; r < RR; r++) {
             gl[r] = 1.f;
             if (FMT == FTMOE_FMT_NVFP4 && r < nr)
-                gl[r] = __half2float(*reinterpret_cast<const __half *>(p.bank[5] + (int64_t)h.slot * p.bank_bytes[5] +
-                                                                       2 * (int64_t)(h.n0 + j0 + r)));
+                gl[r] = __half2float(reinterpret_cast<const __half *>(st + Seg<FMT, kDown>::goff(R, H, I))[j0 + r]);
         }
         if (FMT == FTMOE_FMT_BF16) {
             // lane step = 4 consecutive k: 8-byte weight reads and 16-byte h reads are
@@ -416,6 +419,11 @@ __global__ void __launch_bounds__(kTmaThreads, 1) ffn_rows_tma_kernel(FfnParams 
                         bulk_g2s(st + 2 * R * wr, sb + n0 * sr, (uint32_t)(rows * sr), &full[s], pol);
                         bulk_g2s(st + 2 * R * wr + R * sr, sb + ((int64_t)I + n0) * sr, (uint32_t)(rows * sr),
                                  &full[s], pol);
+                        // per-row globals: rows * 2 bytes, a multiple of 16 (rows is a multiple of 8)
+                        const unsigned char *gb = p.bank[2] + (int64_t)slot * p.bank_bytes[2];
+                        unsigned char *gd = st + Seg<FMT, PHASE>::goff(R, H, I);
+                        bulk_g2s(gd, gb + 2 * (int64_t)n0, (uint32_t)(2 * rows), &full[s], pol);
+                        bulk_g2s(gd + 2 * R, gb + 2 * ((int64_t)I + n0), (uint32_t)(2 * rows), &full[s], pol);
                     }
                 } else {
                     const int wb_i = FMT == FTMOE_FMT_BF16 ? 1 : 3;
@@ -424,6 +432,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1) ffn_rows_tma_kernel(FfnParams 
                     if (FMT == FTMOE_FMT_NVFP4) {
                         const unsigned char *sb = p.bank[4] + (int64_t)slot * p.bank_bytes[4];
                         bulk_g2s(st + R * wr, sb + n0 * sr, (uint32_t)(rows * sr), &full[s], pol);
+                        const unsigned char *gb = p.bank[5] + (int64_t)slot * p.bank_bytes[5];
+                        bulk_g2s(st + Seg<FMT, PHASE>::goff(R, H, I), gb + 2 * (int64_t)n0, (uint32_t)(2 * rows),
+                                 &full[s], pol);
                     }
                 }
                 if (!waited) {  // h rows are written by the gate_up kernel
@@ -519,7 +530,9 @@ bool make_cfg(const FfnParams &p, TmaCfg &c) {
     const int rmin_busy = PHASE == kGateUp ? kConsumerWarps : 4 * kConsumerWarps;
     for (int pass = 0; pass < 2; pass++) {
         for (int tg = kMaxTok; tg >= 1; tg >>= 1) {
-            for (int R = rmax; R >= (pass == 0 ? rmin_busy : 1); R >>= 1) {
+            // nvfp4 items stage their per-row f16 globals with bulk copies of 2R bytes: R >= 8
+            const int rmin = pass == 0 ? rmin_busy : (FMT == FTMOE_FMT_NVFP4 ? 8 : 1);
+            for (int R = rmax; R >= rmin; R >>= 1) {
                 const int64_t wb = Seg<FMT, PHASE>::bytes(R, H, I);
                 if (wb > 72 * 1024) continue;
                 const int64_t stage = ((wb + 127) & ~(int64_t)127) + (int64_t)tg * c.tok_bytes;
@@ -564,7 +577,11 @@ cudaError_t launch_one(const FfnParams &p, int num_sms, cudaStream_t st) {
 bool ffn_rows_tma_supported(const FfnParams &p) {
     if (!p.s.upoff || !p.s.n_passes) return false;
     if (p.fmt == FTMOE_FMT_BF16) return p.H % 8 == 0 && p.I % 8 == 0;
-    if (p.fmt == FTMOE_FMT_NVFP4) return p.H % 256 == 0 && p.I % 256 == 0 && p.s.x16 && p.s.xexp && p.s.hmax;
+    if (p.fmt == FTMOE_FMT_NVFP4) {
+        TmaCfg c;
+        return p.H % 256 == 0 && p.I % 256 == 0 && p.s.x16 && p.s.xexp && p.s.hmax &&
+               make_cfg<FTMOE_FMT_NVFP4, kGateUp>(p, c) && make_cfg<FTMOE_FMT_NVFP4, kDown>(p, c);
+    }
     return false;
 }
 
