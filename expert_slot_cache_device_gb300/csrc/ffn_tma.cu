@@ -517,14 +517,14 @@ __global__ void __launch_bounds__(kTmaThreads, 1) ffn_rows_tma_kernel(FfnParams 
 }
 
 constexpr size_t kSmemHeader = 128 + kMaxStages * sizeof(StageHdr);
-constexpr size_t kSmemCap = 200 * 1024;
+constexpr size_t kSmemCap = 220 * 1024;
 
 template <int FMT, int PHASE>
 bool make_cfg(const FfnParams &p, TmaCfg &c) {
     const int H = p.H, I = p.I;
     const int nout = PHASE == kGateUp ? I : H;
     c.tok_bytes = PHASE == kGateUp ? 2 * H : 4 * I;
-    const int rmax = PHASE == kGateUp ? 16 : 32;
+    const int rmax = PHASE == kGateUp ? 16 : 64;
     // Prefer enough rows per item to keep all consumer warps busy (gate_up: one neuron per
     // warp; down: four rows per warp), then as many token slots as fit.
     const int rmin_busy = PHASE == kGateUp ? kConsumerWarps : 4 * kConsumerWarps;
@@ -534,7 +534,7 @@ bool make_cfg(const FfnParams &p, TmaCfg &c) {
             const int rmin = pass == 0 ? rmin_busy : (FMT == FTMOE_FMT_NVFP4 ? 8 : 1);
             for (int R = rmax; R >= rmin; R >>= 1) {
                 const int64_t wb = Seg<FMT, PHASE>::bytes(R, H, I);
-                if (wb > 72 * 1024) continue;
+                if (wb > 80 * 1024) continue;
                 const int64_t stage = ((wb + 127) & ~(int64_t)127) + (int64_t)tg * c.tok_bytes;
                 const int64_t stages = (int64_t)((kSmemCap - kSmemHeader) / (size_t)stage);
                 if (stages < 2) continue;
