@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(1024) ffn_route_kernel(FfnParams p) {
         int c = s < p.S ? cnt[s] : 0;
         int ru = block_scan_sum(c > 0, warp_tot, &s_tot_u);
         int rc = block_scan_sum(c, warp_tot, &s_tot_c);
-        int rp = block_scan_sum((c + kPassTokens - 1) / kPassTokens, warp_tot, &s_tot_p);
+        int rp = block_scan_sum((c + p.pass_tokens - 1) / p.pass_tokens, warp_tot, &s_tot_p);
         if (c > 0) {
             int u = base_u + ru;
             p.s.uslot[u] = s;
@@ -748,6 +748,7 @@ cudaError_t launch_ffn(const FfnParams &p_in, int num_sms, cudaStream_t st, cons
     const bool want_x16 = (fp4_rows_tma && p.fmt == FTMOE_FMT_NVFP4) || mx_tma;
     p.x16_emax = p.fmt == FTMOE_FMT_MXFP4 ? 9 : 10;
     p.x16_swz = fp4_rows_tma && p.fmt == FTMOE_FMT_NVFP4;
+    p.pass_tokens = mx_tma ? kMxPassTokens : kPassTokens;
     ffn_route_kernel<<<1 + (want_x16 ? p.bs : 0), 1024, route_smem, st>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 

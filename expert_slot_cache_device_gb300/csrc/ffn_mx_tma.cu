@@ -3,24 +3,33 @@
 // mxfp4 banks are stored transposed (benchmark guide, section 4.2: "_blocks /
 // _scales / _bias"): blocks [K/2, N] (byte (i, n) holds k = 2i in the low nibble and
 // k = 2i + 1 in the high nibble of output column n), scales [K/32, N] e8m0, bias [N].
-// A work item is (distinct slot u, pass of up to four tokens, tile of 128 output
+// A work item is (distinct slot u, pass of up to eight tokens, tile of 128 output
 // columns); it streams the whole reduction axis in stages of kKp = 256 k-pair rows. A
 // producer thread loads each stage with 3-D bulk tensor copies (cp.async.bulk.tensor
-// over [slot, row, column], one box of 128 columns x 256 rows per matrix plus the 16
-// matching scale rows, completion on an mbarrier; rows past the slot's end are
-// zero-filled) and a 1-D bulk copy of the tokens' activations for those rows. Sixteen
-// consumer warps each take one 16-row scale block of the stage: a lane owns 4 adjacent
-// columns, decodes their code bytes to exact f16x2 (k even, k odd), and accumulates
-// with packed f16 FMAs against the row's activation pair (a shared-memory broadcast):
-// each f16 half sums 16 exact products of |e2m1| <= 6 and |x| < 2^9, so it stays below
-// 2^15. The block's partial is scaled by 2^(e8m0 - 127) and accumulated in fp32. After
-// the last stage of an item each warp writes its partials over its own (consumed) code
-// block of that stage, the warps meet behind an mbarrier (bounded wait), the bias is
-// added, and gate_up writes h = silu(g) * u while down writes o.
+// over [slot, row, column], one box of 128 columns x 256 rows per matrix stored with
+// the 128-byte shared-memory swizzle, plus the 16 matching scale rows; completion on an
+// mbarrier; rows past the slot's end are zero-filled) and a 1-D bulk copy of the
+// tokens' activations for those rows.
+//
+// The contraction runs on the tensor cores with the warp-level mma.sync m16n8k16
+// (f16 x f16 -> fp32): M = 16 output columns, N = 8 tokens, K = 16 (8 k-pair rows).
+// Each consumer warp takes two 16-row scale blocks (32 k-pair rows) and one half of
+// the 128 columns (four M tiles). A lane's A fragment is built directly from code bytes:
+// one byte holds (k even, k odd) of one column, which is exactly an f16x2 register of
+// the fragment after cvt.rn.f16x2.e2m1x2. The M index of a tile is a permutation of its
+// columns (lane group g owns columns 4g..4g+3 of a 32-column group) and the k-pair rows
+// of a k step are taken in the order 2*tig, 2*tig + 1, so every lane reads whole 32-bit
+// words and, with the swizzle, the 32 lanes of a load hit 32 distinct banks. The B
+// fragment of lane (g, tig) is token g's activation pairs of its two k-pair rows (one
+// 64-bit load); tokens past the pass's count are zero. Each scale block is accumulated
+// from zero on the tensor cores, multiplied by its e8m0 column scale in fp32 and added
+// to the item's accumulator, so the block scale is exact. After the last stage of an
+// item the warps' partials meet in a shared-memory buffer behind an mbarrier (bounded
+// wait), the bias is added, and gate_up writes h = silu(g) * u while down writes o.
 //
 // Activations: gate_up uses the f16 copy of x (per-token power-of-two scale, max
-// |x| < 2^9); down converts the fp32 h rows with the per-pair power-of-two scale
-// derived from the max |h| recorded by gate_up.
+// |x| < 2^9, so every bf16 value is exact in f16); down converts the fp32 h rows to
+// f16 with the per-pair power-of-two scale derived from the max |h| recorded by gate_up.
 #include <cuda.h>
 
 #include "ffn_common.cuh"
@@ -31,13 +40,15 @@ namespace {
 
 using namespace ffn;
 
-constexpr int kCW = 16;                     // consumer warps (one 16-row scale block each)
+constexpr int kCW = 16;                     // consumer warps
 constexpr int kMxThreads = (kCW + 1) * 32;  // + producer warp
-constexpr int kKp = 256;                    // k-pair rows per stage (16 blocks of 16)
-constexpr int kCols = 128;                  // output columns per item
+constexpr int kKp = 256;                    // k-pair rows per stage (16 scale blocks of 16)
+constexpr int kCols = 128;                  // output columns per item (one 128-byte box row)
 constexpr int kMxStagesMax = 4;
-constexpr int kMxTokMax = 4;
-static_assert(kMxTokMax * kCols * 4 <= 16 * kCols, "a warp's partials fit its 16-row code block");
+constexpr int kMxTokMax = 8;                // tokens per pass = the MMA's N
+constexpr int kBlkPairs = kKp / 32;         // consumer warps per column half
+static_assert(kBlkPairs * 2 == kCW, "two column halves x eight pairs of scale blocks");
+static_assert(kMxTokMax == kMxPassTokens, "the routing kernel cuts passes of kMxTokMax tokens");
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 enum { kGU = 0, kDN = 1 };
@@ -48,8 +59,11 @@ struct MxHdr {
     int32_t texp[kMxTokMax];
 };
 
+// Stage layout (each stage 1024-byte aligned for the swizzle): codes [NM][kKp][kCols],
+// scales [NM][kKp / 16][kCols] at sc_off, tokens [tg] at tok_off with a padded stride,
+// bias [NM][kCols] bf16 at bias_off (filled on an item's last stage).
 struct MxCfg {
-    int32_t tiles, kst, stages, stage_bytes, tok_off, tok_bytes, sc_off, tg;
+    int32_t tiles, kst, stages, stage_bytes, tok_off, tok_stride, sc_off, tg, red_off, bias_off;
 };
 
 __device__ __forceinline__ uint32_t su32(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
@@ -100,59 +114,121 @@ __device__ __forceinline__ void bulk1d(void *dst, const void *src, uint32_t byte
                  : "memory");
 }
 
-// Accumulate one 16-row scale block of the stage for NM matrices (gate, up) and NT tokens.
-template <int NM, int NT, bool DOWN>
-__device__ __forceinline__ void mx_block(const unsigned char *st, const MxCfg &c, int blk,
-                                         float (&acc)[NM][4][kMxTokMax], const float (&hsc)[kMxTokMax]) {
-    const int lane = threadIdx.x & 31;
-    __half2 a16[NM][4][NT];
+// Shared-memory byte of logical (row, byte) of a 128-byte-swizzled code tile whose base
+// is 1024-byte aligned: the 16-byte chunk index is XORed with the row's index mod 8.
+__device__ __forceinline__ int swz128(int row, int byte) { return row * kCols + (byte ^ ((row & 7) << 4)); }
+
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Same with a zero accumulator input (d = A * B).
+__device__ __forceinline__ void mma_f16_16816_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                                uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%10, %10, %10, %10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+// Two e8m0 bytes (low byte first) -> their values 2^(b - 127) as floats, through the
+// exact ue8m0 -> bf16 conversion (bf16 has f32's exponent range, so bf16 << 16 is the
+// f32 value; 0 gives the bf16 subnormal 2^-127, 0xff NaN).
+__device__ __forceinline__ float2 e8m0x2_to_f2(uint32_t two_bytes) {
+    uint32_t b;
+    asm("{\n\t.reg .b16 s;\n\t"
+        "cvt.u16.u32 s, %1;\n\t"
+        "cvt.rn.bf16x2.ue8m0x2 %0, s;\n\t}"
+        : "=r"(b)
+        : "r"(two_bytes & 0xffffu));
+    return make_float2(__uint_as_float(b << 16), __uint_as_float(b & 0xffff0000u));
+}
+
+// (a0, a1) += (t0, t1) * s with one packed fp32 FMA.
+__device__ __forceinline__ void ffma2_s(float &a0, float &a1, float t0, float t1, float s) {
+    uint64_t r;
+    asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+        "mov.b64 ra, {%1, %2};\n\t"
+        "mov.b64 rb, {%3, %3};\n\t"
+        "mov.b64 rc, {%4, %5};\n\t"
+        "fma.rn.f32x2 %0, ra, rb, rc;\n\t}"
+        : "=l"(r)
+        : "f"(t0), "f"(t1), "f"(s), "f"(a0), "f"(a1));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(r));
+}
+
+// One stage of one consumer warp: scale blocks 2bp and 2bp + 1 of the stage, column half
+// hf (M tiles j = 4hf..4hf+3 of the item, here indexed 0..3), all NM matrices.
+//   acc[m][j][0..1]: column 32jp + 4g + 2q,     tokens 2tig, 2tig + 1
+//   acc[m][j][2..3]: column 32jp + 4g + 2q + 1, tokens 2tig, 2tig + 1
+// with j = 2 * (jp - 2hf) + q, g = lane / 4, tig = lane % 4.
+template <int NM, bool DOWN>
+__device__ __forceinline__ void mx_stage_mma(const unsigned char *st, const MxCfg &c, int bp, int hf, int rows,
+                                             int ntok, float tok_scale, float (&acc)[NM][4][4]) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
+    const unsigned char *tokp = st + c.tok_off + g * c.tok_stride;
 #pragma unroll
-    for (int m = 0; m < NM; m++)
+    for (int bb = 0; bb < 2; bb++) {
+        const int blk = 2 * bp + bb;
+        if (blk * 16 >= rows) break;
+        float tmp[NM][4][4];
 #pragma unroll
-        for (int cc = 0; cc < 4; cc++)
+        for (int ks = 0; ks < 2; ks++) {
+            const int rA = blk * 16 + ks * 8 + 2 * tig, rB = rA + 1;  // k-pair rows of this lane
+            uint32_t b0 = 0u, b1 = 0u;
+            if (g < ntok) {
+                if (DOWN) {
+                    const float4 hv = *reinterpret_cast<const float4 *>(tokp + 8 * rA);
+                    b0 = f2_scale_to_h2(hv.x, hv.y, tok_scale);
+                    b1 = f2_scale_to_h2(hv.z, hv.w, tok_scale);
+                } else {
+                    const uint2 xv = *reinterpret_cast<const uint2 *>(tokp + 4 * rA);
+                    b0 = xv.x;
+                    b1 = xv.y;
+                }
+            }
 #pragma unroll
-            for (int t = 0; t < NT; t++) a16[m][cc][t] = __float2half2_rn(0.f);
-    const int r0 = blk * 16;
+            for (int m = 0; m < NM; m++) {
+                const unsigned char *cm = st + m * kKp * kCols;
 #pragma unroll
-    for (int r = r0; r < r0 + 16; r++) {
-        uint32_t xp[NT];
-#pragma unroll
-        for (int t = 0; t < NT; t++) {
-            if (DOWN) {
-                const float2 hv = *reinterpret_cast<const float2 *>(st + c.tok_off + t * c.tok_bytes + 8 * r);
-                const __half2 x2 = __floats2half2_rn(hv.x * hsc[t], hv.y * hsc[t]);
-                xp[t] = *reinterpret_cast<const uint32_t *>(&x2);
-            } else {
-                xp[t] = *reinterpret_cast<const uint32_t *>(st + c.tok_off + t * c.tok_bytes + 4 * r);
+                for (int q2 = 0; q2 < 2; q2++) {
+                    const int byte = 32 * (2 * hf + q2) + 4 * g;
+                    const uint32_t wA = *reinterpret_cast<const uint32_t *>(cm + swz128(rA, byte));
+                    const uint32_t wB = *reinterpret_cast<const uint32_t *>(cm + swz128(rB, byte));
+                    uint32_t hA[4], hB[4];
+                    e2m1x8_h2(wA, hA);
+                    e2m1x8_h2(wB, hB);
+                    if (ks == 0) {  // the block's sum starts from zero
+                        mma_f16_16816_z(tmp[m][2 * q2], hA[0], hA[1], hB[0], hB[1], b0, b1);
+                        mma_f16_16816_z(tmp[m][2 * q2 + 1], hA[2], hA[3], hB[2], hB[3], b0, b1);
+                    } else {
+                        mma_f16_16816(tmp[m][2 * q2], hA[0], hA[1], hB[0], hB[1], b0, b1);
+                        mma_f16_16816(tmp[m][2 * q2 + 1], hA[2], hA[3], hB[2], hB[3], b0, b1);
+                    }
+                }
             }
         }
+        // the block's e8m0 column scales: bytes 0..3 of the word are the columns of
+        // (q = 0, row g), (q = 0, row g + 8), (q = 1, row g), (q = 1, row g + 8)
 #pragma unroll
-        for (int m = 0; m < NM; m++) {
-            const uint32_t cw = *reinterpret_cast<const uint32_t *>(st + m * kKp * kCols + r * kCols + 4 * lane);
-            uint32_t w4[4];  // column cc: (k even, k odd) as exact f16x2
-            e2m1x8_h2(cw, w4);
+        for (int m = 0; m < NM; m++)
 #pragma unroll
-            for (int cc = 0; cc < 4; cc++) {
+            for (int q2 = 0; q2 < 2; q2++) {
+                const uint32_t sw = *reinterpret_cast<const uint32_t *>(
+                    st + c.sc_off + (m * (kKp / 16) + blk) * kCols + 32 * (2 * hf + q2) + 4 * g);
 #pragma unroll
-                for (int t = 0; t < NT; t++)
-                    a16[m][cc][t] = __hfma2(*reinterpret_cast<const __half2 *>(&w4[cc]),
-                                            *reinterpret_cast<const __half2 *>(&xp[t]), a16[m][cc][t]);
+                for (int q = 0; q < 2; q++) {
+                    const float2 sc = e8m0x2_to_f2(sw >> (16 * q));  // (row g, row g + 8)
+                    float *a = acc[m][2 * q2 + q];
+                    const float *t = tmp[m][2 * q2 + q];
+                    ffma2_s(a[0], a[1], t[0], t[1], sc.x);
+                    ffma2_s(a[2], a[3], t[2], t[3], sc.y);
+                }
             }
-        }
-    }
-#pragma unroll
-    for (int m = 0; m < NM; m++) {
-        const uint32_t sw = *reinterpret_cast<const uint32_t *>(st + c.sc_off + m * (kKp / 16) * kCols + blk * kCols +
-                                                                4 * lane);
-#pragma unroll
-        for (int cc = 0; cc < 4; cc++) {
-            const float s = e8m0_to_f(sw >> (8 * cc));
-#pragma unroll
-            for (int t = 0; t < NT; t++) {
-                const float2 f = __half22float2(a16[m][cc][t]);
-                acc[m][cc][t] = fmaf(f.x + f.y, s, acc[m][cc][t]);
-            }
-        }
     }
 }
 
@@ -161,12 +237,16 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     ffn_mx_tma_kernel(FfnParams p, MxCfg c, const __grid_constant__ CUtensorMap blocks_map,
                       const __grid_constant__ CUtensorMap scales_map) {
     constexpr int NM = PHASE == kGU ? 2 : 1;
-    extern __shared__ __align__(128) unsigned char sm[];
+    extern __shared__ __align__(1024) unsigned char sm[];
     uint64_t *full = reinterpret_cast<uint64_t *>(sm);
     uint64_t *empty = full + kMxStagesMax;
     uint64_t *rbar = empty + kMxStagesMax;  // [2] consumer barriers around the reduction
     MxHdr *hdr = reinterpret_cast<MxHdr *>(sm + 256);
-    unsigned char *stage0 = sm + 256 + kMxStagesMax * sizeof(MxHdr);
+    // stages start at the first 1024-byte aligned shared address after the headers (the
+    // 128-byte swizzle pattern of the code tiles repeats every 1024 bytes)
+    const uint32_t hdr_end = su32(sm) + 256 + kMxStagesMax * sizeof(MxHdr);
+    unsigned char *stage0 = sm + (((hdr_end + 1023u) & ~1023u) - su32(sm));
+    float *red = reinterpret_cast<float *>(stage0 + c.red_off);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = p.H, I = p.I;
     const int K2 = (PHASE == kGU ? H : I) / 2;  // k-pair rows
@@ -205,8 +285,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                 cur_pi = pi;
                 slot = p.s.uslot[u];
                 slot = slot < 0 ? 0 : (slot >= p.S ? p.S - 1 : slot);
-                const int pbase = (pi - p.s.upoff[u]) * kPassTokens;
-                cnt = p.s.ucnt[u] - pbase < kPassTokens ? p.s.ucnt[u] - pbase : kPassTokens;
+                const int pbase = (pi - p.s.upoff[u]) * kMxTokMax;
+                cnt = p.s.ucnt[u] - pbase < kMxTokMax ? p.s.ucnt[u] - pbase : kMxTokMax;
                 const int off = p.s.uoff[u] + pbase;
                 if (!waited) {  // h rows and their maxima come from gate_up
                     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -248,7 +328,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                         hh.texp[i] = texp_c[i];
                     }
                     const uint32_t tb = (uint32_t)rows * (PHASE == kGU ? 4u : 8u);
-                    bar_expect(&full[s], box_bytes + (uint32_t)ntok * tb);
+                    // the item's last stage also brings the bias of its columns (bf16; the
+                    // column count is a multiple of 32, so 64-byte multiples)
+                    const int ncol = nout - n0 < kCols ? nout - n0 : kCols;
+                    const uint32_t bb = hh.last ? (uint32_t)(NM * ncol * 2) : 0u;
+                    bar_expect(&full[s], box_bytes + (uint32_t)ntok * tb + bb);
                     unsigned char *st = stage0 + (size_t)s * c.stage_bytes;
                     // rows past the slot's last k-pair row are zero-filled by the copy, not read
                     for (int m = 0; m < NM; m++) {
@@ -262,7 +346,14 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                                               ? static_cast<const void *>(p.s.x16 + (int64_t)(q / p.topk) * H +
                                                                           2 * ks * kKp)
                                               : static_cast<const void *>(p.s.h + (int64_t)q * I + 2 * ks * kKp);
-                        bulk1d(st + c.tok_off + i * c.tok_bytes, src, tb, &full[s]);
+                        bulk1d(st + c.tok_off + i * c.tok_stride, src, tb, &full[s]);
+                    }
+                    if (hh.last) {
+                        const int bi = PHASE == kGU ? 2 : 5;
+                        const unsigned char *bsrc = p.bank[bi] + (int64_t)slot * p.bank_bytes[bi];
+                        for (int m = 0; m < NM; m++)
+                            bulk1d(st + c.bias_off + m * kCols * 2, bsrc + 2 * ((int64_t)n0 + (m ? I : 0)),
+                                   (uint32_t)(ncol * 2), &full[s]);
                     }
                     issued++;
                 }
@@ -285,15 +376,17 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         return;
     }
 
-    // consumers
-    float acc[NM][4][kMxTokMax];
+    // consumers: warp = (pair of scale blocks bp, column half hf)
+    const int bp = warp >> 1, hf = warp & 1;
+    float acc[NM][4][4];
 #pragma unroll
     for (int m = 0; m < NM; m++)
 #pragma unroll
-        for (int cc = 0; cc < 4; cc++)
+        for (int j = 0; j < 4; j++)
 #pragma unroll
-            for (int t = 0; t < kMxTokMax; t++) acc[m][cc][t] = 0.f;
+            for (int i = 0; i < 4; i++) acc[m][j][i] = 0.f;
     uint32_t rphase = 0;
+    const int g = lane >> 2, tig = lane & 3;
     for (int k = 0;; k++) {
         const int s = k % c.stages;
         if (!bar_wait(&full[s], (k / c.stages) & 1)) {
@@ -305,39 +398,32 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         const int ntok = hs.ntok, rows = hs.rows;
         const bool last = hs.last;
         const unsigned char *st = stage0 + (size_t)s * c.stage_bytes;
-        float hsc[kMxTokMax];
-#pragma unroll
-        for (int t = 0; t < kMxTokMax; t++) hsc[t] = t < ntok ? ldexpf(1.f, -hs.texp[t]) : 0.f;
-        if (warp * 16 < rows) {
-            switch (ntok) {
-                case 1: mx_block<NM, 1, PHASE == kDN>(st, c, warp, acc, hsc); break;
-                case 2: mx_block<NM, 2, PHASE == kDN>(st, c, warp, acc, hsc); break;
-                case 3: mx_block<NM, 3, PHASE == kDN>(st, c, warp, acc, hsc); break;
-                default: mx_block<NM, 4, PHASE == kDN>(st, c, warp, acc, hsc); break;
-            }
-        }
+        const float tok_scale = g < ntok ? ldexpf(1.f, -hs.texp[g]) : 0.f;
+        mx_stage_mma<NM, PHASE == kDN>(st, c, bp, hf, rows, ntok, tok_scale, acc);
         if (!last) {
             __syncwarp();
             if (lane == 0) bar_arrive(&empty[s]);
             continue;
         }
 
-        // item end: the warps' partial sums meet in shared memory. Each warp writes its
-        // partials [t][kCols] over its own 16-row code block of each matrix in this stage
-        // (16 x 128 bytes = kMxTokMax x kCols floats), which no other warp reads. The
-        // stage (and its header) is released afterwards.
+        // item end: the warps' partials meet in red [NM][kBlkPairs][kMxTokMax][kCols]
 #pragma unroll
         for (int m = 0; m < NM; m++)
 #pragma unroll
-            for (int t = 0; t < kMxTokMax; t++) {
-                if (t < ntok) {
-                    float4 v = make_float4(acc[m][0][t], acc[m][1][t], acc[m][2][t], acc[m][3][t]);
-                    float *red = reinterpret_cast<float *>(const_cast<unsigned char *>(st) + m * kKp * kCols +
-                                                           warp * 16 * kCols);
-                    reinterpret_cast<float4 *>(red + t * kCols)[lane] = v;
+            for (int j = 0; j < 4; j++) {
+                const int col = 32 * (2 * hf + (j >> 1)) + 4 * g + 2 * (j & 1);
+                float *r = red + ((m * kBlkPairs + bp) * kMxTokMax) * kCols;
+                const int t0 = 2 * tig, t1 = 2 * tig + 1;
+                if (t0 < ntok) {
+                    r[t0 * kCols + col] = acc[m][j][0];
+                    r[t0 * kCols + col + 1] = acc[m][j][2];
+                }
+                if (t1 < ntok) {
+                    r[t1 * kCols + col] = acc[m][j][1];
+                    r[t1 * kCols + col + 1] = acc[m][j][3];
                 }
 #pragma unroll
-                for (int cc = 0; cc < 4; cc++) acc[m][cc][t] = 0.f;
+                for (int i = 0; i < 4; i++) acc[m][j][i] = 0.f;
             }
         __syncwarp();
         if (lane == 0) bar_arrive(&rbar[0]);
@@ -345,8 +431,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             if (lane == 0) atomicCAS(p.status, 0, FTMOE_ERR_STATE);
             return;
         }
-        const int bi = PHASE == kGU ? 2 : 5;
-        const uint16_t *bias = reinterpret_cast<const uint16_t *>(p.bank[bi] + (int64_t)hs.slot * p.bank_bytes[bi]);
+        const uint16_t *bias = reinterpret_cast<const uint16_t *>(st + c.bias_off);  // [NM][kCols], staged
         const int n0 = hs.n0;
         // ntok * kCols and the stride are multiples of 32, so a warp's 32 threads share
         // one token t here and take the max |h| over their columns before a single
@@ -362,23 +447,22 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             for (int m = 0; m < NM; m++) {
                 float sum = 0.f;
 #pragma unroll
-                for (int w = 0; w < kCW; w++)
-                    sum += reinterpret_cast<const float *>(st + m * kKp * kCols + w * 16 * kCols)[t * kCols + col];
+                for (int w = 0; w < kBlkPairs; w++) sum += red[((m * kBlkPairs + w) * kMxTokMax + t) * kCols + col];
                 v[m] = sum * xs_t;
             }
             const int q = hs.pairs[t];
             if (PHASE == kGU) {
                 float hv = 0.f;
                 if (valid) {
-                    const float g = v[0] + __uint_as_float((uint32_t)bias[n] << 16);
-                    const float uu = v[NM - 1] + __uint_as_float((uint32_t)bias[I + n] << 16);
-                    hv = silu(g) * uu;
+                    const float gg = v[0] + __uint_as_float((uint32_t)bias[col] << 16);
+                    const float uu = v[NM - 1] + __uint_as_float((uint32_t)bias[(NM - 1) * kCols + col] << 16);
+                    hv = silu(gg) * uu;
                     p.s.h[(int64_t)q * I + n] = hv;
                 }
                 const uint32_t wm = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv)));
                 if (lane == 0 && wm) atomicMax(&p.s.hmax[q], wm);
             } else if (valid) {
-                p.s.o[(int64_t)q * H + n] = v[0] + __uint_as_float((uint32_t)bias[n] << 16);
+                p.s.o[(int64_t)q * H + n] = v[0] + __uint_as_float((uint32_t)bias[col] << 16);
             }
         }
         __syncwarp();
@@ -401,17 +485,22 @@ bool make_mx_cfg(const FfnParams &p, int phase, MxCfg &c, size_t &smem) {
     c.tiles = (nout + kCols - 1) / kCols;
     c.kst = (K2 + kKp - 1) / kKp;
     c.tg = kMxTokMax;
-    c.tok_bytes = kKp * (phase == kGU ? 4 : 8);
+    // token rows: 4 bytes (f16 pair) or 8 bytes (fp32 pair) per k-pair row; the stride is
+    // padded by 32 / 64 bytes so the B-fragment loads of eight tokens hit distinct banks
+    c.tok_stride = phase == kGU ? kKp * 4 + 32 : kKp * 8 + 64;
     c.sc_off = NM * kKp * kCols;
     c.tok_off = c.sc_off + NM * (kKp / 16) * kCols;
-    c.stage_bytes = (c.tok_off + c.tg * c.tok_bytes + 127) & ~127;
-    const size_t head = 256 + kMxStagesMax * sizeof(MxHdr);
-    const size_t cap = 226 * 1024;
+    c.bias_off = c.tok_off + c.tg * c.tok_stride;
+    c.stage_bytes = (c.bias_off + NM * kCols * 2 + 1023) & ~1023;
+    const size_t red = (size_t)NM * kBlkPairs * kMxTokMax * kCols * 4;
+    const size_t head = 256 + kMxStagesMax * sizeof(MxHdr) + 1024;  // + alignment slack
+    const size_t cap = 227 * 1024;
     int stages = kMxStagesMax;
-    while (stages >= 2 && head + (size_t)stages * c.stage_bytes > cap) stages--;
+    while (stages >= 2 && head + (size_t)stages * c.stage_bytes + red > cap) stages--;
     if (stages < 2) return false;
     c.stages = stages;
-    smem = head + (size_t)stages * c.stage_bytes;
+    c.red_off = stages * c.stage_bytes;
+    smem = head + (size_t)stages * c.stage_bytes + red;
     return true;
 }
 
@@ -477,10 +566,12 @@ EncodeFn encode_fn() {
 }
 
 // 3-D u8 map over [slots, rows, cols] bytes (one slot's rows contiguous, slots at a stride
-// of rows * cols) with a box of 128 columns x box_rows rows x 1 slot. Rows past a slot's
+// of rows * cols) with a box of 128 columns x box_rows rows x 1 slot and the given
+// shared-memory swizzle. Rows past a slot's
 // last row fall outside the map, so a ragged last box is zero-filled instead of reading
 // the next slot.
-bool encode_u8(void *out, const void *base, uint64_t cols, uint64_t rows, uint64_t slots, uint32_t box_rows) {
+bool encode_u8(void *out, const void *base, uint64_t cols, uint64_t rows, uint64_t slots, uint32_t box_rows,
+               CUtensorMapSwizzle swizzle) {
     EncodeFn fn = encode_fn();
     if (!fn || cols % 16 || ((uintptr_t)base % 16)) return false;
     const cuuint64_t dims[3] = {cols, rows, slots};
@@ -488,8 +579,8 @@ bool encode_u8(void *out, const void *base, uint64_t cols, uint64_t rows, uint64
     const cuuint32_t box[3] = {(cuuint32_t)kCols, box_rows, 1};
     const cuuint32_t es[3] = {1, 1, 1};
     return fn(reinterpret_cast<CUtensorMap *>(out), CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims,
-              strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+              strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 }  // namespace
 
@@ -498,10 +589,12 @@ bool make_mx_tma_maps(MxTmaMaps &m, const unsigned char *const *banks, int S, in
     m.valid = false;
     if (H % 32 || I % 32) return false;
     const uint64_t ngu = 2ull * I, ndn = (uint64_t)H;
-    bool ok = encode_u8(m.gu_blocks, banks[0], ngu, (uint64_t)(H / 2), (uint64_t)S, kKp) &&
-              encode_u8(m.gu_scales, banks[1], ngu, (uint64_t)(H / 32), (uint64_t)S, kKp / 16) &&
-              encode_u8(m.dn_blocks, banks[3], ndn, (uint64_t)(I / 2), (uint64_t)S, kKp) &&
-              encode_u8(m.dn_scales, banks[4], ndn, (uint64_t)(I / 32), (uint64_t)S, kKp / 16);
+    // code tiles: 128-byte rows stored with the 128-byte swizzle; scale tiles plain
+    const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B, none = CU_TENSOR_MAP_SWIZZLE_NONE;
+    bool ok = encode_u8(m.gu_blocks, banks[0], ngu, (uint64_t)(H / 2), (uint64_t)S, kKp, sw) &&
+              encode_u8(m.gu_scales, banks[1], ngu, (uint64_t)(H / 32), (uint64_t)S, kKp / 16, none) &&
+              encode_u8(m.dn_blocks, banks[3], ndn, (uint64_t)(I / 2), (uint64_t)S, kKp, sw) &&
+              encode_u8(m.dn_scales, banks[4], ndn, (uint64_t)(I / 32), (uint64_t)S, kKp / 16, none);
     m.valid = ok;
     return ok;
 }

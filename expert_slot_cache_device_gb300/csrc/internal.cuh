@@ -75,13 +75,16 @@ struct FfnScratch {
     uint16_t *x16;      // [bs, H] activations as f16, scaled by 2^-xexp[t] (nullptr: not prepared)
     int32_t *xexp;      // [bs] per-token power-of-two exponent of x16
     uint32_t *hmax;     // [P] bit pattern of max |h| per pair (order-independent atomicMax)
-    int32_t *upoff;     // [P] first pass (group of kPassTokens pairs) of each distinct slot
+    int32_t *upoff;     // [P] first pass (group of pass_tokens pairs) of each distinct slot
     int32_t *n_passes;  // [1] passes over all distinct slots
 };
 
-// Pipelined FFN kernels split each slot's routed pairs into passes of this many tokens;
-// every (pass, tile) is a separate work item so hot experts spread over the SMs.
+// Pipelined FFN kernels split each slot's routed pairs into passes of at most
+// FfnParams::pass_tokens tokens; every (pass, tile) is a separate work item so hot experts
+// spread over the SMs. The row-major kernels use kPassTokens, the transposed mxfp4
+// kernels (tensor-core N = 8) kMxPassTokens.
 constexpr int kPassTokens = 4;
+constexpr int kMxPassTokens = 8;
 
 struct FfnParams {
     FfnScratch s;
@@ -97,6 +100,7 @@ struct FfnParams {
     int32_t fmt, H, I, S, bs, topk, P;
     int32_t x16_emax;  // f16 activation copy keeps max |x| < 2^x16_emax
     int32_t x16_swz;   // f16 activation copy stored in the swz_x16 layout (nvfp4 rows kernels)
+    int32_t pass_tokens;  // tokens per pass of the pipelined kernels (kPassTokens / kMxPassTokens)
 };
 
 // Tensor maps (CUtensorMap, 128 bytes each) over the transposed mxfp4 slot banks.
