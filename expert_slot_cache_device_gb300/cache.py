@@ -92,6 +92,17 @@ class ExpertSlotCache:
     def set_copy_mode(self, mode: int):
         F.ftmoe_set_copy_mode(self.handle, mode)
 
+    def prefetch_layer(self, layer: int, stream=None):
+        F.ftmoe_prefetch_layer(self.handle, layer, _stream(stream))
+
+    def prefill_layers(self, layers, d_ids, d_x, d_w, d_y, compute_stream, copy_stream):
+        """Double-buffered prefill: lists of per-step device tensors (ids [bs, k] int32,
+        x [bs, H] bf16 bits, w [bs, k] fp32, y [bs, H] bf16 bits)."""
+        bs, k = d_ids[0].shape
+        F.ftmoe_prefill_layers(self.handle, list(layers), [t.data_ptr() for t in d_ids], bs, k,
+                               [t.data_ptr() for t in d_x], [t.data_ptr() for t in d_w],
+                               [t.data_ptr() for t in d_y], _stream(compute_stream), _stream(copy_stream))
+
     # ------------------------------------------------------------------ state
     def get_state(self, stream=None):
         S = self.cfg.S

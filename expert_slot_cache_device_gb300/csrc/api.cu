@@ -34,8 +34,8 @@ int cuda_fail(cudaError_t e, const char *what) {
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct Layout {
-    size_t hdr, id2slot, owner, stamp, miss_ids, miss_slots;
-    size_t n_unique, uslot, ucnt, uoff, upairs, h, o, x16, xexp, hmax, upoff;
+    size_t hdr, id2slot, owner, stamp, miss_ids, miss_slots, all_ids, pf_slots;
+    size_t n_unique, uslot, ucnt, uoff, upairs, h, o, x16, xexp, hmax, upoff, pipe_slots;
     size_t total;
     bool ffn;
 };
@@ -90,6 +90,8 @@ Layout make_layout(int fmt, int E, int L, int S, int H, int I, int max_pairs) {
     l.stamp = off; off += align256((size_t)S * 4);
     l.miss_ids = off; off += align256((size_t)maxm * 4);
     l.miss_slots = off; off += align256((size_t)maxm * 4);
+    l.all_ids = off; off += align256((size_t)E * 4);   // 0..E-1: the ids of a whole-layer prefetch
+    l.pf_slots = off; off += align256((size_t)E * 4);  // slots written by a whole-layer prefetch
     l.ffn = fmt != FTMOE_FMT_RAW && max_pairs > 0;
     if (l.ffn) {
         const size_t P = (size_t)max_pairs;
@@ -104,6 +106,7 @@ Layout make_layout(int fmt, int E, int L, int S, int H, int I, int max_pairs) {
         l.xexp = off; off += align256(P * 4);
         l.hmax = off; off += align256(P * 4);
         l.upoff = off; off += align256(P * 4);
+        l.pipe_slots = off; off += 2 * align256(P * 4);  // two routed-slot buffers of the prefill pipeline
     }
     l.total = off;
     return l;
@@ -144,7 +147,14 @@ struct ftmoe_cache {
     FfnScratch s;
     bool ffn;
     MxTmaMaps mx;
+    int32_t *all_ids = nullptr, *pf_slots = nullptr, *pipe_slots[2] = {nullptr, nullptr};
 };
+
+namespace {
+__global__ void iota_kernel(int32_t *p, int n) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = i;
+}
+}  // namespace
 
 extern "C" {
 
@@ -241,7 +251,11 @@ int ftmoe_cache_create(const ftmoe_bank_spec *banks, int32_t num_banks, int32_t 
     c->t.stamp = reinterpret_cast<uint32_t *>(ws + lay.stamp);
     c->t.miss_ids = reinterpret_cast<int32_t *>(ws + lay.miss_ids);
     c->t.miss_slots = reinterpret_cast<int32_t *>(ws + lay.miss_slots);
+    c->all_ids = reinterpret_cast<int32_t *>(ws + lay.all_ids);
+    c->pf_slots = reinterpret_cast<int32_t *>(ws + lay.pf_slots);
     if (lay.ffn) {
+        c->pipe_slots[0] = reinterpret_cast<int32_t *>(ws + lay.pipe_slots);
+        c->pipe_slots[1] = reinterpret_cast<int32_t *>(ws + lay.pipe_slots + align256((size_t)max_pairs * 4));
         c->s.n_unique = reinterpret_cast<int32_t *>(ws + lay.n_unique);
         c->s.uslot = reinterpret_cast<int32_t *>(ws + lay.uslot);
         c->s.ucnt = reinterpret_cast<int32_t *>(ws + lay.ucnt);
@@ -261,6 +275,10 @@ int ftmoe_cache_create(const ftmoe_bank_spec *banks, int32_t num_banks, int32_t 
         make_mx_tma_maps(c->mx, sb, S, H, I);  // on failure the FFN uses the register path
     }
     e = launch_init_state(c->t, E, L, S, static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) {
+        iota_kernel<<<(E + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(c->all_ids, E);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess) {
         delete c;
         return cuda_fail(e, "init state");
@@ -427,6 +445,82 @@ int ftmoe_expert_ffn_hybrid(ftmoe_cache_t *c, const void *d_x_bf16, int32_t bs, 
     p.fmt = c->fmt; p.H = c->H; p.I = c->I; p.S = c->S; p.bs = bs; p.topk = topk; p.P = (int)P;
     CK(launch_ffn(p, c->num_sms, static_cast<cudaStream_t>(stream), &c->mx), "ffn kernels");
     return FTMOE_OK;
+}
+
+int ftmoe_prefetch_layer(ftmoe_cache_t *c, int32_t layer, void *stream) {
+    if (!c) return fail(FTMOE_ERR_INVALID_ARG, "cache is NULL");
+    int rc = ensure_impl(c, layer, c->all_ids, 1, c->E, c->pf_slots, 0, -1, 0.f, nullptr, stream);
+    if (rc) return rc;
+    return ftmoe_copy_missing(c, stream);
+}
+
+int ftmoe_prefill_layers(ftmoe_cache_t *c, int32_t num_layers, const int32_t *h_layers,
+                         const int32_t *const *d_topk_ids, int32_t bs, int32_t topk, const void *const *d_x_bf16,
+                         const float *const *d_weights, void *const *d_y_bf16, void *compute_stream,
+                         void *copy_stream) {
+    if (!c) return fail(FTMOE_ERR_INVALID_ARG, "cache is NULL");
+    if (!c->ffn || c->fmt == FTMOE_FMT_RAW) return fail(FTMOE_ERR_INVALID_ARG, "the cache has no FFN");
+    if (num_layers <= 0) return FTMOE_OK;
+    if (!h_layers || !d_topk_ids || !d_x_bf16 || !d_weights || !d_y_bf16)
+        return fail(FTMOE_ERR_INVALID_ARG, "NULL per-layer array");
+    if ((int64_t)c->S < 2 * (int64_t)c->E)
+        return fail(FTMOE_ERR_INVALID_ARG, "whole-layer double buffering needs S >= 2E (S=%d, E=%d)", c->S, c->E);
+    if (bs <= 0 || topk <= 0 || (int64_t)bs * topk > c->max_pairs)
+        return fail(FTMOE_ERR_INVALID_ARG, "bs*topk must be in [1, max_pairs=%d]", c->max_pairs);
+    for (int i = 0; i < num_layers; i++) {
+        if (h_layers[i] < 0 || h_layers[i] >= c->L)
+            return fail(FTMOE_ERR_INVALID_ARG, "layer %d outside [0, %d)", h_layers[i], c->L);
+        if (!d_topk_ids[i] || !d_x_bf16[i] || !d_weights[i] || !d_y_bf16[i])
+            return fail(FTMOE_ERR_INVALID_ARG, "NULL pointer for pipeline step %d", i);
+    }
+    cudaStream_t cs = static_cast<cudaStream_t>(compute_stream), ps = static_cast<cudaStream_t>(copy_stream);
+    cudaEvent_t ready[2] = {nullptr, nullptr}, done[2] = {nullptr, nullptr};
+    int rc = FTMOE_OK;
+    for (int k = 0; k < 2; k++) {
+        cudaError_t e = cudaEventCreateWithFlags(&ready[k], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&done[k], cudaEventDisableTiming);
+        if (e != cudaSuccess) rc = cuda_fail(e, "event create");
+    }
+    // Copy stream: prefetch(step i) = every expert of the layer made resident and copied,
+    // then the routed ensure of the step (all hits) writes slot buffer i % 2. Compute
+    // stream: the FFN of step i waits for that. The prefetch of step i + 1 waits for the
+    // FFN of step i - 1: it evicts that step's slots and rewrites its slot buffer.
+    auto stage = [&](int i) -> int {
+        int r = ftmoe_prefetch_layer(c, h_layers[i], ps);
+        if (!r) r = ensure_impl(c, h_layers[i], d_topk_ids[i], bs, topk, c->pipe_slots[i & 1], 0, -1, 0.f, nullptr, ps);
+        if (!r) {
+            cudaError_t e = cudaEventRecord(ready[i & 1], ps);
+            if (e != cudaSuccess) r = cuda_fail(e, "event record");
+        }
+        return r;
+    };
+    if (!rc) rc = stage(0);
+    for (int i = 0; !rc && i < num_layers; i++) {
+        cudaError_t e = cudaStreamWaitEvent(cs, ready[i & 1], 0);
+        if (e != cudaSuccess) {
+            rc = cuda_fail(e, "stream wait");
+            break;
+        }
+        rc = ftmoe_expert_ffn(c, d_x_bf16[i], bs, c->pipe_slots[i & 1], d_weights[i], topk, d_y_bf16[i], cs);
+        if (rc) break;
+        e = cudaEventRecord(done[i & 1], cs);
+        if (e != cudaSuccess) {
+            rc = cuda_fail(e, "event record");
+            break;
+        }
+        if (i + 1 < num_layers) {
+            if (i >= 1 && (e = cudaStreamWaitEvent(ps, done[(i - 1) & 1], 0)) != cudaSuccess) {
+                rc = cuda_fail(e, "stream wait");
+                break;
+            }
+            rc = stage(i + 1);
+        }
+    }
+    for (int k = 0; k < 2; k++) {  // released once their pending work completes
+        if (ready[k]) cudaEventDestroy(ready[k]);
+        if (done[k]) cudaEventDestroy(done[k]);
+    }
+    return rc;
 }
 
 int ftmoe_cache_get_state(ftmoe_cache_t *c, int32_t *h_owner, uint32_t *h_stamp, uint32_t *h_clock, void *stream) {

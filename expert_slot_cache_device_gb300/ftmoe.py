@@ -29,7 +29,7 @@ EXPORTS = [
     "ftmoe_copy_missing", "ftmoe_expert_ffn", "ftmoe_set_copy_mode", "ftmoe_cache_get_state",
     "ftmoe_cache_set_state", "ftmoe_get_miss_list", "ftmoe_get_device_status", "ftmoe_h2d_stream_copy",
     "ftmoe_last_error", "ftmoe_expert_ffn_noalloc", "ftmoe_ensure_experts_hybrid", "ftmoe_hybrid_fetch_fraction",
-    "ftmoe_expert_ffn_hybrid", "ftmoe_cpu_expert_ffn",
+    "ftmoe_expert_ffn_hybrid", "ftmoe_cpu_expert_ffn", "ftmoe_prefetch_layer", "ftmoe_prefill_layers",
 ]
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -82,6 +82,8 @@ def lib() -> ctypes.CDLL:
         "ftmoe_hybrid_fetch_fraction": [ctypes.c_double, ctypes.c_double, P],
         "ftmoe_expert_ffn_hybrid": [P, P, i32, P, P, i32, P, P, P],
         "ftmoe_cpu_expert_ffn": [i32, i32, i32, i32, i32, P, P, P, P, P, P, P, i32],
+        "ftmoe_prefetch_layer": [P, i32, P],
+        "ftmoe_prefill_layers": [P, i32, P, P, i32, i32, P, P, P, P, P],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -206,3 +208,20 @@ def ftmoe_cpu_expert_ffn(fmt: int, H: int, I: int, bs: int, topk: int, h_topk_id
     bb = (ctypes.c_int64 * len(bank_bytes))(*bank_bytes)
     _check(lib().ftmoe_cpu_expert_ffn(fmt, H, I, bs, topk, h_topk_ids, h_slots, banks, bb, h_x, h_weights, h_y,
                                       threads))
+
+
+def ftmoe_prefetch_layer(cache: int, layer: int, stream: int) -> None:
+    _check(lib().ftmoe_prefetch_layer(cache, layer, stream))
+
+
+def ftmoe_prefill_layers(cache: int, layers: Sequence[int], d_topk_ids: Sequence[int], bs: int, topk: int,
+                         d_x: Sequence[int], d_weights: Sequence[int], d_y: Sequence[int], compute_stream: int,
+                         copy_stream: int) -> None:
+    """Per-step device pointers are passed as host arrays of addresses."""
+    n = len(layers)
+    if not (len(d_topk_ids) == len(d_x) == len(d_weights) == len(d_y) == n):
+        raise ValueError("one id, x, weight and y pointer per pipeline step")
+    lay = (ctypes.c_int32 * n)(*layers)
+    arr = lambda v: (ctypes.c_void_p * n)(*v)
+    _check(lib().ftmoe_prefill_layers(cache, n, lay, arr(d_topk_ids), bs, topk, arr(d_x), arr(d_weights),
+                                      arr(d_y), compute_stream, copy_stream))

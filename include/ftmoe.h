@@ -219,6 +219,36 @@ int ftmoe_cpu_expert_ffn(int32_t format, int32_t H, int32_t I, int32_t bs, int32
                          const uint16_t *h_x, const float *h_weights, float *h_y,
                          int32_t threads);
 
+/* Whole-layer prefetch (architecture deep-dive, section 五: the global LRU expert cache
+ * streams prefill layer by layer through a double buffer so that copies overlap compute).
+ * Enqueues on `stream` an ensure_experts of all E experts of `layer` (as if every expert
+ * were routed once, ids 0..E-1 in ascending order) followed by ftmoe_copy_missing in the
+ * cache's copy mode. The slots it assigns are written to workspace scratch, not returned.
+ * Same errors as those two calls; with FTMOE_COPY_ENGINE the call waits on the host for
+ * the ensure to finish (the miss list is read back) and then issues copy-engine transfers,
+ * which leave the SMs free for work on other streams. */
+int ftmoe_prefetch_layer(ftmoe_cache_t *cache, int32_t layer, void *stream);
+
+/* Double-buffered prefill over a sequence of layers (architecture deep-dive, section 五:
+ * whole-layer double-buffered prefill streaming, copy overlapped with compute). Step i
+ * runs layer h_layers[i] (host array, num_layers entries) for one batch: bs tokens,
+ * routed ids d_topk_ids[i] (device int32 [bs, topk]), activations d_x_bf16[i] (device
+ * bf16 [bs, H]), router weights d_weights[i] (device fp32 [bs, topk]), output
+ * d_y_bf16[i] (device bf16 [bs, H]); the four arrays of device pointers are host arrays.
+ * Schedule: on copy_stream, step i's ftmoe_prefetch_layer then its routed ensure (all hits)
+ * into one of two workspace slot buffers; on compute_stream, step i's expert FFN waits for
+ * that and runs while copy_stream prefetches step i + 1, which in turn waits for the FFN of
+ * step i - 1 (whose slots it may evict). The LRU sequence equals the calls prefetch(0),
+ * ensure(0), prefetch(1), ensure(1), ... made one after another. Needs S >= 2E (one layer
+ * computing, the next arriving) and 1 <= bs * topk <= max_pairs; -> FTMOE_ERR_INVALID_ARG
+ * otherwise. Returns once everything is enqueued (with FTMOE_COPY_ENGINE after the last
+ * prefetch's miss list was read); the caller synchronises compute_stream for the outputs.
+ * Device-detected errors land in the status word as for the single calls. */
+int ftmoe_prefill_layers(ftmoe_cache_t *cache, int32_t num_layers, const int32_t *h_layers,
+                         const int32_t *const *d_topk_ids, int32_t bs, int32_t topk,
+                         const void *const *d_x_bf16, const float *const *d_weights, void *const *d_y_bf16,
+                         void *compute_stream, void *copy_stream);
+
 /* Select the copy_missing implementation (FTMOE_COPY_*). */
 int ftmoe_set_copy_mode(ftmoe_cache_t *cache, int32_t mode);
 
