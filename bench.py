@@ -52,6 +52,7 @@ def parse():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-hybrid", action="store_true", help="skip the hybrid-path measurements")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill-pipeline measurements")
     ap.add_argument("--copy-mode", default="fused", choices=["fused", "per_bank", "engine"])
     ap.add_argument("--experts", type=int, default=0, help="override E (smaller profiling cases)")
     ap.add_argument("--slots", type=int, default=0, help="override S (smaller profiling cases)")
@@ -345,7 +346,9 @@ def run_gpu(args):
     bs, mr = args.bs, args.miss_rate
     r = wl.make_route(cfg, bs, mr)
     B = cfg.bytes_per_expert
-    cache = ExpertSlotCache(cfg, max(max(cfg.bs_list), bs) * cfg.topk, stream=stream)
+    # every layer's host source aliases layer 0's bank (allowed by the per-layer source
+    # lists) so that the prefill probe can stream any layer
+    cache = ExpertSlotCache(cfg, max(max(cfg.bs_list), bs, PREFILL_BS) * cfg.topk, alias_all=True, stream=stream)
     cache.set_copy_mode({"fused": F.COPY_FUSED, "per_bank": F.COPY_PER_BANK, "engine": F.COPY_ENGINE}[args.copy_mode])
     s = stream.cuda_stream
     d_ids = torch.from_numpy(r.topk_ids).cuda()
@@ -473,6 +476,8 @@ def run_gpu(args):
             line["sweep"] = sweep(args, cfg, cache, stream, torch, F, wl)
         if not args.no_hybrid:
             line["hybrid"] = hybrid_probe(args, cfg, cache, stream, torch, F, wl, link, cpu_cores())
+        if not args.no_prefill:
+            line["prefill"] = prefill_probe(cfg, cache, torch, F)
     cache.close()
     if rank == 0 and not args.no_cpu_baseline:
         hb = [cache.host[b][0].numpy() for b in range(cache.nb)]
@@ -489,6 +494,93 @@ def run_gpu(args):
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+PREFILL_BS = 64      # tokens of the prefill batch of the pipeline probe
+PREFILL_LAYERS = 6   # layers streamed by the probe
+
+
+def prefill_probe(cfg, cache, torch, F):
+    """Whole-layer double-buffered prefill (architecture deep-dive, section 五): a batch of
+    PREFILL_BS tokens through PREFILL_LAYERS layers, every expert of each layer streamed in
+    (prefetch) before its FFN. Times the same calls one after another on one stream (SM
+    copy kernel) and the two-stream pipeline ftmoe_prefill_layers with the copy engines and
+    with the SM copy kernel, plus the prefetch and the FFN alone for reference. Wall time
+    around each run, the device synchronised on both sides; the cache starts empty."""
+    if cfg.S < 2 * cfg.E:
+        return {"skipped": f"needs S >= 2E (S={cfg.S}, E={cfg.E})"}
+    rng = np.random.default_rng(20260)
+    bs, k, L = PREFILL_BS, cfg.topk, PREFILL_LAYERS
+    layers = [l % cfg.L for l in range(L)]
+    ids = [torch.from_numpy(np.stack([rng.permutation(cfg.E)[:k] for _ in range(bs)]).astype(np.int32)).cuda()
+           for _ in range(L)]
+    w = [torch.full((bs, k), 1.0 / k, dtype=torch.float32, device="cuda") for _ in range(L)]
+    x = [torch.from_numpy(wl_bits(rng.standard_normal((bs, cfg.H)).astype(np.float32))).view(torch.bfloat16).cuda()
+         for _ in range(L)]
+    y = [torch.empty((bs, cfg.H), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+    d_slots = torch.empty((bs, k), dtype=torch.int32, device="cuda")
+    compute, copy = torch.cuda.Stream(), torch.cuda.Stream()
+    empty_owner = np.full(cfg.S, -1, np.int32)
+    empty_stamp = np.zeros(cfg.S, np.uint32)
+    B = cfg.bytes_per_expert
+
+    def reset():
+        cache.set_state(empty_owner, empty_stamp, 0, stream=compute)
+        torch.cuda.synchronize()
+
+    def timed(fn, reps=3):
+        best = None
+        for _ in range(reps):
+            reset()
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize()
+            dt = time.perf_counter() - t0
+            best = dt if best is None else min(best, dt)
+        return best * 1e3
+
+    def sequential():
+        for i, l in enumerate(layers):
+            cache.prefetch_layer(l, compute)
+            cache.ensure(l, ids[i], d_slots, compute)
+            cache.ffn(x[i], d_slots, w[i], y[i], compute)
+
+    def prefetch_only():
+        for l in layers:
+            cache.prefetch_layer(l, compute)
+
+    def ffn_only():  # every layer's experts are resident after one prefetch of the same layer
+        for i, l in enumerate(layers):
+            cache.ensure(l, ids[i], d_slots, compute)
+            cache.ffn(x[i], d_slots, w[i], y[i], compute)
+
+    out = {"tokens": bs, "layers": L, "bytes_per_layer": cfg.E * B}
+    cache.set_copy_mode(F.COPY_FUSED)
+    out["sequential_ms"] = timed(sequential)
+    out["prefetch_only_ms"] = timed(prefetch_only)
+    reset()
+    cache.prefetch_layer(layers[0], compute)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i, l in enumerate(layers[:1] * L):
+        cache.ensure(l, ids[i], d_slots, compute)
+        cache.ffn(x[i], d_slots, w[i], y[i], compute)
+    torch.cuda.synchronize()
+    out["ffn_only_ms"] = (time.perf_counter() - t0) * 1e3
+    for mode, name in ((F.COPY_ENGINE, "pipelined_engine_ms"), (F.COPY_FUSED, "pipelined_sm_copy_ms")):
+        cache.set_copy_mode(mode)
+        out[name] = timed(lambda: cache.prefill_layers(layers, ids, x, w, y, compute, copy))
+    cache.set_copy_mode(F.COPY_FUSED)
+    best = min(out["pipelined_engine_ms"], out["pipelined_sm_copy_ms"])
+    out["overlap_speedup"] = out["sequential_ms"] / best
+    out["link_GBps_pipelined"] = L * cfg.E * B / (best / 1e3) / 1e9
+    reset()
+    return out
+
+
+def wl_bits(a):
+    from expert_slot_cache_device_gb300 import workload as wl
+    return wl.f32_to_bf16_bits(a).view(np.int16)
 
 
 def hybrid_probe(args, cfg, cache, stream, torch, F, wl, link_gbps, cores):

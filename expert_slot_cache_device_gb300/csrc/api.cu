@@ -148,6 +148,10 @@ struct ftmoe_cache {
     bool ffn;
     MxTmaMaps mx;
     int32_t *all_ids = nullptr, *pf_slots = nullptr, *pipe_slots[2] = {nullptr, nullptr};
+    cudaStream_t aux = nullptr;  // copy-engine stream of the prefill pipeline (created on first use)
+    ~ftmoe_cache() {
+        if (aux) cudaStreamDestroy(aux);
+    }
 };
 
 namespace {
@@ -372,6 +376,37 @@ static void fill_copy_params(const ftmoe_cache *c, int b_first, int b_count, Cop
     p.tile0[b_count] = tiles;
 }
 
+// Copy-engine arm of copy_missing: reads the last ensure's miss list back (waiting on
+// read_st) and issues one cudaMemcpyAsync per (miss, bank) on copy_st.
+static int copy_engine(ftmoe_cache_t *c, cudaStream_t read_st, cudaStream_t copy_st) {
+    const int maxm = c->E < c->S ? c->E : c->S;
+    std::vector<int32_t> ids(maxm), slots(maxm);
+    int32_t m = 0;
+    CK(cudaMemcpyAsync(&m, c->t.num_miss, 4, cudaMemcpyDeviceToHost, read_st), "read miss count");
+    CK(cudaStreamSynchronize(read_st), "sync");
+    if (m > 0) {
+        CK(cudaMemcpyAsync(ids.data(), c->t.miss_ids, (size_t)m * 4, cudaMemcpyDeviceToHost, read_st), "read miss ids");
+        CK(cudaMemcpyAsync(slots.data(), c->t.miss_slots, (size_t)m * 4, cudaMemcpyDeviceToHost, read_st),
+           "read miss slots");
+        CK(cudaStreamSynchronize(read_st), "sync");
+    }
+    // misses come in ascending expert id; a run of consecutive experts landing in
+    // consecutive slots is contiguous on both sides, so it is one transfer per bank
+    for (int j = 0; j < m;) {
+        const int64_t e = ids[j] % c->E, s = slots[j];
+        int run = 1;
+        while (j + run < m && ids[j + run] == ids[j] + run && slots[j + run] == slots[j] + run) run++;
+        for (int b = 0; b < c->nb; b++) {
+            const unsigned char *src = static_cast<const unsigned char *>(c->host[b][c->last_layer]) + e * c->bytes[b];
+            CK(cudaMemcpyAsync(c->dev_slots[b] + s * c->bytes[b], src, (size_t)run * c->bytes[b],
+                               cudaMemcpyHostToDevice, copy_st),
+               "copy engine");
+        }
+        j += run;
+    }
+    return FTMOE_OK;
+}
+
 int ftmoe_copy_missing(ftmoe_cache_t *c, void *stream) {
     if (!c) return fail(FTMOE_ERR_INVALID_ARG, "cache is NULL");
     if (c->last_layer < 0) return fail(FTMOE_ERR_STATE, "copy_missing before any ensure_experts call");
@@ -388,25 +423,7 @@ int ftmoe_copy_missing(ftmoe_cache_t *c, void *stream) {
             CK(launch_copy(p, c->vec16, grid, st), "copy kernel (per bank)");
         }
     } else {
-        const int maxm = c->E < c->S ? c->E : c->S;
-        std::vector<int32_t> ids(maxm), slots(maxm);
-        int32_t m = 0;
-        CK(cudaMemcpyAsync(&m, c->t.num_miss, 4, cudaMemcpyDeviceToHost, st), "read miss count");
-        CK(cudaStreamSynchronize(st), "sync");
-        if (m > 0) {
-            CK(cudaMemcpyAsync(ids.data(), c->t.miss_ids, (size_t)m * 4, cudaMemcpyDeviceToHost, st), "read miss ids");
-            CK(cudaMemcpyAsync(slots.data(), c->t.miss_slots, (size_t)m * 4, cudaMemcpyDeviceToHost, st), "read miss slots");
-            CK(cudaStreamSynchronize(st), "sync");
-        }
-        for (int j = 0; j < m; j++) {
-            const int64_t e = ids[j] % c->E, s = slots[j];
-            for (int b = 0; b < c->nb; b++) {
-                const unsigned char *src = static_cast<const unsigned char *>(c->host[b][c->last_layer]) + e * c->bytes[b];
-                CK(cudaMemcpyAsync(c->dev_slots[b] + s * c->bytes[b], src, (size_t)c->bytes[b],
-                                   cudaMemcpyHostToDevice, st),
-                   "copy engine");
-            }
-        }
+        return copy_engine(c, st, st);
     }
     return FTMOE_OK;
 }
@@ -474,51 +491,66 @@ int ftmoe_prefill_layers(ftmoe_cache_t *c, int32_t num_layers, const int32_t *h_
             return fail(FTMOE_ERR_INVALID_ARG, "NULL pointer for pipeline step %d", i);
     }
     cudaStream_t cs = static_cast<cudaStream_t>(compute_stream), ps = static_cast<cudaStream_t>(copy_stream);
-    cudaEvent_t ready[2] = {nullptr, nullptr}, done[2] = {nullptr, nullptr};
+    const bool engine = c->copy_mode == FTMOE_COPY_ENGINE;
+    if (engine && !c->aux) {
+        cudaError_t e = cudaStreamCreateWithFlags(&c->aux, cudaStreamNonBlocking);
+        if (e != cudaSuccess) {
+            c->aux = nullptr;
+            return cuda_fail(e, "stream create");
+        }
+    }
+    cudaEvent_t ready[2] = {nullptr, nullptr}, done[2] = {nullptr, nullptr}, cdone[2] = {nullptr, nullptr};
     int rc = FTMOE_OK;
-    for (int k = 0; k < 2; k++) {
+    for (int k = 0; k < 2 && !rc; k++) {
         cudaError_t e = cudaEventCreateWithFlags(&ready[k], cudaEventDisableTiming);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&done[k], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&cdone[k], cudaEventDisableTiming);
         if (e != cudaSuccess) rc = cuda_fail(e, "event create");
     }
-    // Copy stream: prefetch(step i) = every expert of the layer made resident and copied,
-    // then the routed ensure of the step (all hits) writes slot buffer i % 2. Compute
-    // stream: the FFN of step i waits for that. The prefetch of step i + 1 waits for the
-    // FFN of step i - 1: it evicts that step's slots and rewrites its slot buffer.
+    auto record = [&](cudaEvent_t ev, cudaStream_t st) -> int {
+        cudaError_t e = cudaEventRecord(ev, st);
+        return e == cudaSuccess ? FTMOE_OK : cuda_fail(e, "event record");
+    };
+    auto wait = [&](cudaStream_t st, cudaEvent_t ev) -> int {
+        cudaError_t e = cudaStreamWaitEvent(st, ev, 0);
+        return e == cudaSuccess ? FTMOE_OK : cuda_fail(e, "stream wait");
+    };
+    // Step i's slots replace those of step i - 2 (S >= 2E and LRU order), so its copies and
+    // its routed-slot buffer (i % 2) wait for the FFN of step i - 2.
+    // SM-copy modes, all on copy_stream: prefetch(i) (ensure of every expert + copy kernel),
+    // routed ensure -> ready[i % 2]; the FFN of step i waits for ready[i % 2].
+    // Copy-engine mode: the ensures stay on copy_stream (the miss list is read back from it
+    // at once, not behind the previous step's transfers) while the transfers queue on an
+    // internal stream -> cdone[i % 2]; the FFN of step i waits for ready and cdone.
     auto stage = [&](int i) -> int {
-        int r = ftmoe_prefetch_layer(c, h_layers[i], ps);
-        if (!r) r = ensure_impl(c, h_layers[i], d_topk_ids[i], bs, topk, c->pipe_slots[i & 1], 0, -1, 0.f, nullptr, ps);
+        int r = FTMOE_OK;
+        if (i >= 2) r = wait(ps, done[i & 1]);
+        if (!r) r = ensure_impl(c, h_layers[i], c->all_ids, 1, c->E, c->pf_slots, 0, -1, 0.f, nullptr, ps);
         if (!r) {
-            cudaError_t e = cudaEventRecord(ready[i & 1], ps);
-            if (e != cudaSuccess) r = cuda_fail(e, "event record");
+            if (engine) {
+                if (i >= 2) r = wait(c->aux, done[i & 1]);
+                if (!r) r = copy_engine(c, ps, c->aux);
+                if (!r) r = record(cdone[i & 1], c->aux);
+            } else {
+                r = ftmoe_copy_missing(c, ps);
+            }
         }
+        if (!r) r = ensure_impl(c, h_layers[i], d_topk_ids[i], bs, topk, c->pipe_slots[i & 1], 0, -1, 0.f, nullptr, ps);
+        if (!r) r = record(ready[i & 1], ps);
         return r;
     };
     if (!rc) rc = stage(0);
     for (int i = 0; !rc && i < num_layers; i++) {
-        cudaError_t e = cudaStreamWaitEvent(cs, ready[i & 1], 0);
-        if (e != cudaSuccess) {
-            rc = cuda_fail(e, "stream wait");
-            break;
-        }
-        rc = ftmoe_expert_ffn(c, d_x_bf16[i], bs, c->pipe_slots[i & 1], d_weights[i], topk, d_y_bf16[i], cs);
-        if (rc) break;
-        e = cudaEventRecord(done[i & 1], cs);
-        if (e != cudaSuccess) {
-            rc = cuda_fail(e, "event record");
-            break;
-        }
-        if (i + 1 < num_layers) {
-            if (i >= 1 && (e = cudaStreamWaitEvent(ps, done[(i - 1) & 1], 0)) != cudaSuccess) {
-                rc = cuda_fail(e, "stream wait");
-                break;
-            }
-            rc = stage(i + 1);
-        }
+        rc = wait(cs, ready[i & 1]);
+        if (!rc && engine) rc = wait(cs, cdone[i & 1]);
+        if (!rc) rc = ftmoe_expert_ffn(c, d_x_bf16[i], bs, c->pipe_slots[i & 1], d_weights[i], topk, d_y_bf16[i], cs);
+        if (!rc) rc = record(done[i & 1], cs);
+        if (!rc && i + 1 < num_layers) rc = stage(i + 1);
     }
     for (int k = 0; k < 2; k++) {  // released once their pending work completes
         if (ready[k]) cudaEventDestroy(ready[k]);
         if (done[k]) cudaEventDestroy(done[k]);
+        if (cdone[k]) cudaEventDestroy(cdone[k]);
     }
     return rc;
 }

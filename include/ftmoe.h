@@ -77,7 +77,8 @@ extern "C" {
 #define FTMOE_COPY_PER_BANK 1 /* one kernel launch per bank */
 #define FTMOE_COPY_ENGINE 2   /* copy engines: reads the miss list back to the host
                                  (synchronises the stream), then one cudaMemcpyAsync
-                                 per (miss, bank) */
+                                 per bank and run of consecutive experts landing in
+                                 consecutive slots (a single miss is a run of one) */
 
 /* Limits of one cache. */
 #define FTMOE_MAX_BANKS 8
@@ -237,13 +238,17 @@ int ftmoe_prefetch_layer(ftmoe_cache_t *cache, int32_t layer, void *stream);
  * d_y_bf16[i] (device bf16 [bs, H]); the four arrays of device pointers are host arrays.
  * Schedule: on copy_stream, step i's ftmoe_prefetch_layer then its routed ensure (all hits)
  * into one of two workspace slot buffers; on compute_stream, step i's expert FFN waits for
- * that and runs while copy_stream prefetches step i + 1, which in turn waits for the FFN of
- * step i - 1 (whose slots it may evict). The LRU sequence equals the calls prefetch(0),
- * ensure(0), prefetch(1), ensure(1), ... made one after another. Needs S >= 2E (one layer
- * computing, the next arriving) and 1 <= bs * topk <= max_pairs; -> FTMOE_ERR_INVALID_ARG
- * otherwise. Returns once everything is enqueued (with FTMOE_COPY_ENGINE after the last
- * prefetch's miss list was read); the caller synchronises compute_stream for the outputs.
- * Device-detected errors land in the status word as for the single calls. */
+ * that and runs while step i + 1 is prefetched. Step i's copies and slot buffer wait for the
+ * FFN of step i - 2, whose slots they replace. With FTMOE_COPY_ENGINE the ensures stay on
+ * copy_stream, the miss list of each prefetch is read back from it right away, and the
+ * transfers queue on a stream the cache creates on first use (destroyed with the cache), so
+ * the copy engines stay busy back to back while the SMs run the FFN; the FFN of a step then
+ * also waits for its transfers. The LRU sequence equals the calls prefetch(0), ensure(0),
+ * prefetch(1), ensure(1), ... made one after another. Needs S >= 2E (one layer computing,
+ * the next arriving) and 1 <= bs * topk <= max_pairs; -> FTMOE_ERR_INVALID_ARG otherwise.
+ * Returns once everything is enqueued (the host waits for the miss lists in copy-engine
+ * mode); the caller synchronises compute_stream for the outputs. Device-detected errors land
+ * in the status word as for the single calls. */
 int ftmoe_prefill_layers(ftmoe_cache_t *cache, int32_t num_layers, const int32_t *h_layers,
                          const int32_t *const *d_topk_ids, int32_t bs, int32_t topk,
                          const void *const *d_x_bf16, const float *const *d_weights, void *const *d_y_bf16,
