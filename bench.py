@@ -197,28 +197,14 @@ def measured_peaks():
 
 
 def link_peak(torch, F, stream):
-    """Host-to-device link ceiling in this run: best of 5 for a 1 GiB pinned->device
-    cudaMemcpyAsync and for the SM zero-copy read kernel."""
+    """Host-to-device link ceiling in this run (ftmoe_measure_link): best of 5 for a 1 GiB
+    pinned->device cudaMemcpyAsync and for the SM zero-copy read kernel."""
     src = torch.empty(LINK_PROBE_BYTES, dtype=torch.uint8, pin_memory=True)
     src.fill_(7)
     dst = torch.empty(LINK_PROBE_BYTES, dtype=torch.uint8, device="cuda")
-    out = {}
-    for name in ("memcpy", "sm_read"):
-        best = 1e30
-        for _ in range(5):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            if name == "memcpy":
-                with torch.cuda.stream(stream):
-                    dst.copy_(src, non_blocking=True)
-            else:
-                F.ftmoe_h2d_stream_copy(dst.data_ptr(), src.data_ptr(), LINK_PROBE_BYTES, stream.cuda_stream)
-            b.record(stream)
-            b.synchronize()
-            best = min(best, a.elapsed_time(b) / 1e3)
-        out[name] = LINK_PROBE_BYTES / best / 1e9
+    mc, sm = F.ftmoe_measure_link(src.data_ptr(), dst.data_ptr(), LINK_PROBE_BYTES, 5, stream.cuda_stream)
     del src, dst
-    return out
+    return {"memcpy": mc, "sm_read": sm}
 
 
 def cpu_cores():
@@ -596,23 +582,14 @@ def hybrid_probe(args, cfg, cache, stream, torch, F, wl, link_gbps, cores):
     bank_ptrs = [cache.host_ptrs[b][0] for b in range(cache.nb)]
     bank_bytes = [g.bytes for g in cache.schema]
     fmt = F.FORMATS[cfg.fmt]
-    # CPU executor bandwidth: every routed pair of a 2-token batch on distinct experts
+    # CPU executor bandwidth (ftmoe_measure_cpu_moe) and the backend decision
+    # (ftmoe_moe_backend_decision, default threshold 2x)
     k = cfg.topk
-    ids = np.arange(2 * k, dtype=np.int32).reshape(2, k) % cfg.E
-    sl = np.full((2, k), -1, np.int32)
-    x = np.zeros((2, cfg.H), np.uint16)
-    w = np.ones((2, k), np.float32)
-    y = np.empty((2, cfg.H), np.float32)
-    times = []
-    for _ in range(3):
-        t0 = time.perf_counter()
-        F.ftmoe_cpu_expert_ffn(fmt, cfg.H, cfg.I, 2, k, ids.ctypes.data, sl.ctypes.data, bank_ptrs, bank_bytes,
-                               x.ctypes.data, w.ctypes.data, y.ctypes.data, cores)
-        times.append(time.perf_counter() - t0)
-    cpu_gbps = 2 * k * B / min(times) / 1e9
-    frac = F.ftmoe_hybrid_fetch_fraction(link_gbps, cpu_gbps)
+    cpu_gbps = F.ftmoe_measure_cpu_moe(fmt, cfg.H, cfg.I, cfg.E, bank_ptrs, bank_bytes, 2 * k, cores, 3)
+    backend, frac = F.ftmoe_moe_backend_decision(fmt, link_gbps, cpu_gbps, 0.0)
     out = {"cpu_moe_GBps": cpu_gbps, "link_GBps": link_gbps, "cores": cores,
-           "decision": "hybrid" if cpu_gbps > 2 * link_gbps else "offload", "fetch_fraction": frac}
+           "decision": "hybrid" if backend == F.BACKEND_HYBRID else "offload",
+           "fetch_fraction": F.ftmoe_hybrid_fetch_fraction(link_gbps, cpu_gbps)}
 
     r = wl.make_route(cfg, args.bs, args.miss_rate)
     install_hits(cache, r)

@@ -132,6 +132,7 @@ int check_geometry(int fmt, int nb, int E, int L, int S, int H, int I, int max_p
 }  // namespace
 
 int ftmoe::report_error(int code, const char *msg) { return fail(code, "%s", msg); }
+int ftmoe_probe_report(int code, const char *msg) { return fail(code, "%s", msg); }
 
 struct ftmoe_cache {
     int fmt, E, L, S, H, I, max_pairs, nb;

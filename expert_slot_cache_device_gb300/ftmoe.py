@@ -30,7 +30,9 @@ EXPORTS = [
     "ftmoe_cache_set_state", "ftmoe_get_miss_list", "ftmoe_get_device_status", "ftmoe_h2d_stream_copy",
     "ftmoe_last_error", "ftmoe_expert_ffn_noalloc", "ftmoe_ensure_experts_hybrid", "ftmoe_hybrid_fetch_fraction",
     "ftmoe_expert_ffn_hybrid", "ftmoe_cpu_expert_ffn", "ftmoe_prefetch_layer", "ftmoe_prefill_layers",
+    "ftmoe_measure_link", "ftmoe_measure_cpu_moe", "ftmoe_moe_backend_decision",
 ]
+BACKEND_OFFLOAD, BACKEND_HYBRID = 0, 1
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -84,6 +86,9 @@ def lib() -> ctypes.CDLL:
         "ftmoe_cpu_expert_ffn": [i32, i32, i32, i32, i32, P, P, P, P, P, P, P, i32],
         "ftmoe_prefetch_layer": [P, i32, P],
         "ftmoe_prefill_layers": [P, i32, P, P, i32, i32, P, P, P, P, P],
+        "ftmoe_measure_link": [P, P, sz, i32, P, P, P],
+        "ftmoe_measure_cpu_moe": [i32, i32, i32, i32, P, P, i32, i32, i32, P],
+        "ftmoe_moe_backend_decision": [i32, ctypes.c_double, ctypes.c_double, ctypes.c_double, P, P],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -225,3 +230,27 @@ def ftmoe_prefill_layers(cache: int, layers: Sequence[int], d_topk_ids: Sequence
     arr = lambda v: (ctypes.c_void_p * n)(*v)
     _check(lib().ftmoe_prefill_layers(cache, n, lay, arr(d_topk_ids), bs, topk, arr(d_x), arr(d_weights),
                                       arr(d_y), compute_stream, copy_stream))
+
+
+def ftmoe_measure_link(h_src: int, d_dst: int, nbytes: int, reps: int, stream: int):
+    """Returns (memcpy GB/s, SM read GB/s)."""
+    a, b = ctypes.c_double(0), ctypes.c_double(0)
+    _check(lib().ftmoe_measure_link(h_src, d_dst, nbytes, reps, stream, ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
+
+
+def ftmoe_measure_cpu_moe(fmt: int, H: int, I: int, E: int, layer_banks: Sequence[int], bank_bytes: Sequence[int],
+                          experts: int, threads: int, reps: int) -> float:
+    nb = len(layer_banks)
+    out = ctypes.c_double(0)
+    _check(lib().ftmoe_measure_cpu_moe(fmt, H, I, E, (ctypes.c_void_p * nb)(*layer_banks),
+                                       (ctypes.c_int64 * nb)(*bank_bytes), experts, threads, reps,
+                                       ctypes.byref(out)))
+    return out.value
+
+
+def ftmoe_moe_backend_decision(fmt: int, link_gbps: float, cpu_gbps: float, threshold: float = 0.0):
+    """Returns (backend, fetch_fraction)."""
+    be, fr = ctypes.c_int32(0), ctypes.c_float(0)
+    _check(lib().ftmoe_moe_backend_decision(fmt, link_gbps, cpu_gbps, threshold, ctypes.byref(be), ctypes.byref(fr)))
+    return be.value, fr.value

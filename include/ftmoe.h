@@ -254,6 +254,35 @@ int ftmoe_prefill_layers(ftmoe_cache_t *cache, int32_t num_layers, const int32_t
                          const void *const *d_x_bf16, const float *const *d_weights, void *const *d_y_bf16,
                          void *compute_stream, void *copy_stream);
 
+/* MoE backends of the decision below. */
+#define FTMOE_BACKEND_OFFLOAD 0  /* fetch every miss over the host link */
+#define FTMOE_BACKEND_HYBRID 1   /* fetch a share, compute the rest on the host CPU */
+
+/* Host -> device link probe (benchmark guide, section 5.2: the pinned -> device gather
+ * bandwidth, the linear pinned <-> device copy ceiling). Times `bytes` from the page-locked
+ * host buffer h_src to the device buffer d_dst on `stream`, best of `reps`, once with
+ * cudaMemcpyAsync (copy engines) and once with the SM zero-copy read kernel of
+ * ftmoe_h2d_stream_copy; writes both rates in GB/s (1e9 bytes/s). Synchronises the stream.
+ * Caller-owned buffers; FTMOE_ERR_INVALID_ARG for NULL pointers, bytes == 0 or reps <= 0. */
+int ftmoe_measure_link(const void *h_src, void *d_dst, size_t bytes, int32_t reps, void *stream,
+                       double *memcpy_gbps, double *sm_read_gbps);
+
+/* CPU MoE probe (benchmark guide, section 5.2: the bandwidth the CPU MoE kernel reaches on
+ * the host's memory). Runs ftmoe_cpu_expert_ffn on `experts` tokens, each routed to a
+ * different expert (t % E) of the layer banks h_layer_banks (host, schema order, bank_bytes
+ * per expert), best of `reps`; *gbps = experts * bytes per expert / time. Host only.
+ * FTMOE_ERR_FORMAT for formats without a CPU MoE path. */
+int ftmoe_measure_cpu_moe(int32_t format, int32_t H, int32_t I, int32_t E, const void *const *h_layer_banks,
+                          const int64_t *bank_bytes, int32_t experts, int32_t threads, int32_t reps,
+                          double *gbps);
+
+/* Backend decision (benchmark guide, section 5.2): FTMOE_BACKEND_HYBRID when the format has
+ * a CPU MoE path and cpu_gbps > threshold * link_gbps (threshold <= 0: the default 2.0),
+ * with *fetch_fraction from ftmoe_hybrid_fetch_fraction; otherwise FTMOE_BACKEND_OFFLOAD
+ * with *fetch_fraction = 1. Formats without a CPU path (raw) always offload. Host only. */
+int ftmoe_moe_backend_decision(int32_t format, double link_gbps, double cpu_gbps, double threshold,
+                               int32_t *backend, float *fetch_fraction);
+
 /* Select the copy_missing implementation (FTMOE_COPY_*). */
 int ftmoe_set_copy_mode(ftmoe_cache_t *cache, int32_t mode);
 
