@@ -60,6 +60,9 @@ CONFIGS: Dict[str, Config] = {
                  (1, 16, 64), (0.05, 0.5), "zipf", 1.1, 0),
     "c5": Config("c5", "bf16_trace_E256_k8_H4096_I1536_L61_S1024", 4, "bf16", 256, 8, 4096, 1536, 61,
                  1024, (1,), (), "zipf", 1.2, 7, steps=512),
+    # block-FP8 layer: the nvfp4 layer's shape with the block-FP8 bank schema
+    "c6": Config("c6", "fp8_E256_k8_H7168_I2048_L58_S512", 5, "fp8", 256, 8, 7168, 2048, 58, 512,
+                 (1, 8, 32), (0.1, 0.3, 1.0), "uniform", 0.0, 0),
 }
 
 
@@ -112,6 +115,14 @@ def bank_schema(cfg: Config) -> List[BankGeom]:
             BankGeom("down_scales", "e8m0", I // 32, H),
             BankGeom("down_bias", "bf16", H, 2),
         ]
+    if cfg.fmt == "fp8":
+        # block FP8: e4m3 weights [N, K] and one binary32 scale per 128 x 128 block
+        return [
+            BankGeom("gate_up_weight", "e4m3", 2 * I, H),
+            BankGeom("gate_up_scale", "f32", (2 * I + 127) // 128, 4 * ((H + 127) // 128)),
+            BankGeom("down_weight", "e4m3", H, I),
+            BankGeom("down_scale", "f32", (H + 127) // 128, 4 * ((I + 127) // 128)),
+        ]
     raise ValueError(f"unknown format {cfg.fmt!r}")
 
 
@@ -145,6 +156,7 @@ def f32_to_e4m3_bits(a: np.ndarray) -> np.ndarray:
 
 
 _SEED_BANK = 0xBA4C
+FP8_Q_STD = 112.0  # standard deviation of the synthetic block-FP8 codes (before e4m3 rounding)
 
 
 def _gen_bank_expert(cfg: Config, b: int, geom: BankGeom, e: int) -> np.ndarray:
@@ -158,9 +170,18 @@ def _gen_bank_expert(cfg: Config, b: int, geom: BankGeom, e: int) -> np.ndarray:
         std = 0.02
         vals = rng.standard_normal(n, dtype=np.float32) * np.float32(std)
         return f32_to_bf16_bits(vals).view(np.uint8)
+    if geom.dtype == "e4m3" and name.endswith("_weight"):
+        # block-FP8 weights: N(0, 1) * 112, so a block's largest |value| reaches the top
+        # of the e4m3 range (448) the way a max-scaled quantisation does
+        vals = rng.standard_normal(geom.bytes, dtype=np.float32) * np.float32(FP8_Q_STD)
+        return f32_to_e4m3_bits(vals)
     if geom.dtype == "e4m3":
         vals = np.abs(rng.standard_normal(geom.bytes, dtype=np.float32))
         return f32_to_e4m3_bits(vals)
+    if geom.dtype == "f32":
+        # block scales: w = q * s has standard deviation ~0.02 * (0.5 + U)
+        u = rng.random(geom.bytes // 4)
+        return ((0.5 + u) * (0.02 / FP8_Q_STD)).astype(np.float32).view(np.uint8)
     if geom.dtype == "f16":
         # Per-output-row global of nvfp4; sized so the row dot product is O(1):
         # 8.5625 is the mean square of the 16 e2m1 code values, K the reduction length.
@@ -216,9 +237,15 @@ def fill_bank_device(cfg: Config, b: int, out, experts: Optional[Sequence[int]] 
             t = torch.randint(0, 256, (n,), dtype=torch.uint8, device=device, generator=gen)
         elif geom.dtype == "bf16":
             t = (torch.randn(n // 2, device=device, generator=gen) * 0.02).to(torch.bfloat16).view(torch.uint8)
+        elif geom.dtype == "e4m3" and geom.name.endswith("_weight"):
+            v = (torch.randn(n, device=device, generator=gen) * FP8_Q_STD).clamp(-448.0, 448.0)
+            t = v.to(torch.float8_e4m3fn).view(torch.uint8)
         elif geom.dtype == "e4m3":
             v = torch.randn(n, device=device, generator=gen).abs().clamp(max=448.0)
             t = v.to(torch.float8_e4m3fn).view(torch.uint8)
+        elif geom.dtype == "f32":
+            u = torch.rand(n // 4, device=device, generator=gen, dtype=torch.float64)
+            t = ((0.5 + u) * (0.02 / FP8_Q_STD)).to(torch.float32).view(torch.uint8)
         elif geom.dtype == "f16":
             K = cfg.H if geom.name.startswith("gate_up") else cfg.I
             u = torch.rand(n // 2, device=device, generator=gen, dtype=torch.float64)

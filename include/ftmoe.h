@@ -63,6 +63,10 @@ extern "C" {
                              global [2I] f16, down codes [H, I/2], scales [H, I/16], global [H] */
 #define FTMOE_FMT_MXFP4 3 /* banks (transposed): gate_up blocks [H/2, 2I] u8, scales [H/32, 2I]
                              e8m0, bias [2I] bf16, down blocks [I/2, H], scales [I/32, H], bias [H] */
+#define FTMOE_FMT_FP8 4   /* block FP8 (architecture deep-dive, section 五 lists it among the
+                             bank schemas): gate_up weight [2I, H] e4m3, scale [2I/128, H/128]
+                             f32 (one per 128 x 128 block), down weight [H, I] e4m3, scale
+                             [H/128, I/128] f32; H and I multiples of 512. No CPU MoE path. */
 
 /* element types of a bank (informative; FFN formats check them against the schema) */
 #define FTMOE_DT_U8 0
@@ -70,6 +74,7 @@ extern "C" {
 #define FTMOE_DT_F16 2
 #define FTMOE_DT_E4M3 3
 #define FTMOE_DT_E8M0 4
+#define FTMOE_DT_F32 5
 
 /* copy_missing implementations (benchmark guide, section 4.4: the fused multi-bank
  * copy is the main path; the per-bank path is kept for A/B comparison) */

@@ -14,12 +14,15 @@
  *          global [N] fp16; w = e2m1 * e4m3 * f16.
  *   mxfp4  blocks [K/2, N] (transposed; low nibble = even k), scales [K/32, N]
  *          e8m0 (2^(b - 127)), bias [N] bf16; w = e2m1 * 2^(b - 127).
+ *   fp8    block FP8 ([ARCH] section 五 lists "FP8 block" among the bank schemas):
+ *          weight [N, K] e4m3fn output-row-major, scale [N/128, K/128] binary32
+ *          row-major, one per 128 x 128 block; w = e4m3 * scale[n / 128][k / 128].
  *   FFN    gu = W_gu x (+ b_gu), h = silu(gu[0:I]) * gu[I:2I],
  *          o = W_d h (+ b_d), y_t = sum_j w_{t,j} o_{t,j}; all in fp64.
  * Number formats follow their published definitions: OCP 8-bit floating point
  * (E4M3, bias 7, no infinities, S.1111.111 = NaN), OCP Microscaling v1.0
- * (E2M1 with bias 1, E8M0 = 2^(e - 127), 0xFF = NaN), IEEE 754 binary16, and
- * bfloat16 = the upper half of an IEEE binary32.
+ * (E2M1 with bias 1, E8M0 = 2^(e - 127), 0xFF = NaN), IEEE 754 binary16 and
+ * binary32 (little-endian bytes), and bfloat16 = the upper half of a binary32.
  */
 #include <math.h>
 #include <stdlib.h>
@@ -88,6 +91,14 @@ double orc_decode(int32_t kind, uint32_t bits) {
 
 static uint32_t rd16(const uint8_t *p, int64_t i) { return (uint32_t)p[2 * i] | ((uint32_t)p[2 * i + 1] << 8); }
 
+static double rdf32(const uint8_t *p, int64_t i) {
+    uint32_t u = (uint32_t)p[4 * i] | ((uint32_t)p[4 * i + 1] << 8) | ((uint32_t)p[4 * i + 2] << 16) |
+                 ((uint32_t)p[4 * i + 3] << 24);
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
 static uint32_t nibble(uint8_t byte, int64_t k) { return (k % 2 == 0) ? (byte & 15u) : (byte >> 4); }
 
 int32_t orc_num_banks(int32_t fmt) {
@@ -95,6 +106,7 @@ int32_t orc_num_banks(int32_t fmt) {
         case ORC_FMT_BF16: return 2;
         case ORC_FMT_NVFP4: return 6;
         case ORC_FMT_MXFP4: return 6;
+        case ORC_FMT_FP8: return 4;
         default: return -1;
     }
 }
@@ -124,6 +136,12 @@ double orc_weight(int32_t fmt, int32_t which, const uint8_t *const *banks, int32
         double c = dec_e2m1(nibble(blocks[(k / 2) * N + n], k));
         double s = dec_e8m0(scales[(k / 32) * N + n]);
         return c * s;
+    }
+    if (fmt == ORC_FMT_FP8) {
+        const uint8_t *wq = banks[2 * which + 0];
+        const uint8_t *sc = banks[2 * which + 1];
+        int64_t kb = (K + 127) / 128; /* scale blocks along k */
+        return dec_e4m3(wq[n * K + k]) * rdf32(sc, (n / 128) * kb + k / 128);
     }
     return NAN;
 }
