@@ -285,6 +285,14 @@ int ftmoe_cache_create(const ftmoe_bank_spec *banks, int32_t num_banks, int32_t 
         for (int b = 0; b < 6; b++) sb[b] = c->dev_slots[b];
         make_mx_tma_maps(c->mx, sb, S, H, I);  // on failure the FFN uses the register path
     }
+    if (format == FTMOE_FMT_FP8 && lay.ffn) {
+        const unsigned char *sb[4];
+        for (int b = 0; b < 4; b++) sb[b] = c->dev_slots[b];
+        if (!make_fp8_tma_maps(c->mx, sb, S, H, I)) {  // block FP8 has no other FFN path
+            delete c;
+            return fail(FTMOE_ERR_FORMAT, "block FP8: tensor maps over the slot banks could not be encoded");
+        }
+    }
     e = launch_init_state(c->t, E, L, S, static_cast<cudaStream_t>(stream));
     if (e == cudaSuccess) {
         iota_kernel<<<(E + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(c->all_ids, E);

@@ -745,10 +745,12 @@ cudaError_t launch_ffn(const FfnParams &p_in, int num_sms, cudaStream_t st, cons
     }
     const bool fp4_rows_tma = num_sms > 0 && ffn_rows_tma_supported(p);
     const bool mx_tma = num_sms > 0 && ffn_mx_tma_supported(p, mx);
-    const bool want_x16 = (fp4_rows_tma && p.fmt == FTMOE_FMT_NVFP4) || mx_tma;
+    const bool fp8_tma = num_sms > 0 && ffn_fp8_tma_supported(p, mx);
+    if (p.fmt == FTMOE_FMT_FP8 && !fp8_tma) return cudaErrorNotSupported;  // block FP8 has one pipeline only
+    const bool want_x16 = (fp4_rows_tma && p.fmt == FTMOE_FMT_NVFP4) || mx_tma || fp8_tma;
     p.x16_emax = p.fmt == FTMOE_FMT_MXFP4 ? 9 : 10;
     p.x16_swz = fp4_rows_tma && p.fmt == FTMOE_FMT_NVFP4;
-    p.pass_tokens = mx_tma ? kMxPassTokens : kPassTokens;
+    p.pass_tokens = (mx_tma || fp8_tma) ? kMxPassTokens : kPassTokens;
     ffn_route_kernel<<<1 + (want_x16 ? p.bs : 0), 1024, route_smem, st>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
@@ -760,6 +762,9 @@ cudaError_t launch_ffn(const FfnParams &p_in, int num_sms, cudaStream_t st, cons
         pdl_combine = true;
     } else if (mx_tma) {
         if ((e = launch_ffn_mx_tma(p, *mx, num_sms, st)) != cudaSuccess) return e;
+        pdl_combine = true;
+    } else if (fp8_tma) {
+        if ((e = launch_ffn_fp8_tma(p, *mx, num_sms, st)) != cudaSuccess) return e;
         pdl_combine = true;
     } else if (p.fmt == FTMOE_FMT_BF16 || p.fmt == FTMOE_FMT_NVFP4) {
         const int tiles_gu = (p.I + kGuNeurons - 1) / kGuNeurons;

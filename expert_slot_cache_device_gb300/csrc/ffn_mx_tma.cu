@@ -34,11 +34,13 @@
 
 #include "ffn_common.cuh"
 #include "internal.cuh"
+#include "pipeline.cuh"
 
 namespace ftmoe {
 namespace {
 
 using namespace ffn;
+using namespace pipe;
 
 constexpr int kCW = 16;                     // consumer warps
 constexpr int kMxThreads = (kCW + 1) * 32;  // + producer warp
@@ -49,7 +51,6 @@ constexpr int kMxTokMax = 8;                // tokens per pass = the MMA's N
 constexpr int kBlkPairs = kKp / 32;         // consumer warps per column half
 static_assert(kBlkPairs * 2 == kCW, "two column halves x eight pairs of scale blocks");
 static_assert(kMxTokMax == kMxPassTokens, "the routing kernel cuts passes of kMxTokMax tokens");
-constexpr uint64_t kWaitNs = 2000000000ull;
 
 enum { kGU = 0, kDN = 1 };
 
@@ -66,100 +67,9 @@ struct MxCfg {
     int32_t tiles, kst, stages, stage_bytes, tok_off, tok_stride, sc_off, tg, red_off, bias_off;
 };
 
-__device__ __forceinline__ uint32_t su32(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
-
-__device__ __forceinline__ uint64_t gtimer() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void bar_init(uint64_t *b, uint32_t n) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(n) : "memory");
-}
-__device__ __forceinline__ void bar_expect(uint64_t *b, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void bar_arrive(uint64_t *b) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
-}
-__device__ __forceinline__ bool bar_wait(uint64_t *b, uint32_t parity) {
-    const uint64_t t0 = gtimer();
-    for (uint32_t i = 0;; i++) {
-        uint32_t ok;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(ok)
-            : "r"(su32(b)), "r"(parity)
-            : "memory");
-        if (ok) return true;
-        if ((i & 255) == 255 && gtimer() - t0 > kWaitNs) return false;
-    }
-}
-
-__device__ __forceinline__ void tma3d(void *dst, const CUtensorMap *map, int x, int y, int z, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-        "[%5];" ::"r"(su32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(su32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void bulk1d(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     su32(dst)),
-                 "l"(src), "r"(bytes), "r"(su32(bar))
-                 : "memory");
-}
-
 // Shared-memory byte of logical (row, byte) of a 128-byte-swizzled code tile whose base
 // is 1024-byte aligned: the 16-byte chunk index is XORed with the row's index mod 8.
 __device__ __forceinline__ int swz128(int row, int byte) { return row * kCols + (byte ^ ((row & 7) << 4)); }
-
-__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                              uint32_t b0, uint32_t b1) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// Same with a zero accumulator input (d = A * B).
-__device__ __forceinline__ void mma_f16_16816_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                                uint32_t b0, uint32_t b1) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%10, %10, %10, %10};"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
-}
-
-// Two e8m0 bytes (low byte first) -> their values 2^(b - 127) as floats, through the
-// exact ue8m0 -> bf16 conversion (bf16 has f32's exponent range, so bf16 << 16 is the
-// f32 value; 0 gives the bf16 subnormal 2^-127, 0xff NaN).
-__device__ __forceinline__ float2 e8m0x2_to_f2(uint32_t two_bytes) {
-    uint32_t b;
-    asm("{\n\t.reg .b16 s;\n\t"
-        "cvt.u16.u32 s, %1;\n\t"
-        "cvt.rn.bf16x2.ue8m0x2 %0, s;\n\t}"
-        : "=r"(b)
-        : "r"(two_bytes & 0xffffu));
-    return make_float2(__uint_as_float(b << 16), __uint_as_float(b & 0xffff0000u));
-}
-
-// (a0, a1) += (t0, t1) * s with one packed fp32 FMA.
-__device__ __forceinline__ void ffma2_s(float &a0, float &a1, float t0, float t1, float s) {
-    uint64_t r;
-    asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
-        "mov.b64 ra, {%1, %2};\n\t"
-        "mov.b64 rb, {%3, %3};\n\t"
-        "mov.b64 rc, {%4, %5};\n\t"
-        "fma.rn.f32x2 %0, ra, rb, rc;\n\t}"
-        : "=l"(r)
-        : "f"(t0), "f"(t1), "f"(s), "f"(a0), "f"(a1));
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(r));
-}
 
 // One stage of one consumer warp: scale blocks 2bp and 2bp + 1 of the stage, column half
 // hf (M tiles j = 4hf..4hf+3 of the item, here indexed 0..3), all NM matrices.
@@ -595,6 +505,17 @@ bool make_mx_tma_maps(MxTmaMaps &m, const unsigned char *const *banks, int S, in
               encode_u8(m.gu_scales, banks[1], ngu, (uint64_t)(H / 32), (uint64_t)S, kKp / 16, none) &&
               encode_u8(m.dn_blocks, banks[3], ndn, (uint64_t)(I / 2), (uint64_t)S, kKp, sw) &&
               encode_u8(m.dn_scales, banks[4], ndn, (uint64_t)(I / 32), (uint64_t)S, kKp / 16, none);
+    m.valid = ok;
+    return ok;
+}
+
+bool make_fp8_tma_maps(MxTmaMaps &m, const unsigned char *const *banks, int S, int H, int I) {
+    m.valid = false;
+    if (H % 512 || I % 512) return false;
+    // block-FP8 weights [N rows, K bytes] per slot, boxes of 128 k x 64 rows, 128-byte swizzle
+    const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    bool ok = encode_u8(m.gu_blocks, banks[0], (uint64_t)H, 2ull * I, (uint64_t)S, 64, sw) &&
+              encode_u8(m.dn_blocks, banks[2], (uint64_t)I, (uint64_t)H, (uint64_t)S, 64, sw);
     m.valid = ok;
     return ok;
 }

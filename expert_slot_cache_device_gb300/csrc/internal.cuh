@@ -104,6 +104,8 @@ struct FfnParams {
 };
 
 // Tensor maps (CUtensorMap, 128 bytes each) over the transposed mxfp4 slot banks.
+// Tensor maps (CUtensorMap, 128 bytes each) of the tensor-map pipelines: the transposed
+// mxfp4 banks, or the block-FP8 weight banks (gu_blocks / dn_blocks).
 struct MxTmaMaps {
     alignas(128) unsigned char gu_blocks[128];
     alignas(128) unsigned char gu_scales[128];
@@ -119,6 +121,10 @@ cudaError_t launch_ffn_rows_tma(const FfnParams &p, int num_sms, cudaStream_t st
 // 2-D tensor-map pipeline for the transposed mxfp4 format.
 bool ffn_mx_tma_supported(const FfnParams &p, const MxTmaMaps *maps);
 cudaError_t launch_ffn_mx_tma(const FfnParams &p, const MxTmaMaps &maps, int num_sms, cudaStream_t st);
+// Tensor-map pipeline for block FP8 (its weight maps sit in gu_blocks / dn_blocks).
+bool make_fp8_tma_maps(MxTmaMaps &m, const unsigned char *const *banks, int S, int H, int I);
+bool ffn_fp8_tma_supported(const FfnParams &p, const MxTmaMaps *maps);
+cudaError_t launch_ffn_fp8_tma(const FfnParams &p, const MxTmaMaps &maps, int num_sms, cudaStream_t st);
 
 // Record `msg` as the thread's last error message and return `code`.
 int report_error(int code, const char *msg);

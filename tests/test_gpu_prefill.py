@@ -23,6 +23,7 @@ CASES = {
     "bf16": wl.scaled(wl.CONFIGS["c2"], E=16, topk=4, H=256, I=128, L=4, S=32),
     "nvfp4": wl.scaled(wl.CONFIGS["c3"], E=8, topk=4, H=512, I=256, L=3, S=16),
     "mxfp4": wl.scaled(wl.CONFIGS["c4"], E=8, topk=4, H=256, I=256, L=3, S=16),
+    "fp8": wl.scaled(wl.CONFIGS["c6"], E=8, topk=4, H=512, I=512, L=3, S=16),
 }
 
 
