@@ -5,20 +5,20 @@
 // schemas; read here as) hold e4m3 weights [N, K] output-row-major and one binary32
 // scale per 128 x 128 block ([N/128, K/128]); w = e4m3 * scale. A work item is (distinct
 // slot u, pass of up to eight tokens, tile of 64 output rows); it streams the reduction
-// axis in stages of 256 k. A producer thread loads each stage with 3-D tensor copies
-// (cp.async.bulk.tensor over [slot, row, k], two boxes of 128 k x 64 rows per matrix,
+// axis in stages of 256 k (gate_up, two matrices) or 512 k (down). A producer thread loads each stage with 3-D tensor copies
+// (cp.async.bulk.tensor over [slot, row, k], boxes of 128 k x 64 rows per matrix,
 // stored with the 128-byte shared-memory swizzle), 1-D bulk copies of the item's block-
 // scale row per matrix (a 64-row tile lies inside one 128-row block) and of the tokens'
 // activations for those 256 k, all completing on the stage's mbarrier.
 //
 // The contraction runs on mma.sync m16n8k16 (f16 x f16 -> fp32): M = 16 output rows,
 // N = 8 tokens, K = 16. Consumer warp w takes M tile w % 4 (rows 16 (w % 4) ..) and a
-// quarter of the stage's k (64 k = four k steps, inside one 128-k scale block). Lane
+// quarter of the stage's k (64 or 128 k, inside one 128-k scale block). Lane
 // (g, tig) reads the 32-bit word at k = 4 tig of rows g and g + 8 of the k step; with
 // cvt.rn.f16x2.e4m3x2 (exact) its low half gives the fragment registers of logical k
 // (2 tig, 2 tig + 1) and its high half those of (2 tig + 8, 2 tig + 9), and the B
 // fragment is the token's activations at the same four k (one 64-bit load). With the
-// swizzle a warp's 32 weight loads hit 32 distinct banks. The four k steps are summed
+// swizzle a warp's 32 weight loads hit 32 distinct banks. A warp's k steps are summed
 // from zero on the tensor cores, then multiplied by the block scale in fp32 and added
 // to the item's accumulator. After the last stage of an item the warps' partials meet
 // in shared memory behind an mbarrier (bounded wait); gate_up writes h = silu(g) * u and
@@ -42,11 +42,15 @@ constexpr int kFCW = 16;                      // consumer warps
 constexpr int kFThreads = (kFCW + 1) * 32;    // + producer warp
 constexpr int kFRows = 64;                    // output rows per item (four M tiles)
 constexpr int kFBox = 128;                    // k per tensor box (one 128-byte box row)
-constexpr int kFKs = 256;                     // k per stage (two boxes)
+// k per stage: 256 (two boxes) for gate_up, which stages two matrices, 512 (four boxes)
+// for down; a consumer warp takes a quarter of it (64 or 128 k, inside one scale block)
+template <int PHASE>
+constexpr int kfks() { return PHASE == 0 ? 256 : 512; }
+constexpr int kRedStride = kFRows + 4;        // padded row of the reduction buffer
 constexpr int kFStagesMax = 4;
 constexpr int kFTok = 8;                      // tokens per pass = the MMA's N
 static_assert(kFTok == kMxPassTokens, "the routing kernel cuts passes of kFTok tokens");
-static_assert(kFCW == 4 * (kFKs / 64), "four M tiles x four k quarters");
+static_assert(kFCW == 16, "four M tiles x four k quarters");
 
 enum { kGU = 0, kDN = 1 };
 
@@ -67,17 +71,18 @@ __device__ __forceinline__ int swz(int row, int byte) { return row * kFBox + (by
 // Two e4m3 codes (low byte first) -> f16x2 (exact).
 __device__ __forceinline__ uint32_t e4m3x2_h2(uint32_t two) { return e4m3x2_to_h2(two); }
 
-template <int NM, bool DOWN>
+template <int NM, bool DOWN, int KS>
 __device__ __forceinline__ void f8_stage_mma(const unsigned char *st, const F8Cfg &c, int mt, int kq, int ntok,
                                              float tok_scale, int kb_first, float (&acc)[NM][4]) {
+    constexpr int KW = KS / 4;  // k of this warp in the stage (64 or 128: one scale block at most)
     const int lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
     const unsigned char *tokp = st + c.tok_off + g * c.tok_stride;
-    const int box = kq >> 1;
+    const int box = (kq * KW) / kFBox, inbox = (kq * KW) % kFBox;
     float tmp[NM][4];
 #pragma unroll
-    for (int ks = 0; ks < 4; ks++) {
-        const int kk = kq * 64 + ks * 16;          // k of this step inside the stage
-        const int byte = 16 * (4 * (kq & 1) + ks) + 4 * tig;  // inside the 128-byte box row
+    for (int ks = 0; ks < KW / 16; ks++) {
+        const int kk = kq * KW + ks * 16;      // k of this step inside the stage
+        const int byte = inbox + 16 * ks + 4 * tig;  // inside the 128-byte box row
         uint32_t b0 = 0u, b1 = 0u;
         if (g < ntok) {
             if (DOWN) {
@@ -92,7 +97,7 @@ __device__ __forceinline__ void f8_stage_mma(const unsigned char *st, const F8Cf
         }
 #pragma unroll
         for (int m = 0; m < NM; m++) {
-            const unsigned char *tile = st + (m * 2 + box) * (kFRows * kFBox);
+            const unsigned char *tile = st + (m * (KS / kFBox) + box) * (kFRows * kFBox);
             const uint32_t wA = *reinterpret_cast<const uint32_t *>(tile + swz(16 * mt + g, byte));
             const uint32_t wB = *reinterpret_cast<const uint32_t *>(tile + swz(16 * mt + g + 8, byte));
             const uint32_t a0 = e4m3x2_h2(wA & 0xffffu), a2 = e4m3x2_h2(wA >> 16);
@@ -103,10 +108,10 @@ __device__ __forceinline__ void f8_stage_mma(const unsigned char *st, const F8Cf
                 mma_f16_16816(tmp[m], a0, a1, a2, a3, b0, b1);
         }
     }
-    // the four k steps lie in one 128 x 128 block: one binary32 scale per matrix
+    // the warp's k steps lie in one 128 x 128 block: one binary32 scale per matrix
 #pragma unroll
     for (int m = 0; m < NM; m++) {
-        const float s = reinterpret_cast<const float *>(st + c.sc_off + m * c.sc_bytes)[kb_first + (kq >> 1)];
+        const float s = reinterpret_cast<const float *>(st + c.sc_off + m * c.sc_bytes)[kb_first + box];
         ffma2_s(acc[m][0], acc[m][1], tmp[m][0], tmp[m][1], s);
         ffma2_s(acc[m][2], acc[m][3], tmp[m][2], tmp[m][3], s);
     }
@@ -116,6 +121,7 @@ template <int PHASE>
 __global__ void __launch_bounds__(kFThreads, 1)
     ffn_fp8_tma_kernel(FfnParams p, F8Cfg c, const __grid_constant__ CUtensorMap wmap) {
     constexpr int NM = PHASE == kGU ? 2 : 1;
+    constexpr int kFKs = kfks<PHASE>();
     extern __shared__ __align__(1024) unsigned char sm[];
     uint64_t *full = reinterpret_cast<uint64_t *>(sm);
     uint64_t *empty = full + kFStagesMax;
@@ -152,7 +158,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
         const int last = (int)((int64_t)(blockIdx.x + 1) * items / gridDim.x);
         bool waited = PHASE == kGU, ok = true;
         int issued = 0;
-        const uint32_t box_bytes = NM * 2 * kFRows * kFBox;
+        const uint32_t box_bytes = NM * (kFKs / kFBox) * kFRows * kFBox;
         const uint32_t tb = kFKs * (PHASE == kGU ? 2u : 4u);  // token bytes per stage
         int u = items > first ? pass_owner(p.s.upoff, nu, first / c.tiles) : 0;
         int cur_pi = -1, slot = 0, cnt = 0;
@@ -210,8 +216,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 const int k0 = ks * kFKs;
                 for (int m = 0; m < NM; m++) {
                     const int row = n0 + (m ? I : 0);
-                    tma3d(st + (m * 2 + 0) * (kFRows * kFBox), &wmap, k0, row, slot, &full[s]);
-                    tma3d(st + (m * 2 + 1) * (kFRows * kFBox), &wmap, k0 + kFBox, row, slot, &full[s]);
+                    for (int bx = 0; bx < kFKs / kFBox; bx++)
+                        tma3d(st + (m * (kFKs / kFBox) + bx) * (kFRows * kFBox), &wmap, k0 + bx * kFBox, row, slot,
+                              &full[s]);
                     // the 64-row tile lies in one 128-row block: its scale row
                     bulk1d(st + c.sc_off + m * c.sc_bytes, scb + (int64_t)slot * scb_bytes + (int64_t)(row / 128) * KB * 4,
                            (uint32_t)c.sc_bytes, &full[s]);
@@ -264,25 +271,26 @@ __global__ void __launch_bounds__(kFThreads, 1)
         const bool last = hs.last;
         const unsigned char *st = stage0 + (size_t)s * c.stage_bytes;
         const float tok_scale = g < ntok ? ldexpf(1.f, -hs.texp[g]) : 0.f;
-        f8_stage_mma<NM, PHASE == kDN>(st, c, mt, kq, ntok, tok_scale, hs.kstage * (kFKs / 128), acc);
+        f8_stage_mma<NM, PHASE == kDN, kFKs>(st, c, mt, kq, ntok, tok_scale, hs.kstage * (kFKs / 128), acc);
         if (!last) {
             __syncwarp();
             if (lane == 0) bar_arrive(&empty[s]);
             continue;
         }
 
-        // item end: partials meet in red [NM][4 k quarters][kFRows][kFTok]
+        // item end: partials meet in red [NM][4 k quarters][kFTok][kRedStride] (the padded
+        // row keeps both the fragment stores and the row-wise sums free of bank conflicts)
 #pragma unroll
         for (int m = 0; m < NM; m++) {
-            float *r = red + ((m * 4 + kq) * kFRows) * kFTok;
+            float *r = red + ((m * 4 + kq) * kFTok) * kRedStride;
             const int r0 = 16 * mt + g, t0 = 2 * tig;
             if (t0 < ntok) {
-                r[r0 * kFTok + t0] = acc[m][0];
-                r[(r0 + 8) * kFTok + t0] = acc[m][2];
+                r[t0 * kRedStride + r0] = acc[m][0];
+                r[t0 * kRedStride + r0 + 8] = acc[m][2];
             }
             if (t0 + 1 < ntok) {
-                r[r0 * kFTok + t0 + 1] = acc[m][1];
-                r[(r0 + 8) * kFTok + t0 + 1] = acc[m][3];
+                r[(t0 + 1) * kRedStride + r0] = acc[m][1];
+                r[(t0 + 1) * kRedStride + r0 + 8] = acc[m][3];
             }
 #pragma unroll
             for (int i = 0; i < 4; i++) acc[m][i] = 0.f;
@@ -304,7 +312,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
             for (int m = 0; m < NM; m++) {
                 float sum = 0.f;
 #pragma unroll
-                for (int q4 = 0; q4 < 4; q4++) sum += red[((m * 4 + q4) * kFRows + row) * kFTok + t];
+                for (int q4 = 0; q4 < 4; q4++) sum += red[((m * 4 + q4) * kFTok + t) * kRedStride + row];
                 v[m] = sum * xs_t;
             }
             const int q = hs.pairs[t];
@@ -334,16 +342,17 @@ bool make_f8_cfg(const FfnParams &p, int phase, F8Cfg &c, size_t &smem) {
     const int K = phase == kGU ? p.H : p.I;
     const int nout = phase == kGU ? p.I : p.H;
     const int NM = phase == kGU ? 2 : 1;
+    const int kFKs = phase == kGU ? kfks<kGU>() : kfks<kDN>();
     if (K % 512 || nout % kFRows) return false;
     c.tiles = nout / kFRows;
     c.kst = K / kFKs;
     c.sc_bytes = (K / 128) * 4;  // one block-scale row (a multiple of 16 bytes)
-    c.sc_off = NM * 2 * kFRows * kFBox;
+    c.sc_off = NM * kFKs * kFRows;
     // token rows padded by 32 / 64 bytes so the eight tokens' B loads hit distinct banks
     c.tok_stride = phase == kGU ? kFKs * 2 + 32 : kFKs * 4 + 64;
     c.tok_off = (c.sc_off + NM * c.sc_bytes + 15) & ~15;
     c.stage_bytes = (c.tok_off + kFTok * c.tok_stride + 1023) & ~1023;
-    const size_t red = (size_t)NM * 4 * kFRows * kFTok * 4;
+    const size_t red = (size_t)NM * 4 * kFTok * kRedStride * 4;
     const size_t head = 256 + kFStagesMax * sizeof(F8Hdr) + 1024;  // + alignment slack
     const size_t cap = 227 * 1024;
     int stages = kFStagesMax;
