@@ -5,7 +5,7 @@
 // schemas; read here as) hold e4m3 weights [N, K] output-row-major and one binary32
 // scale per 128 x 128 block ([N/128, K/128]); w = e4m3 * scale. A work item is (distinct
 // slot u, pass of up to eight tokens, tile of 64 output rows); it streams the reduction
-// axis in stages of 256 k (gate_up, two matrices) or 512 k (down). A producer thread loads each stage with 3-D tensor copies
+// axis in stages of 512 k. A producer thread loads each stage with 3-D tensor copies
 // (cp.async.bulk.tensor over [slot, row, k], boxes of 128 k x 64 rows per matrix,
 // stored with the 128-byte shared-memory swizzle), 1-D bulk copies of the item's block-
 // scale row per matrix (a 64-row tile lies inside one 128-row block) and of the tokens'
@@ -13,7 +13,7 @@
 //
 // The contraction runs on mma.sync m16n8k16 (f16 x f16 -> fp32): M = 16 output rows,
 // N = 8 tokens, K = 16. Consumer warp w takes M tile w % 4 (rows 16 (w % 4) ..) and a
-// quarter of the stage's k (64 or 128 k, inside one 128-k scale block). Lane
+// quarter of the stage's k (128 k, one 128-k scale block). Lane
 // (g, tig) reads the 32-bit word at k = 4 tig of rows g and g + 8 of the k step; with
 // cvt.rn.f16x2.e4m3x2 (exact) its low half gives the fragment registers of logical k
 // (2 tig, 2 tig + 1) and its high half those of (2 tig + 8, 2 tig + 9), and the B
@@ -42,10 +42,10 @@ constexpr int kFCW = 16;                      // consumer warps
 constexpr int kFThreads = (kFCW + 1) * 32;    // + producer warp
 constexpr int kFRows = 64;                    // output rows per item (four M tiles)
 constexpr int kFBox = 128;                    // k per tensor box (one 128-byte box row)
-// k per stage: 256 (two boxes) for gate_up, which stages two matrices, 512 (four boxes)
-// for down; a consumer warp takes a quarter of it (64 or 128 k, inside one scale block)
+// k per stage: 512 (four boxes per matrix); a consumer warp takes a quarter of it (128 k,
+// exactly one scale block). Fewer, larger stages keep more bytes in flight per hand-off.
 template <int PHASE>
-constexpr int kfks() { return PHASE == 0 ? 256 : 512; }
+constexpr int kfks() { return 512; }
 constexpr int kRedStride = kFRows + 4;        // padded row of the reduction buffer
 constexpr int kFStagesMax = 4;
 constexpr int kFTok = 8;                      // tokens per pass = the MMA's N
