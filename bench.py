@@ -329,6 +329,12 @@ def run_gpu(args):
     cfg = wl.CONFIGS[args.config]
     if args.experts or args.slots:
         cfg = wl.scaled(cfg, E=args.experts or cfg.E, S=args.slots or cfg.S)
+    if cfg.steps > 0:  # the multi-step decode trace has its own measurement
+        line = run_trace(cfg, stream, torch, F, wl, ExpertSlotCache)
+        line.update({"n_gpus": world, "steps": args.steps, "warmup": args.warmup})
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return 0
     bs, mr = args.bs, args.miss_rate
     r = wl.make_route(cfg, bs, mr)
     B = cfg.bytes_per_expert
@@ -567,6 +573,66 @@ def prefill_probe(cfg, cache, torch, F):
 def wl_bits(a):
     from expert_slot_cache_device_gb300 import workload as wl
     return wl.f32_to_bf16_bits(a).view(np.int16)
+
+
+def run_trace(cfg, stream, torch, F, wl, ExpertSlotCache):
+    """The multi-step decode trace: every (step, layer) call of cfg.steps steps x cfg.L
+    layers at bs 1, from a cold cache, each call ensure + copy_missing + expert FFN on one
+    stream. All inputs are generated and moved to the device before the timed region.
+    CUDA events around every call give the ensure+copy and FFN times; the library's
+    cumulative counters give calls, distinct ids and fetched misses."""
+    k, n = cfg.topk, cfg.steps * cfg.L
+    ids = np.empty((n, 1, k), np.int32)
+    ws = np.empty((n, 1, k), np.float32)
+    xs = np.empty((n, 1, cfg.H), np.uint16)
+    for step in range(cfg.steps):
+        for layer in range(cfg.L):
+            i = step * cfg.L + layer
+            ids[i], ws[i], xs[i] = wl.trace_call(cfg, step, layer)
+    cache = ExpertSlotCache(cfg, k, alias_all=True, stream=stream)
+    d_ids = torch.from_numpy(ids).cuda()
+    d_w = torch.from_numpy(ws).cuda()
+    d_x = torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16).cuda()
+    d_slots = torch.empty((1, k), dtype=torch.int32, device="cuda")
+    d_y = torch.empty((1, cfg.H), dtype=torch.bfloat16, device="cuda")
+    s = stream.cuda_stream
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    torch.cuda.synchronize()
+    cache.counters(reset=True)
+    clk = ClockSampler(torch.cuda.current_device())
+    clk.start()
+    for step in range(cfg.steps):
+        for layer in range(cfg.L):
+            i = step * cfg.L + layer
+            ev[i][0].record(stream)
+            cache.ensure(layer, d_ids[i], d_slots, stream=s)
+            cache.copy_missing(stream=s)
+            ev[i][1].record(stream)
+            cache.ffn(d_x[i], d_slots, d_w[i], d_y, stream=s)
+            ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    clocks = clk.stop()
+    calls, unique, misses = cache.counters()
+    assert cache.status() == F.OK and calls == n
+    fetch = np.array([ev[i][0].elapsed_time(ev[i][1]) for i in range(n)]).reshape(cfg.steps, cfg.L)
+    ffn = np.array([ev[i][1].elapsed_time(ev[i][2]) for i in range(n)]).reshape(cfg.steps, cfg.L)
+    B = cfg.bytes_per_expert
+    step_ms = fetch.sum(1)
+    cache.close()
+    return {
+        "metric": METRIC, "value": misses * B / (fetch.sum() / 1e3) / 1e9, "unit": "GB/s",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{cfg.name} trace: {cfg.steps} steps x {cfg.L} layers, bs 1, zipf({cfg.zipf_a}) ids, "
+                               f"cold start", "E": cfg.E, "topk": k, "H": cfg.H, "I": cfg.I, "L": cfg.L, "S": cfg.S,
+                   "l2": "inputs larger than L2 (each miss copies 36 MiB)"},
+        "trace": {"calls": calls, "distinct_ids": unique, "misses": misses, "hit_rate": 1.0 - misses / unique,
+                  "copied_GB": misses * B / 1e9, "fetch_ms_total": float(fetch.sum()),
+                  "ffn_ms_total": float(ffn.sum()),
+                  "tok_ms": {"mean": float(step_ms.mean()), "p50": float(np.percentile(step_ms, 50)),
+                             "p99": float(np.percentile(step_ms, 99)), "first_step": float(step_ms[0])},
+                  "ffn_ms_per_token": float(ffn.sum(1).mean())},
+        "clocks": clocks,
+    }
 
 
 def hybrid_probe(args, cfg, cache, stream, torch, F, wl, link_gbps, cores):

@@ -125,6 +125,10 @@ class ExpertSlotCache:
         F.ftmoe_get_miss_list(self.handle, ids.ctypes.data, slots.ctypes.data, m.ctypes.data, _stream(stream))
         return ids[: m[0]].copy(), slots[: m[0]].copy()
 
+    def counters(self, reset: bool = False, stream=None):
+        """(ensure calls, distinct ids looked up, fetched misses) since creation or reset."""
+        return F.ftmoe_get_counters(self.handle, reset, _stream(stream))
+
     def status(self, stream=None) -> int:
         st = np.zeros(1, np.int32)
         F.ftmoe_get_device_status(self.handle, st.ctypes.data, _stream(stream))

@@ -257,6 +257,7 @@ int ftmoe_cache_create(const ftmoe_bank_spec *banks, int32_t num_banks, int32_t 
     c->t.clock = reinterpret_cast<uint32_t *>(ws + lay.hdr);
     c->t.status = reinterpret_cast<int32_t *>(ws + lay.hdr + 4);
     c->t.num_miss = reinterpret_cast<int32_t *>(ws + lay.hdr + 8);
+    c->t.stats = reinterpret_cast<unsigned long long *>(ws + lay.hdr + 16);
     c->t.id2slot = reinterpret_cast<int32_t *>(ws + lay.id2slot);
     c->t.owner = reinterpret_cast<int32_t *>(ws + lay.owner);
     c->t.stamp = reinterpret_cast<uint32_t *>(ws + lay.stamp);
@@ -406,16 +407,21 @@ static int copy_engine(ftmoe_cache_t *c, cudaStream_t read_st, cudaStream_t copy
         CK(cudaStreamSynchronize(read_st), "sync");
     }
     // misses come in ascending expert id; a run of consecutive experts landing in
-    // consecutive slots is contiguous on both sides, so it is one transfer per bank
+    // consecutive slots is contiguous on both sides, so it is one transfer per bank (split
+    // into transfers of at most kEngineChunk bytes)
+    constexpr size_t kEngineChunk = (size_t)256 << 20;
     for (int j = 0; j < m;) {
         const int64_t e = ids[j] % c->E, s = slots[j];
         int run = 1;
         while (j + run < m && ids[j + run] == ids[j] + run && slots[j + run] == slots[j] + run) run++;
         for (int b = 0; b < c->nb; b++) {
             const unsigned char *src = static_cast<const unsigned char *>(c->host[b][c->last_layer]) + e * c->bytes[b];
-            CK(cudaMemcpyAsync(c->dev_slots[b] + s * c->bytes[b], src, (size_t)run * c->bytes[b],
-                               cudaMemcpyHostToDevice, copy_st),
-               "copy engine");
+            unsigned char *dst = c->dev_slots[b] + s * c->bytes[b];
+            const size_t total = (size_t)run * c->bytes[b];
+            for (size_t off = 0; off < total; off += kEngineChunk) {
+                const size_t n = total - off < kEngineChunk ? total - off : kEngineChunk;
+                CK(cudaMemcpyAsync(dst + off, src + off, n, cudaMemcpyHostToDevice, copy_st), "copy engine");
+            }
         }
         j += run;
     }
@@ -612,6 +618,20 @@ int ftmoe_get_miss_list(ftmoe_cache_t *c, int32_t *h_ids, int32_t *h_slots, int3
     if (*h_m > 0) {
         CK(cudaMemcpyAsync(h_ids, c->t.miss_ids, (size_t)*h_m * 4, cudaMemcpyDeviceToHost, st), "read miss ids");
         CK(cudaMemcpyAsync(h_slots, c->t.miss_slots, (size_t)*h_m * 4, cudaMemcpyDeviceToHost, st), "read miss slots");
+        CK(cudaStreamSynchronize(st), "sync");
+    }
+    return FTMOE_OK;
+}
+
+int ftmoe_get_counters(ftmoe_cache_t *c, uint64_t *h_counters, int32_t reset, void *stream) {
+    if (!c || !h_counters) return fail(FTMOE_ERR_INVALID_ARG, "NULL argument");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned long long v[3];
+    CK(cudaMemcpyAsync(v, c->t.stats, sizeof v, cudaMemcpyDeviceToHost, st), "read counters");
+    CK(cudaStreamSynchronize(st), "sync");
+    for (int i = 0; i < 3; i++) h_counters[i] = (uint64_t)v[i];
+    if (reset) {
+        CK(cudaMemsetAsync(c->t.stats, 0, sizeof v, st), "reset counters");
         CK(cudaStreamSynchronize(st), "sync");
     }
     return FTMOE_OK;

@@ -239,6 +239,11 @@ __global__ void __launch_bounds__(kThreads) ensure_kernel(EnsureParams p) {
             p.counts[0] = m;
             p.counts[1] = s_mfull;
         }
+        if (p.t.stats) {  // cumulative: calls, distinct ids (hits + all misses), fetched misses
+            p.t.stats[0] += 1ull;
+            p.t.stats[1] += (unsigned long long)(s_h + s_mfull);
+            p.t.stats[2] += (unsigned long long)m;
+        }
     }
 }
 
@@ -254,6 +259,7 @@ __global__ void init_state_kernel(Tables t, int LE, int S) {
         *t.clock = 0;
         *t.status = 0;
         *t.num_miss = 0;
+        if (t.stats) t.stats[0] = t.stats[1] = t.stats[2] = 0ull;
     }
 }
 

@@ -20,6 +20,7 @@ struct Tables {
     uint32_t *stamp;      // [S]
     int32_t *miss_ids;    // [min(E, S)] flat ids, ascending
     int32_t *miss_slots;  // [min(E, S)]
+    unsigned long long *stats;  // [3] successful ensure calls, distinct ids looked up, fetched misses
 };
 
 // ---------------------------------------------------------------- K1 ensure

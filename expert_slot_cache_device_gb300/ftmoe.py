@@ -30,7 +30,7 @@ EXPORTS = [
     "ftmoe_cache_set_state", "ftmoe_get_miss_list", "ftmoe_get_device_status", "ftmoe_h2d_stream_copy",
     "ftmoe_last_error", "ftmoe_expert_ffn_noalloc", "ftmoe_ensure_experts_hybrid", "ftmoe_hybrid_fetch_fraction",
     "ftmoe_expert_ffn_hybrid", "ftmoe_cpu_expert_ffn", "ftmoe_prefetch_layer", "ftmoe_prefill_layers",
-    "ftmoe_measure_link", "ftmoe_measure_cpu_moe", "ftmoe_moe_backend_decision",
+    "ftmoe_measure_link", "ftmoe_measure_cpu_moe", "ftmoe_moe_backend_decision", "ftmoe_get_counters",
 ]
 BACKEND_OFFLOAD, BACKEND_HYBRID = 0, 1
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -89,6 +89,7 @@ def lib() -> ctypes.CDLL:
         "ftmoe_measure_link": [P, P, sz, i32, P, P, P],
         "ftmoe_measure_cpu_moe": [i32, i32, i32, i32, P, P, i32, i32, i32, P],
         "ftmoe_moe_backend_decision": [i32, ctypes.c_double, ctypes.c_double, ctypes.c_double, P, P],
+        "ftmoe_get_counters": [P, P, i32, P],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -254,3 +255,10 @@ def ftmoe_moe_backend_decision(fmt: int, link_gbps: float, cpu_gbps: float, thre
     be, fr = ctypes.c_int32(0), ctypes.c_float(0)
     _check(lib().ftmoe_moe_backend_decision(fmt, link_gbps, cpu_gbps, threshold, ctypes.byref(be), ctypes.byref(fr)))
     return be.value, fr.value
+
+
+def ftmoe_get_counters(cache: int, reset: bool, stream: int):
+    """Returns (ensure calls, distinct ids looked up, fetched misses)."""
+    out = (ctypes.c_uint64 * 3)()
+    _check(lib().ftmoe_get_counters(cache, out, 1 if reset else 0, stream))
+    return int(out[0]), int(out[1]), int(out[2])

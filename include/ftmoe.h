@@ -83,7 +83,8 @@ extern "C" {
 #define FTMOE_COPY_ENGINE 2   /* copy engines: reads the miss list back to the host
                                  (synchronises the stream), then one cudaMemcpyAsync
                                  per bank and run of consecutive experts landing in
-                                 consecutive slots (a single miss is a run of one) */
+                                 consecutive slots (a single miss is a run of one),
+                                 in transfers of at most 256 MiB */
 
 /* Limits of one cache. */
 #define FTMOE_MAX_BANKS 8
@@ -258,6 +259,14 @@ int ftmoe_prefill_layers(ftmoe_cache_t *cache, int32_t num_layers, const int32_t
                          const int32_t *const *d_topk_ids, int32_t bs, int32_t topk,
                          const void *const *d_x_bf16, const float *const *d_weights, void *const *d_y_bf16,
                          void *compute_stream, void *copy_stream);
+
+/* Cumulative ensure statistics since cache creation (or the last reset): h_counters[0] =
+ * successful ensure calls (plain and hybrid, prefetches included), [1] = distinct ids looked
+ * up (hits + misses before any hybrid cap), [2] = misses given a slot (fetched). Hits =
+ * [1] - misses before the cap; for plain calls the hit rate is 1 - [2] / [1]. Calls that
+ * fail on the device do not count. reset != 0 zeroes them after the read. Synchronises the
+ * stream. This library's observability; the pages define no such counters. */
+int ftmoe_get_counters(ftmoe_cache_t *cache, uint64_t *h_counters, int32_t reset, void *stream);
 
 /* MoE backends of the decision below. */
 #define FTMOE_BACKEND_OFFLOAD 0  /* fetch every miss over the host link */

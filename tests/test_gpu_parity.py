@@ -285,12 +285,13 @@ def test_multistep_trace():
     d_y = torch.empty((1, cfg.H), dtype=torch.bfloat16, device="cuda")
     rng = np.random.default_rng(77)
     sample = set(map(tuple, np.stack([rng.integers(0, cfg.steps, 24), rng.integers(0, cfg.L, 24)], 1).tolist()))
-    total_miss = 0
+    total_miss = total_unique = 0
     for step in range(cfg.steps):
         for layer in range(cfg.L):
             ids, w, x = wl.trace_call(cfg, step, layer)
             rc, slots, mids, msl = orc.ensure(layer, ids)
             assert rc == oracle.OK
+            total_unique += np.unique(ids).size
             d_ids = to_dev(ids)
             cache.ensure(layer, d_ids, d_slots)
             cache.copy_missing()
@@ -312,4 +313,6 @@ def test_multistep_trace():
             assert clock == int(orc.clock[0])
     assert cache.status() == F.OK
     assert total_miss > 0
+    # the cumulative counters agree with the oracle's trace
+    assert cache.counters() == (cfg.steps * cfg.L, total_unique, total_miss)
     cache.close()
