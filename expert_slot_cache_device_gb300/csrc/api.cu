@@ -46,6 +46,7 @@ int schema_banks(int fmt) {
         case FTMOE_FMT_NVFP4: return 6;
         case FTMOE_FMT_MXFP4: return 6;
         case FTMOE_FMT_FP8: return 4;
+        case FTMOE_FMT_Q4_0: return 2;
         default: return -1;
     }
 }
@@ -72,6 +73,7 @@ int64_t schema_bytes(int fmt, int b, int64_t H, int64_t I) {
         const int64_t Nf = b < 2 ? 2 * I : H, Kf = b < 2 ? H : I;
         return b % 2 == 0 ? Nf * Kf : ((Nf + 127) / 128) * ((Kf + 127) / 128) * 4;
     }
+    if (fmt == FTMOE_FMT_Q4_0) return b == 0 ? 2 * I * (H / 32) * 18 : H * (I / 32) * 18;
     return -1;
 }
 
@@ -82,6 +84,7 @@ int schema_dtype(int fmt, int b) {
         return d[b % 3];
     }
     if (fmt == FTMOE_FMT_FP8) return b % 2 == 0 ? FTMOE_DT_E4M3 : FTMOE_DT_F32;
+    if (fmt == FTMOE_FMT_Q4_0) return FTMOE_DT_Q4_0;
     const int d[3] = {FTMOE_DT_U8, FTMOE_DT_E8M0, FTMOE_DT_BF16};
     return d[b % 3];
 }
@@ -129,7 +132,7 @@ int check_geometry(int fmt, int nb, int E, int L, int S, int H, int I, int max_p
     if (nb != schema_banks(fmt))
         return fail(FTMOE_ERR_FORMAT, "format %d needs %d banks, got %d", fmt, schema_banks(fmt), nb);
     if (H <= 0 || I <= 0) return fail(FTMOE_ERR_INVALID_ARG, "H=%d, I=%d must be positive", H, I);
-    const int q = fmt == FTMOE_FMT_BF16 ? 8 : (fmt == FTMOE_FMT_FP8 ? 512 : 32);
+    const int q = fmt == FTMOE_FMT_BF16 ? 8 : (fmt == FTMOE_FMT_FP8 ? 512 : (fmt == FTMOE_FMT_Q4_0 ? 256 : 32));
     if (H % q || I % q)
         return fail(FTMOE_ERR_FORMAT, "format %d needs H and I multiples of %d (H=%d, I=%d)", fmt, q, H, I);
     return FTMOE_OK;

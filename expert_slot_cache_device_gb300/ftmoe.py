@@ -17,10 +17,12 @@ LIB_PATH = os.path.join(_HERE, "libftmoe.so")
 OK = 0
 ERR_INVALID_ARG, ERR_CAPACITY, ERR_ID_RANGE, ERR_CUDA, ERR_FORMAT, ERR_STATE = -1, -2, -3, -4, -5, -6
 ERR_NAMES = {0: "OK", -1: "INVALID_ARG", -2: "CAPACITY", -3: "ID_RANGE", -4: "CUDA", -5: "FORMAT", -6: "STATE"}
-FMT_RAW, FMT_BF16, FMT_NVFP4, FMT_MXFP4, FMT_FP8 = 0, 1, 2, 3, 4
-FORMATS = {"raw": FMT_RAW, "bf16": FMT_BF16, "nvfp4": FMT_NVFP4, "mxfp4": FMT_MXFP4, "fp8": FMT_FP8}
-DT_U8, DT_BF16, DT_F16, DT_E4M3, DT_E8M0, DT_F32 = 0, 1, 2, 3, 4, 5
-DTYPES = {"u8": DT_U8, "bf16": DT_BF16, "f16": DT_F16, "e4m3": DT_E4M3, "e8m0": DT_E8M0, "f32": DT_F32}
+FMT_RAW, FMT_BF16, FMT_NVFP4, FMT_MXFP4, FMT_FP8, FMT_Q4_0 = 0, 1, 2, 3, 4, 5
+FORMATS = {"raw": FMT_RAW, "bf16": FMT_BF16, "nvfp4": FMT_NVFP4, "mxfp4": FMT_MXFP4, "fp8": FMT_FP8,
+           "q4_0": FMT_Q4_0}
+DT_U8, DT_BF16, DT_F16, DT_E4M3, DT_E8M0, DT_F32, DT_Q4_0 = 0, 1, 2, 3, 4, 5, 6
+DTYPES = {"u8": DT_U8, "bf16": DT_BF16, "f16": DT_F16, "e4m3": DT_E4M3, "e8m0": DT_E8M0, "f32": DT_F32,
+          "q4_0": DT_Q4_0}
 COPY_FUSED, COPY_PER_BANK, COPY_ENGINE = 0, 1, 2
 MAX_BANKS = 8
 

@@ -60,6 +60,9 @@ CONFIGS: Dict[str, Config] = {
                  (1, 16, 64), (0.05, 0.5), "zipf", 1.1, 0),
     "c5": Config("c5", "bf16_trace_E256_k8_H4096_I1536_L61_S1024", 4, "bf16", 256, 8, 4096, 1536, 61,
                  1024, (1,), (), "zipf", 1.2, 7, steps=512),
+    # GGUF Q4_0 layer: the nvfp4 layer's shape with the Q4_0 bank schema
+    "c7": Config("c7", "q4_0_E256_k8_H7168_I2048_L58_S512", 6, "q4_0", 256, 8, 7168, 2048, 58, 512,
+                 (1, 8, 32), (0.1, 0.3, 1.0), "uniform", 0.0, 0),
     # block-FP8 layer: the nvfp4 layer's shape with the block-FP8 bank schema
     "c6": Config("c6", "fp8_E256_k8_H7168_I2048_L58_S512", 5, "fp8", 256, 8, 7168, 2048, 58, 512,
                  (1, 8, 32), (0.1, 0.3, 1.0), "uniform", 0.0, 0),
@@ -123,6 +126,12 @@ def bank_schema(cfg: Config) -> List[BankGeom]:
             BankGeom("down_weight", "e4m3", H, I),
             BankGeom("down_scale", "f32", (H + 127) // 128, 4 * ((I + 127) // 128)),
         ]
+    if cfg.fmt == "q4_0":
+        # GGUF Q4_0: rows of K/32 blocks, 18 bytes each (binary16 scale + 16 nibble bytes)
+        return [
+            BankGeom("gate_up_q4_0", "q4_0", 2 * I, (H // 32) * 18),
+            BankGeom("down_q4_0", "q4_0", H, (I // 32) * 18),
+        ]
     raise ValueError(f"unknown format {cfg.fmt!r}")
 
 
@@ -157,6 +166,7 @@ def f32_to_e4m3_bits(a: np.ndarray) -> np.ndarray:
 
 _SEED_BANK = 0xBA4C
 FP8_Q_STD = 112.0  # standard deviation of the synthetic block-FP8 codes (before e4m3 rounding)
+Q4_D = 0.02 / np.sqrt(21.5)  # Q4_0 block scale: (q - 8) over uniform nibbles has mean square 21.5
 
 
 def _gen_bank_expert(cfg: Config, b: int, geom: BankGeom, e: int) -> np.ndarray:
@@ -191,6 +201,13 @@ def _gen_bank_expert(cfg: Config, b: int, geom: BankGeom, e: int) -> np.ndarray:
         return g.astype(np.float16).view(np.uint8)
     if geom.dtype == "e8m0":
         return rng.integers(117, 121, size=geom.bytes, dtype=np.uint8)
+    if geom.dtype == "q4_0":
+        # uniform nibbles (q - 8 has mean square 21.5); d = (0.5 + U) * Q4_D, so w has a
+        # standard deviation near 0.02
+        blocks = rng.integers(0, 256, size=(geom.bytes // 18, 18), dtype=np.uint8)
+        d = ((0.5 + rng.random(blocks.shape[0])) * Q4_D).astype(np.float16)
+        blocks[:, 0:2] = d.view(np.uint8).reshape(-1, 2)
+        return blocks.reshape(-1)
     raise ValueError(geom.dtype)
 
 
@@ -252,6 +269,12 @@ def fill_bank_device(cfg: Config, b: int, out, experts: Optional[Sequence[int]] 
             t = ((0.5 + u) / np.sqrt(8.5625 * K)).to(torch.float16).view(torch.uint8)
         elif geom.dtype == "e8m0":
             t = torch.randint(117, 121, (n,), dtype=torch.uint8, device=device, generator=gen)
+        elif geom.dtype == "q4_0":
+            blocks = torch.randint(0, 256, (n // 18, 18), dtype=torch.uint8, device=device, generator=gen)
+            u = torch.rand(n // 18, device=device, generator=gen, dtype=torch.float64)
+            d = ((0.5 + u) * Q4_D).to(torch.float16).view(torch.uint8).view(-1, 2)
+            blocks[:, 0:2] = d
+            t = blocks.reshape(-1)
         else:
             raise ValueError(geom.dtype)
         out[i].copy_(t, non_blocking=True)

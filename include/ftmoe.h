@@ -67,6 +67,11 @@ extern "C" {
                              bank schemas): gate_up weight [2I, H] e4m3, scale [2I/128, H/128]
                              f32 (one per 128 x 128 block), down weight [H, I] e4m3, scale
                              [H/128, I/128] f32; H and I multiples of 512. No CPU MoE path. */
+#define FTMOE_FMT_Q4_0 5  /* GGUF Q4_0 (architecture deep-dive, sections 五 and 六): gate_up
+                             [2I rows][H/32 blocks] and down [H rows][I/32 blocks] of 18-byte
+                             blocks (binary16 d, 16 bytes qs; element j < 16 = low nibble of
+                             qs[j], j + 16 = high nibble; w = (nibble - 8) * d); H and I
+                             multiples of 256. */
 
 /* element types of a bank (informative; FFN formats check them against the schema) */
 #define FTMOE_DT_U8 0
@@ -75,6 +80,7 @@ extern "C" {
 #define FTMOE_DT_E4M3 3
 #define FTMOE_DT_E8M0 4
 #define FTMOE_DT_F32 5
+#define FTMOE_DT_Q4_0 6
 
 /* copy_missing implementations (benchmark guide, section 4.4: the fused multi-bank
  * copy is the main path; the per-bank path is kept for A/B comparison) */

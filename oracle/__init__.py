@@ -19,7 +19,7 @@ _SO = os.path.join(_HERE, "liboracle.so")
 _SRCS = ["lru.c", "copy.c", "ffn.c"]
 
 OK, ERR_INVALID_ARG, ERR_CAPACITY, ERR_ID_RANGE, ERR_STATE = 0, -1, -2, -3, -6
-FMT = {"bf16": 0, "nvfp4": 1, "mxfp4": 2, "fp8": 3}
+FMT = {"bf16": 0, "nvfp4": 1, "mxfp4": 2, "fp8": 3, "q4_0": 4}
 NUM = {"e2m1": 0, "e4m3": 1, "e8m0": 2, "f16": 3, "bf16": 4}
 
 

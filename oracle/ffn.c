@@ -17,6 +17,10 @@
  *   fp8    block FP8 ([ARCH] section 五 lists "FP8 block" among the bank schemas):
  *          weight [N, K] e4m3fn output-row-major, scale [N/128, K/128] binary32
  *          row-major, one per 128 x 128 block; w = e4m3 * scale[n / 128][k / 128].
+ *   q4_0   GGUF Q4_0 ([ARCH] sections 五 and 六 name a GGUF Q4_0 bank schema and MoE):
+ *          each output row is K/32 blocks of 18 bytes, a binary16 scale d then 16
+ *          bytes qs; element j < 16 of a block is the low nibble of qs[j], element
+ *          j + 16 the high nibble; w = (nibble - 8) * d (the ggml Q4_0 block).
  *   FFN    gu = W_gu x (+ b_gu), h = silu(gu[0:I]) * gu[I:2I],
  *          o = W_d h (+ b_d), y_t = sum_j w_{t,j} o_{t,j}; all in fp64.
  * Number formats follow their published definitions: OCP 8-bit floating point
@@ -107,6 +111,7 @@ int32_t orc_num_banks(int32_t fmt) {
         case ORC_FMT_NVFP4: return 6;
         case ORC_FMT_MXFP4: return 6;
         case ORC_FMT_FP8: return 4;
+        case ORC_FMT_Q4_0: return 2;
         default: return -1;
     }
 }
@@ -142,6 +147,12 @@ double orc_weight(int32_t fmt, int32_t which, const uint8_t *const *banks, int32
         const uint8_t *sc = banks[2 * which + 1];
         int64_t kb = (K + 127) / 128; /* scale blocks along k */
         return dec_e4m3(wq[n * K + k]) * rdf32(sc, (n / 128) * kb + k / 128);
+    }
+    if (fmt == ORC_FMT_Q4_0) {
+        const uint8_t *blk = banks[which] + (n * (K / 32) + k / 32) * 18;
+        int64_t j = k % 32;
+        uint32_t q = j < 16 ? (blk[2 + j] & 15u) : (blk[2 + j - 16] >> 4);
+        return ((double)q - 8.0) * dec_f16(rd16(blk, 0));
     }
     return NAN;
 }

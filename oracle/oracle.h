@@ -44,6 +44,7 @@ extern "C" {
 #define ORC_FMT_NVFP4 1
 #define ORC_FMT_MXFP4 2
 #define ORC_FMT_FP8 3
+#define ORC_FMT_Q4_0 4
 
 /* number kinds for orc_decode */
 #define ORC_NUM_E2M1 0

@@ -11,7 +11,8 @@ The FFN is checked against closed forms, not against a second copy of itself:
   * linearity of the combine in the router weights.
 The readings of the layouts are those of the oracle's header (gate rows first, low
 nibble = even k, nvfp4 scale per 16 along k, mxfp4 blocks transposed [K/2, N], block
-FP8 one binary32 scale per 128 x 128 block).
+FP8 one binary32 scale per 128 x 128 block, Q4_0 18-byte blocks of 32 with element j and
+j + 16 in the low and high nibble of byte j).
 """
 import math
 
@@ -43,6 +44,10 @@ class ExpertBuilder:
         self.fmt, self.H, self.I = fmt, H, I
         cfg = wl.Config("t", "t", 0, fmt, 1, 1, H, I, 1, 1, (1,), (1.0,), "uniform", 0.0, 0)
         self.banks = [np.zeros(g.bytes, np.uint8) for g in wl.bank_schema(cfg)]
+        if fmt == "q4_0":  # zero weights: nibble 8 (q - 8 = 0) everywhere, scale 0 until used
+            for bk in self.banks:
+                blk = bk.reshape(-1, 18)
+                blk[:, 2:] = 0x88
 
     def NK(self, which):
         return (2 * self.I, self.H) if which == 0 else (self.H, self.I)
@@ -55,6 +60,20 @@ class ExpertBuilder:
             bits = int(wl.f32_to_bf16_bits(np.array([v]))[0])
             self.banks[which].view(np.uint16)[n * K + k] = bits
             return bf16_val(bits)
+        if self.fmt == "q4_0":
+            # nibble at (n, k) of the row's 18-byte block; the block's binary16 scale is chosen
+            # on its first use and shared by the block's 32 weights
+            blk = self.banks[which].reshape(-1, 18)[n * (K // 32) + k // 32]
+            j = k % 32
+            q = int(rng.choice([0, 1, 3, 5, 7, 9, 10, 12, 15]))  # never 8 (that is zero)
+            if j < 16:
+                blk[2 + j] = (blk[2 + j] & 0xF0) | q
+            else:
+                blk[2 + j - 16] = (blk[2 + j - 16] & 0x0F) | (q << 4)
+            d = blk[0:2].view(np.float16)
+            if d[0] == 0:
+                d[0] = np.float16(rng.choice([0.25, 0.0625, 1.5, 0.001953125, 3.0]))
+            return (q - 8) * float(d[0])
         if self.fmt == "fp8":
             # e4m3 code at (n, k) of the row-major weight; the 128 x 128 block's binary32
             # scale is chosen on its first use and shared by every weight in the block
@@ -92,7 +111,7 @@ class ExpertBuilder:
 
 
 FMT_GEOMS = [("bf16", 64, 32), ("bf16", 48, 80), ("nvfp4", 64, 32), ("nvfp4", 96, 64), ("mxfp4", 64, 32),
-             ("mxfp4", 96, 64), ("fp8", 256, 128), ("fp8", 128, 256)]
+             ("mxfp4", 96, 64), ("fp8", 256, 128), ("fp8", 128, 256), ("q4_0", 64, 32), ("q4_0", 96, 160)]
 
 
 @pytest.mark.parametrize("fmt,H,I", FMT_GEOMS)
