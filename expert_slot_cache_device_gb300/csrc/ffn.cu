@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(1024) ffn_route_kernel(FfnParams p) {
         const float sc = ldexpf(1.f, -e);
         uint16_t *dst = p.s.x16 + (int64_t)t * p.H;
         for (int k = tid; k < p.H; k += nt)
-            dst[p.x16_swz ? swz_x16(k) : k] =
+            dst[p.x16_swz == 1 ? swz_x16(k) : (p.x16_swz == 2 ? swz_q4x16(k) : k)] =
                 __half_as_ushort(__float2half_rn(__uint_as_float((uint32_t)xr[k] << 16) * sc));
         if (tid == 0) p.s.xexp[t] = e;
         return;
@@ -747,9 +747,11 @@ cudaError_t launch_ffn(const FfnParams &p_in, int num_sms, cudaStream_t st, cons
     const bool mx_tma = num_sms > 0 && ffn_mx_tma_supported(p, mx);
     const bool fp8_tma = num_sms > 0 && ffn_fp8_tma_supported(p, mx);
     if (p.fmt == FTMOE_FMT_FP8 && !fp8_tma) return cudaErrorNotSupported;  // block FP8 has one pipeline only
-    const bool want_x16 = (fp4_rows_tma && p.fmt == FTMOE_FMT_NVFP4) || mx_tma || fp8_tma;
-    p.x16_emax = p.fmt == FTMOE_FMT_MXFP4 ? 9 : 10;
-    p.x16_swz = fp4_rows_tma && p.fmt == FTMOE_FMT_NVFP4;
+    if (p.fmt == FTMOE_FMT_Q4_0 && !fp4_rows_tma) return cudaErrorNotSupported;  // so has Q4_0
+    const bool want_x16 =
+        (fp4_rows_tma && (p.fmt == FTMOE_FMT_NVFP4 || p.fmt == FTMOE_FMT_Q4_0)) || mx_tma || fp8_tma;
+    p.x16_emax = p.fmt == FTMOE_FMT_MXFP4 ? 9 : (p.fmt == FTMOE_FMT_Q4_0 ? 8 : 10);
+    p.x16_swz = fp4_rows_tma && p.fmt == FTMOE_FMT_NVFP4 ? 1 : (fp4_rows_tma && p.fmt == FTMOE_FMT_Q4_0 ? 2 : 0);
     p.pass_tokens = (mx_tma || fp8_tma) ? kMxPassTokens : kPassTokens;
     ffn_route_kernel<<<1 + (want_x16 ? p.bs : 0), 1024, route_smem, st>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -234,6 +234,64 @@ __device__ __forceinline__ uint32_t f2_scale_to_h2(float x, float y, float s) {
     return h;
 }
 
+// GGUF Q4_0 block b of a row staged in shared memory (18 bytes: binary16 scale d, then
+// 16 bytes qs): blocks are only 2-byte aligned, so the block is read as five aligned
+// 32-bit words and the qs words are funnel-shifted out of them. The row must start on a
+// 4-byte boundary; the read may run up to 2 bytes past the block.
+__device__ __forceinline__ void q4_block(const unsigned char *row, int b, uint32_t &d, uint32_t (&qs)[4]) {
+    const int o = 18 * b, a = o & ~3, r = o - a;  // r is 0 or 2
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(row + a);
+    const uint32_t w0 = w[0], w1 = w[1], w2 = w[2], w3 = w[3], w4 = w[4];
+    d = (r ? (w0 >> 16) : w0) & 0xffffu;
+    const uint32_t sh = 16u + 8u * (uint32_t)r;  // 32 (clamped funnel shift) selects the high word
+    qs[0] = __funnelshift_rc(w0, w1, sh);
+    qs[1] = __funnelshift_rc(w1, w2, sh);
+    qs[2] = __funnelshift_rc(w2, w3, sh);
+    qs[3] = __funnelshift_rc(w3, w4, sh);
+}
+
+// Four qs bytes -> (nibble - 8) as exact f16x2 pairs: lo = elements (0,1), (2,3) of the
+// word's low nibbles, hi = the same elements of its high nibbles (element + 16). A nibble
+// q placed under the f16 exponent of 1024 reads as 1024 + q; subtracting 1032 is exact.
+__device__ __forceinline__ uint32_t sub_f16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+__device__ __forceinline__ void q4_word_h2(uint32_t w, uint32_t (&lo)[2], uint32_t (&hi)[2]) {
+    const uint32_t ml = w & 0x0F0F0F0Fu, mh = (w >> 4) & 0x0F0F0F0Fu;
+    const uint32_t e = 0x64646464u, off = 0x64086408u;  // f16x2 (1032, 1032)
+    lo[0] = sub_f16x2(__byte_perm(ml, e, 0x5140), off);
+    lo[1] = sub_f16x2(__byte_perm(ml, e, 0x7362), off);
+    hi[0] = sub_f16x2(__byte_perm(mh, e, 0x5140), off);
+    hi[1] = sub_f16x2(__byte_perm(mh, e, 0x7362), off);
+}
+
+// A Q4_0 block (32 weights as sixteen f16x2 pairs, pair p = elements 2p, 2p + 1) against
+// 32 f16 activations, left as two f16 partial sums of sixteen exact products each
+// (|nibble - 8| <= 8 and |x| < 2^8 keep every partial below 2^15).
+__device__ __forceinline__ uint32_t dot32_h2(const uint32_t (&w)[16], const uint32_t (&x)[16]) {
+    __half2 acc = __hmul2(*reinterpret_cast<const __half2 *>(&w[0]), *reinterpret_cast<const __half2 *>(&x[0]));
+#pragma unroll
+    for (int i = 1; i < 16; i++)
+        acc = __hfma2(*reinterpret_cast<const __half2 *>(&w[i]), *reinterpret_cast<const __half2 *>(&x[i]), acc);
+    return *reinterpret_cast<const uint32_t *>(&acc);
+}
+
+// Decode a Q4_0 block's four qs words into the sixteen pairs of dot32_h2.
+__device__ __forceinline__ void q4_decode(const uint32_t (&qs)[4], uint32_t (&w)[16]) {
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        uint32_t lo[2], hi[2];
+        q4_word_h2(qs[i], lo, hi);
+        w[2 * i] = lo[0];
+        w[2 * i + 1] = lo[1];
+        w[8 + 2 * i] = hi[0];
+        w[9 + 2 * i] = hi[1];
+    }
+}
+
 // Element layouts of the nvfp4 activation vectors staged in shared memory. A lane
 // handles one 16-element block b per step; storing some of its 16-byte groups in a
 // lane-dependent order makes the quarter-warp phases of 128-bit shared loads hit 32
@@ -243,6 +301,11 @@ __device__ __forceinline__ uint32_t f2_scale_to_h2(float x, float y, float s) {
 //   fp32 h rows (64-byte blocks, four 16-byte quarters): quarter q of block b is stored
 //   at quarter q ^ ((b >> 1) & 3).
 __host__ __device__ __forceinline__ int swz_x16(int k) { return k ^ ((k >> 3) & 8); }
+// Q4_0 (32-element blocks): f16 activations, 16-byte unit u of block b stored at
+// u ^ ((b >> 1) & 3); fp32 h rows, unit u of block b stored at u ^ (b & 7).
+__host__ __device__ __forceinline__ int swz_q4x16(int k) { return k ^ ((k >> 3) & 0x18); }
+__host__ __device__ __forceinline__ int swz_q4h32(int n) { return n ^ ((n >> 3) & 0x1C); }
+
 __host__ __device__ __forceinline__ int swz_h32(int n) { return n ^ ((n >> 3) & 12); }
 
 // Distinct slot u owning pass `pi`: the largest u with upoff[u] <= pi (upoff ascending).

@@ -122,16 +122,20 @@ __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wa
 __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 
 // Bytes of the weight segments of an item with `rows` rows (R rows reserve the layout).
+// Formats whose consumers use the power-of-two scaled f16 activation copy and f16 h.
+template <int FMT>
+constexpr bool kF16Act = FMT == FTMOE_FMT_NVFP4 || FMT == FTMOE_FMT_Q4_0;
+
 template <int FMT, int PHASE>
 struct Seg {
     // per-row bytes of the code/weight matrix and of the scale matrix
     __device__ __host__ static int64_t wrow(int H, int I) {
         const int64_t K = PHASE == kGateUp ? H : I;
-        return FMT == FTMOE_FMT_BF16 ? 2 * K : K / 2;
+        return FMT == FTMOE_FMT_BF16 ? 2 * K : (FMT == FTMOE_FMT_Q4_0 ? K / 32 * 18 : K / 2);
     }
     __device__ __host__ static int64_t srow(int H, int I) {
         const int64_t K = PHASE == kGateUp ? H : I;
-        return FMT == FTMOE_FMT_BF16 ? 0 : K / 16;
+        return FMT == FTMOE_FMT_NVFP4 ? K / 16 : 0;
     }
     static constexpr int mats = PHASE == kGateUp ? 2 : 1;  // gate + up, or down
     // offset of the nvfp4 per-row f16 globals (after the codes and scales of R rows)
@@ -204,6 +208,35 @@ __device__ __forceinline__ void gu_consume(const FfnParams &p, const TmaCfg &c, 
                     }
                 }
             }
+        } else if (FMT == FTMOE_FMT_Q4_0) {
+            // lane step = one 32-element Q4_0 block of the gate and of the up row: nibbles ->
+            // exact f16x2 (nibble - 8), 32 exact f16 products summed in two f16 halves of
+            // sixteen, the block's binary16 scale applied in fp32. Activations are staged in
+            // the swz_q4x16 layout: unit u of this lane's block sits at u ^ ((b >> 1) & 3).
+            const unsigned char *rg = st + j * wr, *ru = st + (R + j) * wr;
+            const int nb = H >> 5;
+            const int rot = (lane >> 1) & 3;
+            for (int b = lane; b < nb; b += 32) {
+                uint32_t dg, du, qg[4], qu[4], fa[16], fb[16];
+                q4_block(rg, b, dg, qg);
+                q4_block(ru, b, du, qu);
+                q4_decode(qg, fa);
+                q4_decode(qu, fb);
+#pragma unroll
+                for (int t = 0; t < NT; t++) {
+                    uint32_t xw[16];
+#pragma unroll
+                    for (int uu = 0; uu < 4; uu++) {
+                        const uint4 xv = xs[t * nxv + 4 * b + (uu ^ rot)];
+                        xw[4 * uu] = xv.x;
+                        xw[4 * uu + 1] = xv.y;
+                        xw[4 * uu + 2] = xv.z;
+                        xw[4 * uu + 3] = xv.w;
+                    }
+                    g[t] = fma_h2_scale(dot32_h2(fa, xw), (uint16_t)dg, g[t]);
+                    u[t] = fma_h2_scale(dot32_h2(fb, xw), (uint16_t)du, u[t]);
+                }
+            }
         } else {
             // lane step = one 16-element scale block (two 32-bit code words): codes ->
             // exact f16x2, sixteen exact f16 products summed in two f16 halves of eight,
@@ -235,12 +268,13 @@ __device__ __forceinline__ void gu_consume(const FfnParams &p, const TmaCfg &c, 
         }
 #pragma unroll
         for (int t = 0; t < NT; t++) {
-            const float xs_t = FMT == FTMOE_FMT_NVFP4 ? ldexpf(1.f, h.texp[t]) : 1.f;
+            const float xs_t = kF16Act<FMT> ? ldexpf(1.f, h.texp[t]) : 1.f;
             const float gs = warp_sum(g[t]) * gg * xs_t, us = warp_sum(u[t]) * gu * xs_t;
             if (lane == t) {
                 const float hv = silu(gs) * us;
-                p.s.h[(int64_t)h.pairs[t] * I + (FMT == FTMOE_FMT_NVFP4 ? swz_h32(n) : n)] = hv;
-                if (FMT == FTMOE_FMT_NVFP4) hm.add(p, h.pairs[t], fabsf(hv));
+                const int hn = FMT == FTMOE_FMT_NVFP4 ? swz_h32(n) : (FMT == FTMOE_FMT_Q4_0 ? swz_q4h32(n) : n);
+                p.s.h[(int64_t)h.pairs[t] * I + hn] = hv;
+                if (kF16Act<FMT>) hm.add(p, h.pairs[t], fabsf(hv));
             }
         }
     }
@@ -292,6 +326,38 @@ __device__ __forceinline__ void dn_consume(const FfnParams &p, const TmaCfg &c, 
                     }
                 }
             }
+        } else if (FMT == FTMOE_FMT_Q4_0) {
+            // lane step = one 32-element Q4_0 block of RR rows; h is converted once per
+            // block and token to f16 with the token's power-of-two scale (max |h| < 2^8),
+            // shared by the RR rows. The h rows are staged in the swz_q4h32 layout: unit u of
+            // this lane's block sits at u ^ (b & 7), so the 8 lanes of a phase hit 8 units.
+            const int nb = I >> 5;
+            const int rot = lane & 7;
+            float hsc[NT];
+#pragma unroll
+            for (int t = 0; t < NT; t++) hsc[t] = ldexpf(1.f, -h.texp[t]);
+            for (int b = lane; b < nb; b += 32) {
+                uint32_t fw[RR][16], dr[RR];
+#pragma unroll
+                for (int r = 0; r < RR; r++) {
+                    const int jr = r < nr ? j0 + r : j0;
+                    uint32_t qs[4];
+                    q4_block(st + jr * wr, b, dr[r], qs);
+                    q4_decode(qs, fw[r]);
+                }
+#pragma unroll
+                for (int t = 0; t < NT; t++) {
+                    uint32_t hh[16];
+#pragma unroll
+                    for (int uu = 0; uu < 8; uu++) {
+                        const float4 hv = hs[t * nh4 + 8 * b + (uu ^ rot)];
+                        hh[2 * uu] = f2_scale_to_h2(hv.x, hv.y, hsc[t]);
+                        hh[2 * uu + 1] = f2_scale_to_h2(hv.z, hv.w, hsc[t]);
+                    }
+#pragma unroll
+                    for (int r = 0; r < RR; r++) o[r][t] = fma_h2_scale(dot32_h2(fw[r], hh), (uint16_t)dr[r], o[r][t]);
+                }
+            }
         } else {
             // lane step = one 16-element scale block (two code words); h is converted once
             // per block and token to f16 with the token's power-of-two scale (max |h| <
@@ -340,7 +406,7 @@ __device__ __forceinline__ void dn_consume(const FfnParams &p, const TmaCfg &c, 
             const int n = h.n0 + j0 + r;
 #pragma unroll
             for (int t = 0; t < NT; t++) {
-                const float v = warp_sum(o[r][t]) * gl[r] * (FMT == FTMOE_FMT_NVFP4 ? ldexpf(1.f, h.texp[t]) : 1.f);
+                const float v = warp_sum(o[r][t]) * gl[r] * (kF16Act<FMT> ? ldexpf(1.f, h.texp[t]) : 1.f);
                 if (lane == t) p.s.o[(int64_t)h.pairs[t] * H + n] = v;
             }
         }
@@ -405,7 +471,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) ffn_rows_tma_kernel(FfnParams 
                 hh.slot = slot; hh.n0 = n0; hh.rows = rows; hh.ntok = ntok; hh.done = 0;
                 for (int i = 0; i < ntok; i++) {
                     hh.pairs[i] = p.s.upairs[off + g0 + i];
-                    hh.texp[i] = (PHASE == kGateUp && FMT == FTMOE_FMT_NVFP4) ? p.s.xexp[hh.pairs[i] / p.topk] : 0;
+                    hh.texp[i] = (PHASE == kGateUp && kF16Act<FMT>) ? p.s.xexp[hh.pairs[i] / p.topk] : 0;
                 }
                 const uint32_t wbytes = (uint32_t)Seg<FMT, PHASE>::bytes(rows, H, I);
                 mbar_expect_tx(&full[s], wbytes + (uint32_t)(ntok * c.tok_bytes));
@@ -426,7 +492,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) ffn_rows_tma_kernel(FfnParams 
                         bulk_g2s(gd + 2 * R, gb + 2 * ((int64_t)I + n0), (uint32_t)(2 * rows), &full[s], pol);
                     }
                 } else {
-                    const int wb_i = FMT == FTMOE_FMT_BF16 ? 1 : 3;
+                    const int wb_i = FMT == FTMOE_FMT_NVFP4 ? 3 : 1;
                     const unsigned char *wb = p.bank[wb_i] + (int64_t)slot * p.bank_bytes[wb_i];
                     bulk_g2s(st, wb + n0 * wr, (uint32_t)(rows * wr), &full[s], pol);
                     if (FMT == FTMOE_FMT_NVFP4) {
@@ -441,21 +507,22 @@ __global__ void __launch_bounds__(kTmaThreads, 1) ffn_rows_tma_kernel(FfnParams 
                     griddep_wait();
                     waited = true;
                 }
-                if (PHASE == kDown && FMT == FTMOE_FMT_NVFP4) {
-                    // power-of-two exponent for the f16 copy of each h row (max |h| < 2^10)
+                if (PHASE == kDown && kF16Act<FMT>) {
+                    // power-of-two exponent for the f16 copy of each h row (max |h| < 2^10 for
+                    // nvfp4's sums of 8 products, 2^8 for Q4_0's sums of 16)
                     for (int i = 0; i < ntok; i++) {
                         const float m = __uint_as_float(p.s.hmax[hh.pairs[i]]);
                         int e = 0;
                         if (m > 0.f && m < INFINITY) {
                             frexpf(m, &e);
-                            e -= 10;
+                            e -= FMT == FTMOE_FMT_Q4_0 ? 8 : 10;
                         }
                         hh.texp[i] = e;
                     }
                 }
                 for (int i = 0; i < ntok; i++) {
                     const int q = hh.pairs[i];
-                    const uint16_t *xsrc = FMT == FTMOE_FMT_NVFP4 ? p.s.x16 : p.x;
+                    const uint16_t *xsrc = kF16Act<FMT> ? p.s.x16 : p.x;
                     const void *src = PHASE == kGateUp
                                           ? static_cast<const void *>(xsrc + (int64_t)(q / p.topk) * H)
                                           : static_cast<const void *>(p.s.h + (int64_t)q * I);
@@ -577,11 +644,13 @@ cudaError_t launch_one(const FfnParams &p, int num_sms, cudaStream_t st) {
 bool ffn_rows_tma_supported(const FfnParams &p) {
     if (!p.s.upoff || !p.s.n_passes) return false;
     if (p.fmt == FTMOE_FMT_BF16) return p.H % 8 == 0 && p.I % 8 == 0;
-    if (p.fmt == FTMOE_FMT_NVFP4) {
-        TmaCfg c;
+    TmaCfg c;
+    if (p.fmt == FTMOE_FMT_NVFP4)
         return p.H % 256 == 0 && p.I % 256 == 0 && p.s.x16 && p.s.xexp && p.s.hmax &&
                make_cfg<FTMOE_FMT_NVFP4, kGateUp>(p, c) && make_cfg<FTMOE_FMT_NVFP4, kDown>(p, c);
-    }
+    if (p.fmt == FTMOE_FMT_Q4_0)  // rows of 18-byte blocks: 16-byte multiples when K % 256 == 0
+        return p.H % 256 == 0 && p.I % 256 == 0 && p.s.x16 && p.s.xexp && p.s.hmax &&
+               make_cfg<FTMOE_FMT_Q4_0, kGateUp>(p, c) && make_cfg<FTMOE_FMT_Q4_0, kDown>(p, c);
     return false;
 }
 
@@ -590,6 +659,10 @@ cudaError_t launch_ffn_rows_tma(const FfnParams &p, int num_sms, cudaStream_t st
     if (p.fmt == FTMOE_FMT_BF16) {
         if ((e = launch_one<FTMOE_FMT_BF16, kGateUp>(p, num_sms, st)) != cudaSuccess) return e;
         return launch_one<FTMOE_FMT_BF16, kDown>(p, num_sms, st);
+    }
+    if (p.fmt == FTMOE_FMT_Q4_0) {
+        if ((e = launch_one<FTMOE_FMT_Q4_0, kGateUp>(p, num_sms, st)) != cudaSuccess) return e;
+        return launch_one<FTMOE_FMT_Q4_0, kDown>(p, num_sms, st);
     }
     if ((e = launch_one<FTMOE_FMT_NVFP4, kGateUp>(p, num_sms, st)) != cudaSuccess) return e;
     return launch_one<FTMOE_FMT_NVFP4, kDown>(p, num_sms, st);

@@ -100,7 +100,7 @@ struct FfnParams {
     int32_t *status;
     int32_t fmt, H, I, S, bs, topk, P;
     int32_t x16_emax;  // f16 activation copy keeps max |x| < 2^x16_emax
-    int32_t x16_swz;   // f16 activation copy stored in the swz_x16 layout (nvfp4 rows kernels)
+    int32_t x16_swz;   // f16 activation copy layout: 0 plain, 1 swz_x16 (nvfp4), 2 swz_q4x16 (Q4_0)
     int32_t pass_tokens;  // tokens per pass of the pipelined kernels (kPassTokens / kMxPassTokens)
 };
 

@@ -202,12 +202,12 @@ def _run_point(cache, cfg, bs, mr, modes=(F.COPY_FUSED, F.COPY_PER_BANK, F.COPY_
     return assert_ffn_close(y[toks], ref, f"{cfg.key} bs={bs} mr={mr}")
 
 
-@pytest.mark.parametrize("key", ["c1", "c2", "c3", "c4", "c6"])
+@pytest.mark.parametrize("key", ["c1", "c2", "c3", "c4", "c6", "c7"])
 def test_workload_points(key):
     cfg = wl.CONFIGS[key]
     max_pairs = max(cfg.bs_list) * cfg.topk
     cache = ExpertSlotCache(cfg, max_pairs)
-    sample = {"c1": None, "c2": 4, "c3": 2, "c4": 3, "c6": 2}[key]
+    sample = {"c1": None, "c2": 4, "c3": 2, "c4": 3, "c6": 2, "c7": 2}[key]
     for bs in cfg.bs_list:
         for mr in cfg.mr_list:
             _run_point(cache, cfg, bs, mr, ffn_tokens=sample)
@@ -226,6 +226,8 @@ SCALED = [
     ("mxfp4", dict(E=5, H=576, I=320, L=2, S=5)),
     ("fp8", dict(E=6, H=512, I=512, L=2, S=6)),
     ("fp8", dict(E=5, H=1024, I=1536, L=2, S=5)),
+    ("q4_0", dict(E=6, H=512, I=256, L=2, S=6)),
+    ("q4_0", dict(E=5, H=1024, I=768, L=2, S=5)),
 ]
 
 
@@ -233,7 +235,7 @@ SCALED = [
 def test_ffn_small_geometries(fmt, geo):
     """Several tiles with ragged tails, hot experts with more tokens than one pass
     holds, duplicate experts in a row, and a token routed to a single expert."""
-    base = {"bf16": "c2", "nvfp4": "c3", "mxfp4": "c4", "fp8": "c6"}[fmt]
+    base = {"bf16": "c2", "nvfp4": "c3", "mxfp4": "c4", "fp8": "c6", "q4_0": "c7"}[fmt]
     cfg = wl.scaled(wl.CONFIGS[base], topk=3, **geo)
     bs = 11
     cache = ExpertSlotCache(cfg, bs * cfg.topk)

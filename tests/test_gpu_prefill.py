@@ -24,6 +24,7 @@ CASES = {
     "nvfp4": wl.scaled(wl.CONFIGS["c3"], E=8, topk=4, H=512, I=256, L=3, S=16),
     "mxfp4": wl.scaled(wl.CONFIGS["c4"], E=8, topk=4, H=256, I=256, L=3, S=16),
     "fp8": wl.scaled(wl.CONFIGS["c6"], E=8, topk=4, H=512, I=512, L=3, S=16),
+    "q4_0": wl.scaled(wl.CONFIGS["c7"], E=8, topk=4, H=512, I=256, L=3, S=16),
 }
 
 
