@@ -154,8 +154,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
         const int nu = *p.s.n_unique;
         const int npass = nu > 0 ? *p.s.n_passes : 0;
         const int items = npass * c.tiles;
-        const int first = (int)((int64_t)blockIdx.x * items / gridDim.x);
-        const int last = (int)((int64_t)(blockIdx.x + 1) * items / gridDim.x);
+        // items dealt round-robin: the passes of one expert run side by side and share L2
+        const int first = blockIdx.x;
         bool waited = PHASE == kGU, ok = true;
         int issued = 0;
         const uint32_t box_bytes = NM * (kFKs / kFBox) * kFRows * kFBox;
@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
         int pairs_c[kFTok], texp_c[kFTok];
         const unsigned char *scb = p.bank[PHASE == kGU ? 1 : 3];
         const int64_t scb_bytes = p.bank_bytes[PHASE == kGU ? 1 : 3];
-        for (int it = first; it < last && ok; it++) {
+        for (int it = first; it < items && ok; it += gridDim.x) {
             const int pi = it / c.tiles, tile = it - pi * c.tiles;
             if (pi != cur_pi) {  // new pass: advance the owner and cache its tokens
                 while (u + 1 < nu && p.s.upoff[u + 1] <= pi) u++;

@@ -180,15 +180,18 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         const int nu = *p.s.n_unique;
         const int npass = nu > 0 ? *p.s.n_passes : 0;
         const int items = npass * c.tiles;
-        const int first = (int)((int64_t)blockIdx.x * items / gridDim.x);
-        const int last = (int)((int64_t)(blockIdx.x + 1) * items / gridDim.x);
+        // items are dealt round-robin, so at any moment the CTAs hold neighbouring column
+        // tiles of the same expert rows and a 128-byte line shared by two tiles (the up
+        // half starts 64 bytes into a line when I is an odd multiple of 64) is still in L2
+        // when the second tile asks for it
+        const int first = blockIdx.x;
         bool waited = PHASE == kGU, ok = true;
         int issued = 0;
         const uint32_t box_bytes = NM * (kKp * kCols + (kKp / 16) * kCols);
         int u = items > first ? pass_owner(p.s.upoff, nu, first / c.tiles) : 0;
         int cur_pi = -1, slot = 0, cnt = 0;
         int pairs_c[kMxTokMax], texp_c[kMxTokMax];
-        for (int it = first; it < last && ok; it++) {
+        for (int it = first; it < items && ok; it += gridDim.x) {
             const int pi = it / c.tiles, tile = it - pi * c.tiles;
             if (pi != cur_pi) {  // new pass: advance the owner and cache its tokens
                 while (u + 1 < nu && p.s.upoff[u + 1] <= pi) u++;

@@ -437,12 +437,13 @@ __global__ void __launch_bounds__(kTmaThreads, 1) ffn_rows_tma_kernel(FfnParams 
 
     if (warp == kProducerWarp) {
         if (lane != 0) return;
-        // Work items [first, last) of this CTA.
+        // Work items blockIdx.x, blockIdx.x + gridDim.x, ... of this CTA: dealt round-robin,
+        // the CTAs hold neighbouring tiles and the passes of one expert at the same time,
+        // so an expert read again by its next pass is still in L2.
         const int nu = *p.s.n_unique;
         const int npass = nu > 0 ? *p.s.n_passes : 0;
         const int items = npass * c.tiles;
-        const int first = (int)((int64_t)blockIdx.x * items / gridDim.x);
-        const int last = (int)((int64_t)(blockIdx.x + 1) * items / gridDim.x);
+        const int first = blockIdx.x;
         const uint64_t pol = evict_first_policy();
         const int H = p.H, I = p.I, R = c.R;
         const int nout = PHASE == kGateUp ? I : H;
@@ -450,9 +451,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1) ffn_rows_tma_kernel(FfnParams 
         bool waited = PHASE == kGateUp, ok = true;
         int issued = 0;
         int u = items > first ? pass_owner(p.s.upoff, nu, first / c.tiles) : 0;
-        for (int it = first; it < last && ok; it++) {
+        for (int it = first; it < items && ok; it += gridDim.x) {
             const int pi = it / c.tiles, tile = it - pi * c.tiles;
-            while (u + 1 < nu && p.s.upoff[u + 1] <= pi) u++;  // contiguous items: walk forward
+            while (u + 1 < nu && p.s.upoff[u + 1] <= pi) u++;  // increasing passes: walk forward
             int slot = p.s.uslot[u];
             slot = slot < 0 ? 0 : (slot >= p.S ? p.S - 1 : slot);
             const int pbase = (pi - p.s.upoff[u]) * kPassTokens;
