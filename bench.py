@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--no-hybrid", action="store_true", help="skip the hybrid-path measurements")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill-pipeline measurements")
     ap.add_argument("--copy-mode", default="fused", choices=["fused", "per_bank", "engine"])
+    ap.add_argument("--ffn-kernels", default="auto", choices=["auto", "rows", "mma"],
+                    help="FFN kernel family of bf16 layers (auto: chosen per call)")
     ap.add_argument("--experts", type=int, default=0, help="override E (smaller profiling cases)")
     ap.add_argument("--slots", type=int, default=0, help="override S (smaller profiling cases)")
     return ap.parse_args()
@@ -153,7 +155,7 @@ def install_hits(cache, r):
 # workload); a recorded figure is reported only while these sources are unchanged.
 TRAFFIC_SOURCES = {
     "copy": ["copy.cu", "internal.cuh"],
-    "ffn": ["ffn_tma.cu", "ffn_common.cuh", "internal.cuh"],
+    "ffn": ["ffn_rows_mma.cu", "pipeline.cuh", "ffn_common.cuh", "internal.cuh"],
 }
 
 
@@ -342,6 +344,8 @@ def run_gpu(args):
     # lists) so that the prefill probe can stream any layer
     cache = ExpertSlotCache(cfg, max(max(cfg.bs_list), bs, PREFILL_BS) * cfg.topk, alias_all=True, stream=stream)
     cache.set_copy_mode({"fused": F.COPY_FUSED, "per_bank": F.COPY_PER_BANK, "engine": F.COPY_ENGINE}[args.copy_mode])
+    if args.ffn_kernels != "auto":
+        cache.set_ffn_kernels({"rows": F.FFN_ROWS, "mma": F.FFN_MMA}[args.ffn_kernels])
     s = stream.cuda_stream
     d_ids = torch.from_numpy(r.topk_ids).cuda()
     d_slots = torch.empty_like(d_ids)
@@ -443,6 +447,7 @@ def run_gpu(args):
             "config": {"workload": f"{cfg.name} bs={bs} miss_rate={mr}", "E": cfg.E, "topk": cfg.topk, "H": cfg.H,
                        "I": cfg.I, "L": cfg.L, "S": cfg.S, "bs": bs, "miss_rate": mr, "active": r.active,
                        "misses": r.misses, "copy_MiB": r.misses * B / 2 ** 20, "copy_mode": args.copy_mode,
+                       "ffn_kernels": args.ffn_kernels,
                        "l2": f"inputs larger than L2: {r.misses * B / 2**20:.0f} MiB copied and "
                              f"{r.active * B / 2**20:.0f} MiB of expert weights read per step",
                        "parallelism": f"replicas x{world}",

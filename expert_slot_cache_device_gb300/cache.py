@@ -92,6 +92,10 @@ class ExpertSlotCache:
     def set_copy_mode(self, mode: int):
         F.ftmoe_set_copy_mode(self.handle, mode)
 
+    def set_ffn_kernels(self, kind: int):
+        """FFN kernel family of a bf16 cache: F.FFN_AUTO, F.FFN_ROWS or F.FFN_MMA."""
+        F.ftmoe_set_ffn_kernels(self.handle, kind)
+
     def prefetch_layer(self, layer: int, stream=None):
         F.ftmoe_prefetch_layer(self.handle, layer, _stream(stream))
 

@@ -147,6 +147,7 @@ struct ftmoe_cache {
     int fmt, E, L, S, H, I, max_pairs, nb;
     int num_sms;
     int copy_mode = FTMOE_COPY_FUSED;
+    int ffn_kernels = FTMOE_FFN_AUTO;
     int last_layer = -1;
     bool vec16 = true;
     std::vector<std::vector<const void *>> host;      // [nb][L] host addresses
@@ -289,6 +290,10 @@ int ftmoe_cache_create(const ftmoe_bank_spec *banks, int32_t num_banks, int32_t 
         for (int b = 0; b < 6; b++) sb[b] = c->dev_slots[b];
         make_mx_tma_maps(c->mx, sb, S, H, I);  // on failure the FFN uses the register path
     }
+    if (format == FTMOE_FMT_BF16 && lay.ffn) {
+        const unsigned char *sb[2] = {c->dev_slots[0], c->dev_slots[1]};
+        make_bf16_tma_maps(c->mx, sb, S, H, I);  // on failure the FFN uses the CUDA-core pipeline
+    }
     if (format == FTMOE_FMT_FP8 && lay.ffn) {
         const unsigned char *sb[4];
         for (int b = 0; b < 4; b++) sb[b] = c->dev_slots[b];
@@ -320,6 +325,18 @@ int ftmoe_set_copy_mode(ftmoe_cache_t *c, int32_t mode) {
     if (mode != FTMOE_COPY_FUSED && mode != FTMOE_COPY_PER_BANK && mode != FTMOE_COPY_ENGINE)
         return fail(FTMOE_ERR_INVALID_ARG, "unknown copy mode %d", mode);
     c->copy_mode = mode;
+    return FTMOE_OK;
+}
+
+int ftmoe_set_ffn_kernels(ftmoe_cache_t *c, int32_t kind) {
+    if (!c) return fail(FTMOE_ERR_INVALID_ARG, "cache is NULL");
+    if (kind != FTMOE_FFN_AUTO && kind != FTMOE_FFN_ROWS && kind != FTMOE_FFN_MMA)
+        return fail(FTMOE_ERR_INVALID_ARG, "unknown FFN kernel kind %d", kind);
+    if (kind != FTMOE_FFN_AUTO && c->fmt != FTMOE_FMT_BF16)
+        return fail(FTMOE_ERR_FORMAT, "only bf16 caches have two FFN kernel families");
+    if (kind == FTMOE_FFN_MMA && !c->mx.valid)
+        return fail(FTMOE_ERR_FORMAT, "no tensor-core FFN for this cache (H, I multiples of 256 and FFN scratch)");
+    c->ffn_kernels = kind;
     return FTMOE_OK;
 }
 
@@ -484,7 +501,7 @@ int ftmoe_expert_ffn_hybrid(ftmoe_cache_t *c, const void *d_x_bf16, int32_t bs, 
     p.y = static_cast<uint16_t *>(d_y_bf16);
     p.status = c->t.status;
     p.fmt = c->fmt; p.H = c->H; p.I = c->I; p.S = c->S; p.bs = bs; p.topk = topk; p.P = (int)P;
-    CK(launch_ffn(p, c->num_sms, static_cast<cudaStream_t>(stream), &c->mx), "ffn kernels");
+    CK(launch_ffn(p, c->num_sms, static_cast<cudaStream_t>(stream), &c->mx, c->ffn_kernels), "ffn kernels");
     return FTMOE_OK;
 }
 

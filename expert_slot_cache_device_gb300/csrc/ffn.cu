@@ -735,7 +735,7 @@ cudaError_t launch_dyn(K kernel, int grid, size_t smem, cudaStream_t st, const F
 
 }  // namespace
 
-cudaError_t launch_ffn(const FfnParams &p_in, int num_sms, cudaStream_t st, const MxTmaMaps *mx) {
+cudaError_t launch_ffn(const FfnParams &p_in, int num_sms, cudaStream_t st, const MxTmaMaps *mx, int kernels) {
     FfnParams p = p_in;
     cudaError_t e;
     size_t route_smem = (size_t)p.S * sizeof(int);
@@ -743,7 +743,10 @@ cudaError_t launch_ffn(const FfnParams &p_in, int num_sms, cudaStream_t st, cons
         e = cudaFuncSetAttribute(ffn_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)route_smem);
         if (e != cudaSuccess) return e;
     }
-    const bool fp4_rows_tma = num_sms > 0 && ffn_rows_tma_supported(p);
+    // bf16: the tensor-core pipeline wherever the shape has it (AUTO: it matches the CUDA-core
+    // pipeline up to one token per expert and is faster from two up), unless ROWS is asked
+    const bool bf16_mma = num_sms > 0 && kernels != FTMOE_FFN_ROWS && ffn_bf16_mma_supported(p, mx);
+    const bool fp4_rows_tma = num_sms > 0 && !bf16_mma && ffn_rows_tma_supported(p);
     const bool mx_tma = num_sms > 0 && ffn_mx_tma_supported(p, mx);
     const bool fp8_tma = num_sms > 0 && ffn_fp8_tma_supported(p, mx);
     if (p.fmt == FTMOE_FMT_FP8 && !fp8_tma) return cudaErrorNotSupported;  // block FP8 has one pipeline only
@@ -752,14 +755,17 @@ cudaError_t launch_ffn(const FfnParams &p_in, int num_sms, cudaStream_t st, cons
         (fp4_rows_tma && (p.fmt == FTMOE_FMT_NVFP4 || p.fmt == FTMOE_FMT_Q4_0)) || mx_tma || fp8_tma;
     p.x16_emax = p.fmt == FTMOE_FMT_MXFP4 ? 9 : (p.fmt == FTMOE_FMT_Q4_0 ? 8 : 10);
     p.x16_swz = fp4_rows_tma && p.fmt == FTMOE_FMT_NVFP4 ? 1 : (fp4_rows_tma && p.fmt == FTMOE_FMT_Q4_0 ? 2 : 0);
-    p.pass_tokens = (mx_tma || fp8_tma) ? kMxPassTokens : kPassTokens;
+    p.pass_tokens = (mx_tma || fp8_tma || bf16_mma) ? kMxPassTokens : kPassTokens;
     ffn_route_kernel<<<1 + (want_x16 ? p.bs : 0), 1024, route_smem, st>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
     const int umax = p.P < p.S ? p.P : p.S;  // distinct slots at most
     const size_t budget = 64 * 1024;
     bool pdl_combine = false;
-    if (fp4_rows_tma) {
+    if (bf16_mma) {
+        if ((e = launch_ffn_bf16_mma(p, *mx, num_sms, st)) != cudaSuccess) return e;
+        pdl_combine = true;
+    } else if (fp4_rows_tma) {
         if ((e = launch_ffn_rows_tma(p, num_sms, st)) != cudaSuccess) return e;
         pdl_combine = true;
     } else if (mx_tma) {

@@ -187,6 +187,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         const int first = blockIdx.x;
         bool waited = PHASE == kGU, ok = true;
         int issued = 0;
+        const uint64_t pol = evict_first_l2();  // weights are read once
         const uint32_t box_bytes = NM * (kKp * kCols + (kKp / 16) * kCols);
         int u = items > first ? pass_owner(p.s.upoff, nu, first / c.tiles) : 0;
         int cur_pi = -1, slot = 0, cnt = 0;
@@ -250,8 +251,9 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                     // rows past the slot's last k-pair row are zero-filled by the copy, not read
                     for (int m = 0; m < NM; m++) {
                         const int x = n0 + (m ? I : 0);
-                        tma3d(st + m * kKp * kCols, &blocks_map, x, ks * kKp, slot, &full[s]);
-                        tma3d(st + c.sc_off + m * (kKp / 16) * kCols, &scales_map, x, ks * (kKp / 16), slot, &full[s]);
+                        tma3d_hint(st + m * kKp * kCols, &blocks_map, x, ks * kKp, slot, &full[s], pol);
+                        tma3d_hint(st + c.sc_off + m * (kKp / 16) * kCols, &scales_map, x, ks * (kKp / 16), slot,
+                                   &full[s], pol);
                     }
                     for (int i = 0; i < ntok; i++) {
                         const int q = hh.pairs[i];
@@ -508,6 +510,17 @@ bool make_mx_tma_maps(MxTmaMaps &m, const unsigned char *const *banks, int S, in
               encode_u8(m.gu_scales, banks[1], ngu, (uint64_t)(H / 32), (uint64_t)S, kKp / 16, none) &&
               encode_u8(m.dn_blocks, banks[3], ndn, (uint64_t)(I / 2), (uint64_t)S, kKp, sw) &&
               encode_u8(m.dn_scales, banks[4], ndn, (uint64_t)(I / 32), (uint64_t)S, kKp / 16, none);
+    m.valid = ok;
+    return ok;
+}
+
+bool make_bf16_tma_maps(MxTmaMaps &m, const unsigned char *const *banks, int S, int H, int I) {
+    m.valid = false;
+    if (H % 256 || I % 256) return false;
+    // bf16 weights [N rows, 2K bytes] per slot, boxes of 128 bytes (64 k) x 64 rows, 128-byte swizzle
+    const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    bool ok = encode_u8(m.gu_blocks, banks[0], 2ull * H, 2ull * I, (uint64_t)S, 64, sw) &&
+              encode_u8(m.dn_blocks, banks[1], 2ull * I, (uint64_t)H, (uint64_t)S, 64, sw);
     m.valid = ok;
     return ok;
 }

@@ -2,9 +2,10 @@
 // warp-specialised bulk-copy pipeline.
 //
 // Decode batches make the FFN a grouped GEMV that must stream every used expert's
-// weights from HBM exactly once. Here each CTA owns a contiguous range of work items
-// (distinct slot u, tile of R output rows), so neighbouring CTAs read neighbouring
-// rows. One producer thread fills a ring of shared-memory stages with 1-D bulk
+// weights from HBM exactly once. Work items (pass of a distinct slot u, tile of R output
+// rows) are dealt round-robin over the CTAs, so at any moment the CTAs read neighbouring
+// rows and the passes of one hot expert side by side (its second pass hits L2). One
+// producer thread fills a ring of shared-memory stages with 1-D bulk
 // asynchronous copies (cp.async.bulk, completion counted on an mbarrier): the item's
 // weight rows (gate and up rows of R neurons, or R down rows, plus the nvfp4 block
 // scales) and the token vectors the item needs (bf16 activations for gate_up, fp32
@@ -149,10 +150,9 @@ struct Seg {
 
 // ---------------------------------------------------------------- consumers
 
-// Running max |h| of one pair, kept by lane t for the pair in token slot t: consecutive
-// items of a CTA mostly share their pairs, so the pair's max word is updated once per
-// run of items instead of once per row (per-row atomics on a handful of words
-// serialised on one L2 slice).
+// Running max |h| of one pair, kept by lane t for the pair in token slot t: the pair's max
+// word is updated once per item (or run of items sharing the pair) instead of once per
+// row (per-row atomics on a handful of words serialised on one L2 slice).
 struct HMax {
     int pair = -1;
     float m = 0.f;

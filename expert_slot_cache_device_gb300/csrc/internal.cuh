@@ -104,9 +104,8 @@ struct FfnParams {
     int32_t pass_tokens;  // tokens per pass of the pipelined kernels (kPassTokens / kMxPassTokens)
 };
 
-// Tensor maps (CUtensorMap, 128 bytes each) over the transposed mxfp4 slot banks.
 // Tensor maps (CUtensorMap, 128 bytes each) of the tensor-map pipelines: the transposed
-// mxfp4 banks, or the block-FP8 weight banks (gu_blocks / dn_blocks).
+// mxfp4 banks, or the block-FP8 / bf16 weight banks (gu_blocks / dn_blocks).
 struct MxTmaMaps {
     alignas(128) unsigned char gu_blocks[128];
     alignas(128) unsigned char gu_scales[128];
@@ -115,7 +114,10 @@ struct MxTmaMaps {
     bool valid = false;
 };
 bool make_mx_tma_maps(MxTmaMaps &m, const unsigned char *const *banks, int S, int H, int I);
-cudaError_t launch_ffn(const FfnParams &p, int num_sms, cudaStream_t st, const MxTmaMaps *mx = nullptr);
+// kernels: FTMOE_FFN_* (bf16 caches: AUTO takes the tensor-core pipeline where the shape has
+// it; other formats ignore it).
+cudaError_t launch_ffn(const FfnParams &p, int num_sms, cudaStream_t st, const MxTmaMaps *mx = nullptr,
+                       int kernels = FTMOE_FFN_AUTO);
 // Persistent bulk-copy pipeline for the row-major formats (bf16; nvfp4 with H, I multiples of 256).
 bool ffn_rows_tma_supported(const FfnParams &p);
 cudaError_t launch_ffn_rows_tma(const FfnParams &p, int num_sms, cudaStream_t st);
@@ -126,6 +128,10 @@ cudaError_t launch_ffn_mx_tma(const FfnParams &p, const MxTmaMaps &maps, int num
 bool make_fp8_tma_maps(MxTmaMaps &m, const unsigned char *const *banks, int S, int H, int I);
 bool ffn_fp8_tma_supported(const FfnParams &p, const MxTmaMaps *maps);
 cudaError_t launch_ffn_fp8_tma(const FfnParams &p, const MxTmaMaps &maps, int num_sms, cudaStream_t st);
+// Tensor-core pipeline for bf16 (weight maps in gu_blocks / dn_blocks; H, I multiples of 256).
+bool make_bf16_tma_maps(MxTmaMaps &m, const unsigned char *const *banks, int S, int H, int I);
+bool ffn_bf16_mma_supported(const FfnParams &p, const MxTmaMaps *maps);
+cudaError_t launch_ffn_bf16_mma(const FfnParams &p, const MxTmaMaps &maps, int num_sms, cudaStream_t st);
 
 // Record `msg` as the thread's last error message and return `code`.
 int report_error(int code, const char *msg);

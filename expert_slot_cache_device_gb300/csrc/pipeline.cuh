@@ -1,5 +1,5 @@
 // Device helpers shared by the tensor-map pipelines: shared-memory addresses, bounded
-// mbarrier waits, bulk and tensor copies, and the warp-level f16 MMA.
+// mbarrier waits, bulk and tensor copies, and the warp-level f16 / bf16 MMA.
 #pragma once
 #include <cuda.h>
 #include <cstdint>
@@ -50,6 +50,24 @@ __device__ __forceinline__ void tma3d(void *dst, const CUtensorMap *map, int x, 
         : "memory");
 }
 
+// The same with an L2 cache policy (createpolicy), e.g. evict-first for weights read once:
+// the lines a preceding copy left dirty in L2 then stay there instead of being written back
+// while the weights stream through.
+__device__ __forceinline__ void tma3d_hint(void *dst, const CUtensorMap *map, int x, int y, int z, uint64_t *bar,
+                                           uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+        "{%2, %3, %4}], [%5], %6;" ::"r"(su32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(su32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t evict_first_l2() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 __device__ __forceinline__ void bulk1d(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                      su32(dst)),
@@ -72,6 +90,25 @@ __device__ __forceinline__ void mma_f16_16816_z(float (&d)[4], uint32_t a0, uint
         "{%10, %10, %10, %10};"
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+// d += A * B with bf16 operands and an fp32 accumulator (A 16 x 16 row, B 16 x 8 col).
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Four 8 x 8 matrices of 16-bit elements from shared memory (lane l gives the address of
+// row l % 8 of matrix l / 8); lane (g, tig) receives elements (g, 2 tig) and (g, 2 tig + 1)
+// of each matrix, which for the matrices (rows 0-7 | 8-15) x (k 0-7 | 8-15) of a 16 x 16
+// tile is the A fragment of mma m16n8k16.
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(su32(p)));
 }
 
 // Two e8m0 bytes (low byte first) -> their values 2^(b - 127) as floats, through the

@@ -24,6 +24,7 @@ DT_U8, DT_BF16, DT_F16, DT_E4M3, DT_E8M0, DT_F32, DT_Q4_0 = 0, 1, 2, 3, 4, 5, 6
 DTYPES = {"u8": DT_U8, "bf16": DT_BF16, "f16": DT_F16, "e4m3": DT_E4M3, "e8m0": DT_E8M0, "f32": DT_F32,
           "q4_0": DT_Q4_0}
 COPY_FUSED, COPY_PER_BANK, COPY_ENGINE = 0, 1, 2
+FFN_AUTO, FFN_ROWS, FFN_MMA = 0, 1, 2
 MAX_BANKS = 8
 
 EXPORTS = [
@@ -33,6 +34,7 @@ EXPORTS = [
     "ftmoe_last_error", "ftmoe_expert_ffn_noalloc", "ftmoe_ensure_experts_hybrid", "ftmoe_hybrid_fetch_fraction",
     "ftmoe_expert_ffn_hybrid", "ftmoe_cpu_expert_ffn", "ftmoe_prefetch_layer", "ftmoe_prefill_layers",
     "ftmoe_measure_link", "ftmoe_measure_cpu_moe", "ftmoe_moe_backend_decision", "ftmoe_get_counters",
+    "ftmoe_set_ffn_kernels",
 ]
 BACKEND_OFFLOAD, BACKEND_HYBRID = 0, 1
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -76,6 +78,7 @@ def lib() -> ctypes.CDLL:
         "ftmoe_copy_missing": [P, P],
         "ftmoe_expert_ffn": [P, P, i32, P, P, i32, P, P],
         "ftmoe_set_copy_mode": [P, i32],
+        "ftmoe_set_ffn_kernels": [P, i32],
         "ftmoe_cache_get_state": [P, P, P, P, P],
         "ftmoe_cache_set_state": [P, P, P, u32, P],
         "ftmoe_get_miss_list": [P, P, P, P, P],
@@ -162,6 +165,10 @@ def ftmoe_expert_ffn(cache: int, d_x: int, bs: int, d_slots: int, d_weights: int
 
 def ftmoe_set_copy_mode(cache: int, mode: int) -> None:
     _check(lib().ftmoe_set_copy_mode(cache, mode))
+
+
+def ftmoe_set_ffn_kernels(cache: int, kind: int) -> None:
+    _check(lib().ftmoe_set_ffn_kernels(cache, kind))
 
 
 def ftmoe_cache_get_state(cache: int, h_owner: int, h_stamp: int, h_clock: int, stream: int) -> None:

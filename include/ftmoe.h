@@ -92,6 +92,13 @@ extern "C" {
                                  consecutive slots (a single miss is a run of one),
                                  in transfers of at most 256 MiB */
 
+/* Expert FFN kernel families of a bf16 cache (other formats have one family each and
+ * accept FTMOE_FFN_AUTO only) */
+#define FTMOE_FFN_AUTO 0   /* MMA where the shape has it, else ROWS (default) */
+#define FTMOE_FFN_ROWS 1   /* CUDA-core bulk-copy pipeline: fp32 FMAs, passes of 4 tokens */
+#define FTMOE_FFN_MMA 2    /* tensor-core pipeline: bf16 mma.sync, passes of 8 tokens,
+                              h kept as two bf16 terms; needs H and I multiples of 256 */
+
 /* Limits of one cache. */
 #define FTMOE_MAX_BANKS 8
 #define FTMOE_MAX_EXPERTS 8192      /* E */
@@ -305,6 +312,14 @@ int ftmoe_moe_backend_decision(int32_t format, double link_gbps, double cpu_gbps
 
 /* Select the copy_missing implementation (FTMOE_COPY_*). */
 int ftmoe_set_copy_mode(ftmoe_cache_t *cache, int32_t mode);
+
+/* Select the expert FFN kernels (FTMOE_FFN_*) of later ftmoe_expert_ffn calls. Both
+ * families compute the same FFN (hit experts read from the slot cache: benchmark guide,
+ * section 1; bf16 gate_up and down banks: section 4.2). FTMOE_ERR_INVALID_ARG for an
+ * unknown kind; FTMOE_ERR_FORMAT for ROWS or MMA on a cache that is not bf16, or for MMA
+ * when the shape has no tensor-core pipeline (H or I not a multiple of 256, or the cache
+ * was created without FFN scratch). Host only. */
+int ftmoe_set_ffn_kernels(ftmoe_cache_t *cache, int32_t kind);
 
 /* Read the state into host arrays h_owner[S] (flat id or -1), h_stamp[S], *h_clock.
  * Synchronises the stream. */

@@ -271,6 +271,62 @@ def test_ffn_small_geometries(fmt, geo):
     cache.close()
 
 
+def _install_all(cache, cfg, rng):
+    perm = rng.permutation(cfg.S)
+    slot_of = {e: int(perm[e]) for e in range(cfg.E)}
+    for b in range(cache.nb):
+        for e in range(cfg.E):
+            cache.slots[b][slot_of[e]].copy_(cache.host[b][0][e])
+    return slot_of
+
+
+@pytest.mark.parametrize("geo", [dict(E=6, H=1024, I=256, L=2, S=6), dict(E=5, H=512, I=768, L=2, S=7)])
+def test_bf16_ffn_kernel_families(geo):
+    """Both bf16 FFN kernel families (CUDA-core rows pipeline, tensor-core pipeline) and the
+    automatic choice against the oracle on one routed batch: a hot expert over two passes
+    of eight tokens, duplicates within a row, several 64-row tiles per matrix."""
+    cfg = wl.scaled(wl.CONFIGS["c2"], topk=4, **geo)
+    bs = 13
+    cache = ExpertSlotCache(cfg, bs * cfg.topk)
+    rng = np.random.default_rng(geo["I"])
+    ids = rng.integers(0, cfg.E, (bs, cfg.topk)).astype(np.int32)
+    ids[:, 0] = 1
+    ids[4] = [3, 3, 3, 3]
+    w = rng.random((bs, cfg.topk)).astype(np.float32)
+    x = wl.f32_to_bf16_bits(rng.standard_normal((bs, cfg.H)).astype(np.float32))
+    slot_of = _install_all(cache, cfg, rng)
+    slots = np.vectorize(slot_of.get)(ids).astype(np.int32)
+    ref = oracle_ffn(cache, 0, ids, w, x)
+    for kind in (F.FFN_ROWS, F.FFN_MMA, F.FFN_AUTO):
+        cache.set_ffn_kernels(kind)
+        d_y = torch.empty((bs, cfg.H), dtype=torch.bfloat16, device="cuda")
+        cache.ffn(x_dev(x), to_dev(slots), to_dev(w), d_y)
+        assert cache.status() == F.OK
+        assert_ffn_close(bf16_to_f64(d_y), ref, f"bf16 kernels={kind} {geo}")
+    with pytest.raises(F.FtmoeError) as ei:
+        cache.set_ffn_kernels(7)
+    assert ei.value.code == F.ERR_INVALID_ARG
+    cache.close()
+
+
+def test_ffn_kernel_selector_formats():
+    """ROWS / MMA only on bf16 caches; MMA only where the shape has the tensor-core pipeline."""
+    c1 = ExpertSlotCache(wl.CONFIGS["c1"], 8)  # I = 128: no tensor-core pipeline
+    c1.set_ffn_kernels(F.FFN_ROWS)
+    c1.set_ffn_kernels(F.FFN_AUTO)
+    with pytest.raises(F.FtmoeError) as ei:
+        c1.set_ffn_kernels(F.FFN_MMA)
+    assert ei.value.code == F.ERR_FORMAT
+    c1.close()
+    nv = ExpertSlotCache(wl.scaled(wl.CONFIGS["c3"], E=4, H=512, I=256, L=1, S=4), 8)
+    nv.set_ffn_kernels(F.FFN_AUTO)
+    for kind in (F.FFN_ROWS, F.FFN_MMA):
+        with pytest.raises(F.FtmoeError) as ei:
+            nv.set_ffn_kernels(kind)
+        assert ei.value.code == F.ERR_FORMAT
+    nv.close()
+
+
 # ------------------------------------------------------------------ multi-step trace
 
 
