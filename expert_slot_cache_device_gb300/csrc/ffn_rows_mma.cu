@@ -70,6 +70,7 @@ constexpr int kFStagesMax = 4;
 constexpr int kFTok = 8;                      // tokens per pass = the MMA's N
 static_assert(kFTok == kMxPassTokens, "the routing kernel cuts passes of kFTok tokens");
 static_assert(kFCW == 16, "four M tiles x four boxes");
+static_assert(kFTok * kFRows <= kFCW * 32, "one epilogue output per consumer thread at most");
 
 enum { kGU = 0, kDN = 1 };
 
@@ -402,11 +403,16 @@ __device__ __forceinline__ void rows_mma_body(const FfnParams &p, const F8Cfg &c
             if (lane == 0) atomicCAS(p.status, 0, FTMOE_ERR_STATE);
             return;
         }
-        const int n0 = hs.n0;
-        // i = t * kFRows + row: a warp's 32 threads share one token t (kFRows % 32 == 0)
-        for (int i = threadIdx.x; i < ntok * kFRows; i += kFCW * 32) {
-            const int t = i / kFRows, row = i - t * kFRows;
-            const float xs_t = WK == kWE4M3 ? ldexpf(1.f, hs.texp[t]) : 1.f;
+        // the epilogue needs only this thread's token from the header (ntok * kFRows <=
+        // kFCW * 32, so every thread has at most one output), so the stage is released
+        // now and the producer refills it while the outputs are formed
+        const int n0 = hs.n0, i = threadIdx.x, t = i / kFRows, row = i - t * kFRows;
+        const bool has = i < ntok * kFRows;  // whole warps: ntok * kFRows is a multiple of 32
+        const int q_t = has ? hs.pairs[t] : 0, e_t = has ? hs.texp[t] : 0;
+        __syncwarp();
+        if (lane == 0) bar_arrive(&empty[s]);
+        if (has) {
+            const float xs_t = WK == kWE4M3 ? ldexpf(1.f, e_t) : 1.f;
             float v[NM];
 #pragma unroll
             for (int m = 0; m < NM; m++) {
@@ -415,13 +421,10 @@ __device__ __forceinline__ void rows_mma_body(const FfnParams &p, const F8Cfg &c
                 for (int q4 = 0; q4 < 4; q4++) sum += red[((m * 4 + q4) * kFTok + t) * kRedStride + row];
                 v[m] = sum * xs_t;
             }
-            rows_mma_store<WK, PHASE, NM>(p, hs.pairs[t], n0 + row, v, lane);
+            rows_mma_store<WK, PHASE, NM>(p, q_t, n0 + row, v, lane);
         }
         __syncwarp();
-        if (lane == 0) {
-            bar_arrive(&rbar[1]);
-            bar_arrive(&empty[s]);
-        }
+        if (lane == 0) bar_arrive(&rbar[1]);
         if (!bar_wait(&rbar[1], rphase)) {
             if (lane == 0) atomicCAS(p.status, 0, FTMOE_ERR_STATE);
             return;
