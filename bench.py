@@ -155,7 +155,8 @@ def install_hits(cache, r):
 # workload); a recorded figure is reported only while these sources are unchanged.
 TRAFFIC_SOURCES = {
     "copy": ["copy.cu", "internal.cuh"],
-    "ffn": ["ffn_rows_mma.cu", "pipeline.cuh", "ffn_common.cuh", "internal.cuh"],
+    "ffn_rows": ["ffn_tma.cu", "ffn_common.cuh", "internal.cuh"],      # CUDA-core pipelines
+    "ffn_mma": ["ffn_rows_mma.cu", "pipeline.cuh", "ffn_common.cuh", "internal.cuh"],  # tensor-core
 }
 
 
@@ -346,6 +347,8 @@ def run_gpu(args):
     cache.set_copy_mode({"fused": F.COPY_FUSED, "per_bank": F.COPY_PER_BANK, "engine": F.COPY_ENGINE}[args.copy_mode])
     if args.ffn_kernels != "auto":
         cache.set_ffn_kernels({"rows": F.FFN_ROWS, "mma": F.FFN_MMA}[args.ffn_kernels])
+    # the FFN kernel family this call runs (CUDA-core rows pipelines or tensor-core pipelines)
+    ffn_kind = "ffn_mma" if F.ftmoe_ffn_kernels_for(cache.handle, bs, cfg.topk) == F.FFN_MMA else "ffn_rows"
     s = stream.cuda_stream
     d_ids = torch.from_numpy(r.topk_ids).cuda()
     d_slots = torch.empty_like(d_ids)
@@ -447,7 +450,7 @@ def run_gpu(args):
             "config": {"workload": f"{cfg.name} bs={bs} miss_rate={mr}", "E": cfg.E, "topk": cfg.topk, "H": cfg.H,
                        "I": cfg.I, "L": cfg.L, "S": cfg.S, "bs": bs, "miss_rate": mr, "active": r.active,
                        "misses": r.misses, "copy_MiB": r.misses * B / 2 ** 20, "copy_mode": args.copy_mode,
-                       "ffn_kernels": args.ffn_kernels,
+                       "ffn_kernels": f"{args.ffn_kernels}: {'tensor cores' if ffn_kind == 'ffn_mma' else 'CUDA cores'}",
                        "l2": f"inputs larger than L2: {r.misses * B / 2**20:.0f} MiB copied and "
                              f"{r.active * B / 2**20:.0f} MiB of expert weights read per step",
                        "parallelism": f"replicas x{world}",
@@ -462,7 +465,7 @@ def run_gpu(args):
                                         f"{links['memcpy']:.1f}, SM zero-copy read {links['sm_read']:.1f}) GB/s"},
             "roofline_ffn": {"bound": "hbm", "kernel": "expert FFN (route + gate_up + down + combine)",
                              "achieved": ffn_ach, "peak": hbm_peak, "unit": "GB/s", "frac": ffn_ach / hbm_peak,
-                             "traffic": recorded_traffic(f"{cfg.name}/bs{bs}/mr{mr}", "ffn"),
+                             "traffic": recorded_traffic(f"{cfg.name}/bs{bs}/mr{mr}", ffn_kind),
                              "peak_source": hbm_src},
             "link_peak_GBps": links,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

@@ -340,6 +340,23 @@ int ftmoe_set_ffn_kernels(ftmoe_cache_t *c, int32_t kind) {
     return FTMOE_OK;
 }
 
+int ftmoe_ffn_kernels_for(ftmoe_cache_t *c, int32_t bs, int32_t topk, int32_t *kind) {
+    if (!c || !kind) return fail(FTMOE_ERR_INVALID_ARG, "NULL argument");
+    if (bs < 0 || topk <= 0) return fail(FTMOE_ERR_INVALID_ARG, "bs=%d, topk=%d", bs, topk);
+    if (!c->ffn) return fail(FTMOE_ERR_STATE, "the cache was created without FFN scratch");
+    FfnParams p;
+    memset(&p, 0, sizeof p);
+    p.s = c->s;
+    p.fmt = c->fmt; p.H = c->H; p.I = c->I; p.S = c->S; p.bs = bs; p.topk = topk; p.P = bs * topk;
+    p.E = c->E;
+    if (c->fmt == FTMOE_FMT_BF16)
+        *kind = ffn_bf16_uses_mma(p, c->num_sms, &c->mx, c->ffn_kernels) ? FTMOE_FFN_MMA : FTMOE_FFN_ROWS;
+    else  // block FP8 and mxfp4 run on the tensor cores, nvfp4 and Q4_0 on the CUDA cores
+        *kind = (c->fmt == FTMOE_FMT_FP8 || (c->fmt == FTMOE_FMT_MXFP4 && c->mx.valid)) ? FTMOE_FFN_MMA
+                                                                                        : FTMOE_FFN_ROWS;
+    return FTMOE_OK;
+}
+
 static int ensure_impl(ftmoe_cache_t *c, int32_t layer, const int32_t *d_topk_ids, int32_t bs, int32_t topk,
                        int32_t *d_slots_out, int hybrid, int32_t max_fetch, float fetch_fraction, int32_t *d_counts,
                        void *stream) {
@@ -501,6 +518,7 @@ int ftmoe_expert_ffn_hybrid(ftmoe_cache_t *c, const void *d_x_bf16, int32_t bs, 
     p.y = static_cast<uint16_t *>(d_y_bf16);
     p.status = c->t.status;
     p.fmt = c->fmt; p.H = c->H; p.I = c->I; p.S = c->S; p.bs = bs; p.topk = topk; p.P = (int)P;
+    p.E = c->E;
     CK(launch_ffn(p, c->num_sms, static_cast<cudaStream_t>(stream), &c->mx, c->ffn_kernels), "ffn kernels");
     return FTMOE_OK;
 }

@@ -735,6 +735,15 @@ cudaError_t launch_dyn(K kernel, int grid, size_t smem, cudaStream_t st, const F
 
 }  // namespace
 
+bool ffn_bf16_uses_mma(const FfnParams &p, int num_sms, const MxTmaMaps *mx, int kernels) {
+    // AUTO: the tensor-core pipeline, except around one routed token per expert (E/4 <= P <
+    // 2E), where the CUDA-core pipeline, which needs no cross-warp reduction per item, is
+    // about 1% faster; from two tokens per expert up the tensor cores win by 10-35%
+    const bool one_per_expert = 4 * (int64_t)p.P >= p.E && p.P < 2 * (int64_t)p.E;
+    return num_sms > 0 && kernels != FTMOE_FFN_ROWS && ffn_bf16_mma_supported(p, mx) &&
+           (kernels == FTMOE_FFN_MMA || !one_per_expert);
+}
+
 cudaError_t launch_ffn(const FfnParams &p_in, int num_sms, cudaStream_t st, const MxTmaMaps *mx, int kernels) {
     FfnParams p = p_in;
     cudaError_t e;
@@ -743,9 +752,7 @@ cudaError_t launch_ffn(const FfnParams &p_in, int num_sms, cudaStream_t st, cons
         e = cudaFuncSetAttribute(ffn_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)route_smem);
         if (e != cudaSuccess) return e;
     }
-    // bf16: the tensor-core pipeline wherever the shape has it (AUTO: it matches the CUDA-core
-    // pipeline up to one token per expert and is faster from two up), unless ROWS is asked
-    const bool bf16_mma = num_sms > 0 && kernels != FTMOE_FFN_ROWS && ffn_bf16_mma_supported(p, mx);
+    const bool bf16_mma = ffn_bf16_uses_mma(p, num_sms, mx, kernels);
     const bool fp4_rows_tma = num_sms > 0 && !bf16_mma && ffn_rows_tma_supported(p);
     const bool mx_tma = num_sms > 0 && ffn_mx_tma_supported(p, mx);
     const bool fp8_tma = num_sms > 0 && ffn_fp8_tma_supported(p, mx);

@@ -99,6 +99,7 @@ struct FfnParams {
     uint16_t *y;            // [bs, H] bf16
     int32_t *status;
     int32_t fmt, H, I, S, bs, topk, P;
+    int32_t E;         // experts per layer (0: unknown; used only to choose kernels)
     int32_t x16_emax;  // f16 activation copy keeps max |x| < 2^x16_emax
     int32_t x16_swz;   // f16 activation copy layout: 0 plain, 1 swz_x16 (nvfp4), 2 swz_q4x16 (Q4_0)
     int32_t pass_tokens;  // tokens per pass of the pipelined kernels (kPassTokens / kMxPassTokens)
@@ -114,8 +115,9 @@ struct MxTmaMaps {
     bool valid = false;
 };
 bool make_mx_tma_maps(MxTmaMaps &m, const unsigned char *const *banks, int S, int H, int I);
-// kernels: FTMOE_FFN_* (bf16 caches: AUTO takes the tensor-core pipeline where the shape has
-// it; other formats ignore it).
+// kernels: FTMOE_FFN_* (bf16 caches: see ffn_bf16_uses_mma; other formats ignore it).
+// Whether a bf16 call runs the tensor-core pipeline (the AUTO rule lives here).
+bool ffn_bf16_uses_mma(const FfnParams &p, int num_sms, const MxTmaMaps *mx, int kernels);
 cudaError_t launch_ffn(const FfnParams &p, int num_sms, cudaStream_t st, const MxTmaMaps *mx = nullptr,
                        int kernels = FTMOE_FFN_AUTO);
 // Persistent bulk-copy pipeline for the row-major formats (bf16; nvfp4 with H, I multiples of 256).

@@ -34,7 +34,7 @@ EXPORTS = [
     "ftmoe_last_error", "ftmoe_expert_ffn_noalloc", "ftmoe_ensure_experts_hybrid", "ftmoe_hybrid_fetch_fraction",
     "ftmoe_expert_ffn_hybrid", "ftmoe_cpu_expert_ffn", "ftmoe_prefetch_layer", "ftmoe_prefill_layers",
     "ftmoe_measure_link", "ftmoe_measure_cpu_moe", "ftmoe_moe_backend_decision", "ftmoe_get_counters",
-    "ftmoe_set_ffn_kernels",
+    "ftmoe_set_ffn_kernels", "ftmoe_ffn_kernels_for",
 ]
 BACKEND_OFFLOAD, BACKEND_HYBRID = 0, 1
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -79,6 +79,7 @@ def lib() -> ctypes.CDLL:
         "ftmoe_expert_ffn": [P, P, i32, P, P, i32, P, P],
         "ftmoe_set_copy_mode": [P, i32],
         "ftmoe_set_ffn_kernels": [P, i32],
+        "ftmoe_ffn_kernels_for": [P, i32, i32, P],
         "ftmoe_cache_get_state": [P, P, P, P, P],
         "ftmoe_cache_set_state": [P, P, P, u32, P],
         "ftmoe_get_miss_list": [P, P, P, P, P],
@@ -169,6 +170,12 @@ def ftmoe_set_copy_mode(cache: int, mode: int) -> None:
 
 def ftmoe_set_ffn_kernels(cache: int, kind: int) -> None:
     _check(lib().ftmoe_set_ffn_kernels(cache, kind))
+
+
+def ftmoe_ffn_kernels_for(cache: int, bs: int, topk: int) -> int:
+    kind = ctypes.c_int32(0)
+    _check(lib().ftmoe_ffn_kernels_for(cache, bs, topk, ctypes.byref(kind)))
+    return kind.value
 
 
 def ftmoe_cache_get_state(cache: int, h_owner: int, h_stamp: int, h_clock: int, stream: int) -> None:

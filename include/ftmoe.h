@@ -94,7 +94,9 @@ extern "C" {
 
 /* Expert FFN kernel families of a bf16 cache (other formats have one family each and
  * accept FTMOE_FFN_AUTO only) */
-#define FTMOE_FFN_AUTO 0   /* MMA where the shape has it, else ROWS (default) */
+#define FTMOE_FFN_AUTO 0   /* MMA where the shape has it, except ROWS when the call has
+                              about one routed pair per expert (E/4 <= bs*topk < 2E);
+                              default */
 #define FTMOE_FFN_ROWS 1   /* CUDA-core bulk-copy pipeline: fp32 FMAs, passes of 4 tokens */
 #define FTMOE_FFN_MMA 2    /* tensor-core pipeline: bf16 mma.sync, passes of 8 tokens,
                               h kept as two bf16 terms; needs H and I multiples of 256 */
@@ -320,6 +322,12 @@ int ftmoe_set_copy_mode(ftmoe_cache_t *cache, int32_t mode);
  * when the shape has no tensor-core pipeline (H or I not a multiple of 256, or the cache
  * was created without FFN scratch). Host only. */
 int ftmoe_set_ffn_kernels(ftmoe_cache_t *cache, int32_t kind);
+
+/* The kernel family (FTMOE_FFN_ROWS: CUDA cores, FTMOE_FFN_MMA: tensor cores) that
+ * ftmoe_expert_ffn on this cache runs for a call of bs tokens x topk experts, under the
+ * current ftmoe_set_ffn_kernels choice. FTMOE_ERR_INVALID_ARG for NULL or bs < 0 or
+ * topk <= 0; FTMOE_ERR_STATE for a cache created without FFN scratch. Host only. */
+int ftmoe_ffn_kernels_for(ftmoe_cache_t *cache, int32_t bs, int32_t topk, int32_t *kind);
 
 /* Read the state into host arrays h_owner[S] (flat id or -1), h_stamp[S], *h_clock.
  * Synchronises the stream. */

@@ -310,8 +310,19 @@ def test_bf16_ffn_kernel_families(geo):
 
 
 def test_ffn_kernel_selector_formats():
-    """ROWS / MMA only on bf16 caches; MMA only where the shape has the tensor-core pipeline."""
+    """ROWS / MMA only on bf16 caches; MMA only where the shape has the tensor-core pipeline;
+    the AUTO choice as reported by ftmoe_ffn_kernels_for."""
+    c2 = ExpertSlotCache(wl.scaled(wl.CONFIGS["c2"], E=16, L=1, S=16), 128)
+    kinds = {bs: F.ftmoe_ffn_kernels_for(c2.handle, bs, 8) for bs in (1, 2, 3, 4, 8)}
+    # E = 16: ROWS for 4 <= 8 bs < 32 routed pairs (about one per expert), MMA otherwise
+    assert kinds == {1: F.FFN_ROWS, 2: F.FFN_ROWS, 3: F.FFN_ROWS, 4: F.FFN_MMA, 8: F.FFN_MMA}, kinds
+    c2.set_ffn_kernels(F.FFN_MMA)
+    assert F.ftmoe_ffn_kernels_for(c2.handle, 2, 8) == F.FFN_MMA
+    c2.set_ffn_kernels(F.FFN_ROWS)
+    assert F.ftmoe_ffn_kernels_for(c2.handle, 8, 8) == F.FFN_ROWS
+    c2.close()
     c1 = ExpertSlotCache(wl.CONFIGS["c1"], 8)  # I = 128: no tensor-core pipeline
+    assert F.ftmoe_ffn_kernels_for(c1.handle, 8, 1) == F.FFN_ROWS
     c1.set_ffn_kernels(F.FFN_ROWS)
     c1.set_ffn_kernels(F.FFN_AUTO)
     with pytest.raises(F.FtmoeError) as ei:

@@ -50,6 +50,11 @@ def test_workspace_bytes_and_host_checks(lib):
     with pytest.raises(F.FtmoeError) as e:
         F.ftmoe_cache_workspace_bytes(F.FMT_RAW, 1, 8, 2, 9000, 0, 0, 0)
     assert e.value.code == F.ERR_INVALID_ARG
+    # the FFN kernel selector and its query check their handle before anything else
+    for call in (lambda: F.ftmoe_set_ffn_kernels(0, F.FFN_MMA), lambda: F.ftmoe_ffn_kernels_for(0, 4, 8)):
+        with pytest.raises(F.FtmoeError) as e:
+            call()
+        assert e.value.code == F.ERR_INVALID_ARG
 
 
 def test_create_rejects_schema_mismatch_before_any_cuda_call(lib):
