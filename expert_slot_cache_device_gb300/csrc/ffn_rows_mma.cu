@@ -139,6 +139,46 @@ __device__ __forceinline__ void f8_stage_mma(const unsigned char *st, const F8Cf
     }
 }
 
+// Block-FP8 down: warp kp takes k [32 kp, 32 kp + 32) of the stage (two k steps, inside one
+// 128-k scale block) for all four M tiles, so the fp32 -> f16 conversion of each token's h
+// pair is done once per stage instead of once per M tile.
+__device__ __forceinline__ void f8_stage_mma_kp16(const unsigned char *st, const F8Cfg &c, int kp, int ntok,
+                                                  float tok_scale, int kb_first, float (&acc)[4][4]) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
+    const unsigned char *tokp = st + c.tok_off + g * c.tok_stride;
+    const int box = kp >> 2, inbox = 32 * (kp & 3);
+    const unsigned char *tile = st + box * (kFRows * kFBox);
+    float tmp[4][4];
+#pragma unroll
+    for (int ks = 0; ks < 2; ks++) {
+        const int kk = 32 * kp + 16 * ks;            // k of this step inside the stage
+        const int byte = inbox + 16 * ks + 4 * tig;  // inside the 128-byte box row
+        uint32_t b0 = 0u, b1 = 0u;
+        if (g < ntok) {
+            const float4 hv = *reinterpret_cast<const float4 *>(tokp + 4 * (kk + 4 * tig));
+            b0 = f2_scale_to_h2(hv.x, hv.y, tok_scale);
+            b1 = f2_scale_to_h2(hv.z, hv.w, tok_scale);
+        }
+#pragma unroll
+        for (int mt = 0; mt < 4; mt++) {
+            const uint32_t wA = *reinterpret_cast<const uint32_t *>(tile + swz(16 * mt + g, byte));
+            const uint32_t wB = *reinterpret_cast<const uint32_t *>(tile + swz(16 * mt + g + 8, byte));
+            const uint32_t a0 = e4m3x2_h2(wA & 0xffffu), a2 = e4m3x2_h2(wA >> 16);
+            const uint32_t a1 = e4m3x2_h2(wB & 0xffffu), a3 = e4m3x2_h2(wB >> 16);
+            if (ks == 0)
+                mma_f16_16816_z(tmp[mt], a0, a1, a2, a3, b0, b1);
+            else
+                mma_f16_16816(tmp[mt], a0, a1, a2, a3, b0, b1);
+        }
+    }
+    const float s = reinterpret_cast<const float *>(st + c.sc_off)[kb_first + box];
+#pragma unroll
+    for (int mt = 0; mt < 4; mt++) {
+        ffma2_s(acc[mt][0], acc[mt][1], tmp[mt][0], tmp[mt][1], s);
+        ffma2_s(acc[mt][2], acc[mt][3], tmp[mt][2], tmp[mt][3], s);
+    }
+}
+
 // bf16: box kq of the stage (64 k in four k steps) for M tile mt of every matrix. Down runs
 // the hi and the lo term of h through the same A fragment.
 template <int NM, bool DOWN>
@@ -348,12 +388,15 @@ __device__ __forceinline__ void rows_mma_body(const FfnParams &p, const F8Cfg &c
         return;
     }
 
-    // consumers: warp = (M tile mt, box kq)
+    // consumers: warp = (M tile mt, box kq); block-FP8 down: warp = sixteenth kp of the
+    // stage's k over all four M tiles (acc[a]: matrix a, or M tile a for block-FP8 down)
+    constexpr bool KP16 = WK == kWE4M3 && PHASE == kDN;
+    constexpr int NA = KP16 ? 4 : NM, NPART = KP16 ? 16 : 4;
     const int mt = warp & 3, kq = warp >> 2;
     const int g = lane >> 2, tig = lane & 3;
-    float acc[NM][4];
+    float acc[NA][4];
 #pragma unroll
-    for (int m = 0; m < NM; m++)
+    for (int m = 0; m < NA; m++)
 #pragma unroll
         for (int i = 0; i < 4; i++) acc[m][i] = 0.f;
     uint32_t rphase = 0;
@@ -368,7 +411,10 @@ __device__ __forceinline__ void rows_mma_body(const FfnParams &p, const F8Cfg &c
         const int ntok = hs.ntok;
         const bool last = hs.last;
         const unsigned char *st = stage0 + (size_t)s * c.stage_bytes;
-        if (WK == kWE4M3) {
+        if constexpr (KP16) {
+            const float tok_scale = g < ntok ? ldexpf(1.f, -hs.texp[g]) : 0.f;
+            f8_stage_mma_kp16(st, c, warp, ntok, tok_scale, hs.kstage * (kFKs / 128), acc);
+        } else if constexpr (WK == kWE4M3) {
             const float tok_scale = g < ntok ? ldexpf(1.f, -hs.texp[g]) : 0.f;
             f8_stage_mma<NM, PHASE == kDN>(st, c, mt, kq, ntok, tok_scale, hs.kstage * (kFKs / 128), acc);
         } else {
@@ -380,22 +426,23 @@ __device__ __forceinline__ void rows_mma_body(const FfnParams &p, const F8Cfg &c
             continue;
         }
 
-        // item end: partials meet in red [NM][4 boxes][kFTok][kRedStride] (the padded row
+        // item end: partials meet in red [NM][NPART][kFTok][kRedStride] (the padded row
         // keeps both the fragment stores and the row-wise sums free of bank conflicts)
 #pragma unroll
-        for (int m = 0; m < NM; m++) {
-            float *r = red + ((m * 4 + kq) * kFTok) * kRedStride;
-            const int r0 = 16 * mt + g, t0 = 2 * tig;
+        for (int a = 0; a < NA; a++) {
+            const int m = KP16 ? 0 : a, part = KP16 ? warp : kq, mta = KP16 ? a : mt;
+            float *r = red + ((m * NPART + part) * kFTok) * kRedStride;
+            const int r0 = 16 * mta + g, t0 = 2 * tig;
             if (t0 < ntok) {
-                r[t0 * kRedStride + r0] = acc[m][0];
-                r[t0 * kRedStride + r0 + 8] = acc[m][2];
+                r[t0 * kRedStride + r0] = acc[a][0];
+                r[t0 * kRedStride + r0 + 8] = acc[a][2];
             }
             if (t0 + 1 < ntok) {
-                r[(t0 + 1) * kRedStride + r0] = acc[m][1];
-                r[(t0 + 1) * kRedStride + r0 + 8] = acc[m][3];
+                r[(t0 + 1) * kRedStride + r0] = acc[a][1];
+                r[(t0 + 1) * kRedStride + r0 + 8] = acc[a][3];
             }
 #pragma unroll
-            for (int i = 0; i < 4; i++) acc[m][i] = 0.f;
+            for (int i = 0; i < 4; i++) acc[a][i] = 0.f;
         }
         __syncwarp();
         if (lane == 0) bar_arrive(&rbar[0]);
@@ -418,7 +465,7 @@ __device__ __forceinline__ void rows_mma_body(const FfnParams &p, const F8Cfg &c
             for (int m = 0; m < NM; m++) {
                 float sum = 0.f;
 #pragma unroll
-                for (int q4 = 0; q4 < 4; q4++) sum += red[((m * 4 + q4) * kFTok + t) * kRedStride + row];
+                for (int q4 = 0; q4 < NPART; q4++) sum += red[((m * NPART + q4) * kFTok + t) * kRedStride + row];
                 v[m] = sum * xs_t;
             }
             rows_mma_store<WK, PHASE, NM>(p, q_t, n0 + row, v, lane);
@@ -466,7 +513,8 @@ bool make_f8_cfg(const FfnParams &p, int wk, int phase, F8Cfg &c, size_t &smem) 
     const int planes = c.tok_plane ? 2 : 1;
     c.tok_off = (c.sc_off + NM * c.sc_bytes + 15) & ~15;
     c.stage_bytes = (c.tok_off + planes * kFTok * c.tok_stride + 1023) & ~1023;
-    const size_t red = (size_t)NM * 4 * kFTok * kRedStride * 4;
+    const int npart = wk == kWE4M3 && phase == kDN ? 16 : 4;  // partial sums per output
+    const size_t red = (size_t)NM * npart * kFTok * kRedStride * 4;
     const size_t head = 256 + kFStagesMax * sizeof(F8Hdr) + 1024;  // + alignment slack
     const size_t cap = 227 * 1024;
     int stages = kFStagesMax;
