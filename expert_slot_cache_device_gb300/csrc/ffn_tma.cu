@@ -10,9 +10,10 @@
 // weight rows (gate and up rows of R neurons, or R down rows, plus the nvfp4 block
 // scales) and the token vectors the item needs (bf16 activations for gate_up, fp32
 // h rows for down). It also writes a small stage header (slot, rows, tokens). Eight
-// consumer warps wait on the stage's mbarrier, compute from shared memory (a warp
-// per row, lanes over 16-byte chunks, warp-shuffle reductions, fp32 accumulation,
-// nvfp4 decoded in registers) and release the stage. Several stages stay in flight
+// consumer warps (sixteen for nvfp4 down) wait on the stage's mbarrier, compute from
+// shared memory (a warp per row, or per group of four rows in down, lanes over 16-byte
+// chunks, warp-shuffle reductions, fp32 accumulation, nvfp4 and Q4_0 decoded in
+// registers) and release the stage. Several stages stay in flight
 // per SM, so the HBM stream never waits on a CTA's start-up latency; weight copies
 // carry an L2 evict-first policy because they are read once.
 //
@@ -31,14 +32,21 @@ namespace {
 
 using namespace ffn;
 
-constexpr int kConsumerWarps = 8;
-constexpr int kProducerWarp = kConsumerWarps;
-constexpr int kTmaThreads = (kConsumerWarps + 1) * 32;
+enum { kGateUp = 0, kDown = 1 };
+
+// Consumer warps per CTA (the producer warp comes after them). nvfp4 down has 16: its
+// consumers are bound by instruction latency (one group of four rows per warp and stage at
+// 64-row items) and its registers fit a 544-thread CTA; the other kernels keep 8, either
+// bound by the weight stream (bf16) or by registers (Q4_0 down) or by the rows one stage
+// holds (gate_up: a warp per neuron).
+constexpr int kDnWarpsNvfp4 = 16;
+template <int FMT, int PHASE>
+constexpr int kConsumerWarps = FMT == FTMOE_FMT_NVFP4 && PHASE == kDown ? kDnWarpsNvfp4 : 8;
+template <int FMT, int PHASE>
+constexpr int kTmaThreads = (kConsumerWarps<FMT, PHASE> + 1) * 32;
 constexpr int kMaxStages = 4;
 constexpr int kMaxTok = 4;  // tokens per stage
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any healthy wait
-
-enum { kGateUp = 0, kDown = 1 };
 
 struct StageHdr {
     int32_t slot, n0, rows, ntok, done, pad0, pad1, pad2;
@@ -177,7 +185,7 @@ __device__ __forceinline__ void gu_consume(const FfnParams &p, const TmaCfg &c, 
     const int64_t wr = Seg<FMT, kGateUp>::wrow(H, I), sr = Seg<FMT, kGateUp>::srow(H, I);
     const uint4 *xs = reinterpret_cast<const uint4 *>(st + c.tok_off);
     const int nxv = H >> 3;  // 16-byte vectors per token (8 bf16)
-    for (int j = warp; j < h.rows; j += kConsumerWarps) {
+    for (int j = warp; j < h.rows; j += kConsumerWarps<FMT, kGateUp>) {
         const int n = h.n0 + j;
         float g[NT], u[NT];
 #pragma unroll
@@ -289,7 +297,7 @@ __device__ __forceinline__ void dn_consume(const FfnParams &p, const TmaCfg &c, 
     const float4 *hs = reinterpret_cast<const float4 *>(st + c.tok_off);
     const int nh4 = I >> 2;
     constexpr int RR = 4;  // rows sharing each h read
-    for (int j0 = warp * RR; j0 < h.rows; j0 += kConsumerWarps * RR) {
+    for (int j0 = warp * RR; j0 < h.rows; j0 += kConsumerWarps<FMT, kDown> * RR) {
         const int nr = h.rows - j0 < RR ? h.rows - j0 : RR;
         float o[RR][NT];
 #pragma unroll
@@ -416,7 +424,7 @@ __device__ __forceinline__ void dn_consume(const FfnParams &p, const TmaCfg &c, 
 // ---------------------------------------------------------------- kernel
 
 template <int FMT, int PHASE>
-__global__ void __launch_bounds__(kTmaThreads, 1) ffn_rows_tma_kernel(FfnParams p, TmaCfg c) {
+__global__ void __launch_bounds__(kTmaThreads<FMT, PHASE>, 1) ffn_rows_tma_kernel(FfnParams p, TmaCfg c) {
     extern __shared__ __align__(128) unsigned char sm[];
     uint64_t *full = reinterpret_cast<uint64_t *>(sm);
     uint64_t *empty = full + kMaxStages;
@@ -427,7 +435,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) ffn_rows_tma_kernel(FfnParams 
     if (threadIdx.x == 0) {
         for (int s = 0; s < c.stages; s++) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps);
+            mbar_init(&empty[s], kConsumerWarps<FMT, PHASE>);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -435,7 +443,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) ffn_rows_tma_kernel(FfnParams 
     if (PHASE == kGateUp) griddep_wait();  // routing tables come from the previous kernel
     griddep_launch();
 
-    if (warp == kProducerWarp) {
+    if (warp == kConsumerWarps<FMT, PHASE>) {  // producer
         if (lane != 0) return;
         // Work items blockIdx.x, blockIdx.x + gridDim.x, ... of this CTA: dealt round-robin,
         // the CTAs hold neighbouring tiles and the passes of one expert at the same time,
@@ -595,7 +603,7 @@ bool make_cfg(const FfnParams &p, TmaCfg &c) {
     const int rmax = PHASE == kGateUp ? 16 : 64;
     // Prefer enough rows per item to keep all consumer warps busy (gate_up: one neuron per
     // warp; down: four rows per warp), then as many token slots as fit.
-    const int rmin_busy = PHASE == kGateUp ? kConsumerWarps : 4 * kConsumerWarps;
+    const int rmin_busy = PHASE == kGateUp ? kConsumerWarps<FMT, PHASE> : 4 * kConsumerWarps<FMT, PHASE>;
     for (int pass = 0; pass < 2; pass++) {
         for (int tg = kMaxTok; tg >= 1; tg >>= 1) {
             // nvfp4 items stage their per-row f16 globals with bulk copies of 2R bytes: R >= 8
@@ -629,7 +637,7 @@ cudaError_t launch_one(const FfnParams &p, int num_sms, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_sms);
-    cfg.blockDim = dim3(kTmaThreads);
+    cfg.blockDim = dim3(kTmaThreads<FMT, PHASE>);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
