@@ -53,6 +53,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-hybrid", action="store_true", help="skip the hybrid-path measurements")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill-pipeline measurements")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay measurement")
     ap.add_argument("--copy-mode", default="fused", choices=["fused", "per_bank", "engine"])
     ap.add_argument("--ffn-kernels", default="auto", choices=["auto", "rows", "mma"],
                     help="FFN kernel family of bf16 layers (auto: chosen per call)")
@@ -478,6 +479,8 @@ def run_gpu(args):
             line["hybrid"] = hybrid_probe(args, cfg, cache, stream, torch, F, wl, link, cpu_cores())
         if not args.no_prefill:
             line["prefill"] = prefill_probe(cfg, cache, torch, F)
+        if not args.no_graph:
+            line["graph"] = graph_probe(cfg, cache, torch, F, wl)
     cache.close()
     if rank == 0 and not args.no_cpu_baseline:
         hb = [cache.host[b][0].numpy() for b in range(cache.nb)]
@@ -498,6 +501,56 @@ def run_gpu(args):
 
 PREFILL_BS = 64      # tokens of the prefill batch of the pipeline probe
 PREFILL_LAYERS = 6   # layers streamed by the probe
+
+
+def graph_probe(cfg, cache, torch, F, wl, bs=1, calls=None, reps=20):
+    """Decode calls at batch `bs` with every routed expert resident (the prepared state of
+    miss rate 0), one call = ensure + copy_missing + FFN of one layer: `calls` calls issued
+    one by one against the same calls captured once in a CUDA graph and replayed (what a
+    serving loop does per token, rewriting the id / weight / activation buffers in place).
+    Median over `reps` runs of the device time per call (CUDA events, warm L2: the resident
+    experts' weights, bs * topk * B bytes, may partly stay in L2 between calls)."""
+    calls = calls or cfg.L
+    r = wl.make_route(cfg, bs, 0.0)
+    d_ids = torch.from_numpy(r.topk_ids).cuda()
+    d_w = torch.from_numpy(r.weights).cuda()
+    d_x = torch.from_numpy(r.x.view(np.int16).copy()).view(torch.bfloat16).cuda()
+    d_slots = torch.empty_like(d_ids)
+    d_y = torch.empty((bs, cfg.H), dtype=torch.bfloat16, device="cuda")
+    st = torch.cuda.Stream()
+
+    def run():
+        for _ in range(calls):
+            cache.ensure(0, d_ids, d_slots, stream=st)
+            cache.copy_missing(stream=st)
+            cache.ffn(d_x, d_slots, d_w, d_y, stream=st)
+
+    def timed(fn):
+        out = []
+        for _ in range(reps):
+            cache.set_state(r.owner, r.stamp, r.clock, stream=st)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            with torch.cuda.stream(st):  # a graph replays on the current stream
+                fn()
+            b.record(st)
+            b.synchronize()
+            out.append(a.elapsed_time(b) * 1e3 / calls)
+        return statistics.median(out)
+
+    cache.set_state(r.owner, r.stamp, r.clock, stream=st)
+    run()
+    torch.cuda.synchronize()
+    eager = timed(run)
+    g = torch.cuda.CUDAGraph()
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=st, capture_error_mode="thread_local"):
+        run()
+    replay = timed(g.replay)
+    assert cache.status() == F.OK
+    del g
+    return {"bs": bs, "calls": calls, "misses_per_call": 0, "eager_us_per_call": eager,
+            "graph_us_per_call": replay, "speedup": eager / replay if replay > 0 else None}
 
 
 def prefill_probe(cfg, cache, torch, F):

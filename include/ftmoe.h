@@ -36,6 +36,12 @@
  *     leave the cache state untouched, make the kernel write nothing else, and
  *     are recorded in a sticky device status word read by
  *     ftmoe_get_device_status. No kernel traps, asserts or spin-waits.
+ *   - ftmoe_ensure_experts, ftmoe_copy_missing (FTMOE_COPY_FUSED / PER_BANK) and
+ *     ftmoe_expert_ffn only enqueue kernels, so a sequence of them can be captured
+ *     into a CUDA graph (stream capture) and replayed: the graph reads the id, weight
+ *     and activation buffers and the cache tables at replay time. Calls that read
+ *     back to the host (FTMOE_COPY_ENGINE, the get_* and measure_* entry points)
+ *     cannot be captured.
  */
 #ifndef FTMOE_H
 #define FTMOE_H
