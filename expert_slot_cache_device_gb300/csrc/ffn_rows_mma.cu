@@ -21,7 +21,8 @@
 //
 // The contraction runs on mma.sync m16n8k16 with fp32 accumulators: M = 16 output rows,
 // N = 8 tokens, K = 16. Consumer warp w takes M tile w % 4 (rows 16 (w % 4) ..) and box
-// w / 4 of every stage.
+// w / 4 of every stage (block-FP8 down: k sixteenth w of the stage over all four M tiles, so
+// the h pairs are converted to f16 once per stage).
 //   block FP8 (f16 x f16): lane (g, tig) reads the 32-bit word at k = 4 tig of rows g and
 //   g + 8 of the k step; with cvt.rn.f16x2.e4m3x2 (exact) its low half gives the fragment
 //   registers of logical k (2 tig, 2 tig + 1) and its high half those of (2 tig + 8,
@@ -92,9 +93,11 @@ __device__ __forceinline__ int swz(int row, int byte) { return row * kFBox + (by
 // Two e4m3 codes (low byte first) -> f16x2 (exact).
 __device__ __forceinline__ uint32_t e4m3x2_h2(uint32_t two) { return e4m3x2_to_h2(two); }
 
-template <int NM, bool DOWN>
+// Block-FP8 gate_up: box kq of the stage (128 k, one scale block) for M tile mt of both
+// matrices; the B fragment is the token's f16 activations.
+template <int NM>
 __device__ __forceinline__ void f8_stage_mma(const unsigned char *st, const F8Cfg &c, int mt, int kq, int ntok,
-                                             float tok_scale, int kb_first, float (&acc)[NM][4]) {
+                                             int kb_first, float (&acc)[NM][4]) {
     constexpr int KS = kfks<kWE4M3>();
     constexpr int KW = KS / 4;  // k of this warp in the stage: one 128-k scale block
     const int lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
@@ -107,15 +110,9 @@ __device__ __forceinline__ void f8_stage_mma(const unsigned char *st, const F8Cf
         const int byte = inbox + 16 * ks + 4 * tig;  // inside the 128-byte box row
         uint32_t b0 = 0u, b1 = 0u;
         if (g < ntok) {
-            if (DOWN) {
-                const float4 hv = *reinterpret_cast<const float4 *>(tokp + 4 * (kk + 4 * tig));
-                b0 = f2_scale_to_h2(hv.x, hv.y, tok_scale);
-                b1 = f2_scale_to_h2(hv.z, hv.w, tok_scale);
-            } else {
-                const uint2 xv = *reinterpret_cast<const uint2 *>(tokp + 2 * (kk + 4 * tig));
-                b0 = xv.x;
-                b1 = xv.y;
-            }
+            const uint2 xv = *reinterpret_cast<const uint2 *>(tokp + 2 * (kk + 4 * tig));
+            b0 = xv.x;
+            b1 = xv.y;
         }
 #pragma unroll
         for (int m = 0; m < NM; m++) {
@@ -415,8 +412,7 @@ __device__ __forceinline__ void rows_mma_body(const FfnParams &p, const F8Cfg &c
             const float tok_scale = g < ntok ? ldexpf(1.f, -hs.texp[g]) : 0.f;
             f8_stage_mma_kp16(st, c, warp, ntok, tok_scale, hs.kstage * (kFKs / 128), acc);
         } else if constexpr (WK == kWE4M3) {
-            const float tok_scale = g < ntok ? ldexpf(1.f, -hs.texp[g]) : 0.f;
-            f8_stage_mma<NM, PHASE == kDN>(st, c, mt, kq, ntok, tok_scale, hs.kstage * (kFKs / 128), acc);
+            f8_stage_mma<NM>(st, c, mt, kq, ntok, hs.kstage * (kFKs / 128), acc);
         } else {
             bf_stage_mma<NM, PHASE == kDN>(st, c, mt, kq, ntok, acc);
         }
