@@ -56,6 +56,11 @@ __device__ __forceinline__ void copy_tile(unsigned char *dst, const unsigned cha
 
 template <bool VEC>
 __global__ void __launch_bounds__(kCopyThreads) copy_missing_kernel(CopyParams p) {
+    // launched as a programmatic dependent of ensure_experts: the CTAs become resident while
+    // it runs and wait here until its miss list is complete and visible; the FFN's routing
+    // kernel may in turn launch early behind this grid
+    asm volatile("griddepcontrol.launch_dependents;" :::);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int m = *p.num_miss;
     const int64_t tpe = p.tile0[p.nb];  // tiles per expert over all banks
     const int64_t total = (int64_t)m * tpe;
@@ -87,11 +92,17 @@ __global__ void __launch_bounds__(kCopyThreads) linear_copy_kernel(unsigned char
 }  // namespace
 
 cudaError_t launch_copy(const CopyParams &p, bool vec16, int grid, cudaStream_t st) {
-    if (vec16)
-        copy_missing_kernel<true><<<grid, kCopyThreads, 0, st>>>(p);
-    else
-        copy_missing_kernel<false><<<grid, kCopyThreads, 0, st>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kCopyThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return vec16 ? cudaLaunchKernelEx(&cfg, copy_missing_kernel<true>, p)
+                 : cudaLaunchKernelEx(&cfg, copy_missing_kernel<false>, p);
 }
 
 cudaError_t launch_linear_copy(unsigned char *dst, const unsigned char *src, int64_t bytes, bool vec16, int grid,

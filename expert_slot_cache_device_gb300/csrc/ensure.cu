@@ -115,6 +115,9 @@ __global__ void __launch_bounds__(kThreads) ensure_kernel(EnsureParams p) {
 
     const int tid = threadIdx.x, nt = blockDim.x;
     const int E = p.E, S = p.S;
+    // the copy kernel behind this one may become resident now; it waits for this grid to
+    // finish before it reads the miss list
+    asm volatile("griddepcontrol.launch_dependents;" :::);
     // Prologue: issue every independent global load before the first use, so the
     // call pays about one memory latency instead of one per step.
     const int32_t *row = p.t.id2slot + (int64_t)p.layer * E;

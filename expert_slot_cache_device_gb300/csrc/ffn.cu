@@ -85,6 +85,9 @@ __global__ void __launch_bounds__(1024) ffn_route_kernel(FfnParams p) {
     __shared__ float s_wmax[32];
     const int tid = threadIdx.x, nt = blockDim.x;
     asm volatile("griddepcontrol.launch_dependents;" :::);
+    // launched as a programmatic dependent of the previous kernel (the copy of the missed
+    // experts, whose bytes the FFN reads): wait for it before reading slots or x
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (blockIdx.x > 0) {
         const int t = blockIdx.x - 1;
         const uint16_t *xr = p.x + (int64_t)t * p.H;
@@ -763,8 +766,19 @@ cudaError_t launch_ffn(const FfnParams &p_in, int num_sms, cudaStream_t st, cons
     p.x16_emax = p.fmt == FTMOE_FMT_MXFP4 ? 9 : (p.fmt == FTMOE_FMT_Q4_0 ? 8 : 10);
     p.x16_swz = fp4_rows_tma && p.fmt == FTMOE_FMT_NVFP4 ? 1 : (fp4_rows_tma && p.fmt == FTMOE_FMT_Q4_0 ? 2 : 0);
     p.pass_tokens = (mx_tma || fp8_tma || bf16_mma) ? kMxPassTokens : kPassTokens;
-    ffn_route_kernel<<<1 + (want_x16 ? p.bs : 0), 1024, route_smem, st>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1 + (want_x16 ? p.bs : 0));
+        cfg.blockDim = dim3(1024);
+        cfg.dynamicSmemBytes = route_smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if ((e = cudaLaunchKernelEx(&cfg, ffn_route_kernel, p)) != cudaSuccess) return e;
+    }
 
     const int umax = p.P < p.S ? p.P : p.S;  // distinct slots at most
     const size_t budget = 64 * 1024;
