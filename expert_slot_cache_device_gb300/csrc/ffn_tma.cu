@@ -34,14 +34,14 @@ using namespace ffn;
 
 enum { kGateUp = 0, kDown = 1 };
 
-// Consumer warps per CTA (the producer warp comes after them). nvfp4 down has 16: its
-// consumers are bound by instruction latency (one group of four rows per warp and stage at
-// 64-row items) and its registers fit a 544-thread CTA; the other kernels keep 8, either
-// bound by the weight stream (bf16) or by registers (Q4_0 down) or by the rows one stage
-// holds (gate_up: a warp per neuron).
+// Consumer warps per CTA (the producer warp comes after them). nvfp4 and bf16 down have 16:
+// their consumers are bound by instruction latency (one group of four rows per warp and
+// stage at 64-row items) and their registers fit a 544-thread CTA; the other kernels keep
+// 8, bound by registers (Q4_0 down) or by the rows one stage holds (gate_up: a warp per
+// neuron).
 constexpr int kDnWarpsNvfp4 = 16;
 template <int FMT, int PHASE>
-constexpr int kConsumerWarps = FMT == FTMOE_FMT_NVFP4 && PHASE == kDown ? kDnWarpsNvfp4 : 8;
+constexpr int kConsumerWarps = (FMT == FTMOE_FMT_NVFP4 || FMT == FTMOE_FMT_BF16) && PHASE == kDown ? kDnWarpsNvfp4 : 8;
 template <int FMT, int PHASE>
 constexpr int kTmaThreads = (kConsumerWarps<FMT, PHASE> + 1) * 32;
 constexpr int kMaxStages = 4;
@@ -610,7 +610,9 @@ bool make_cfg(const FfnParams &p, TmaCfg &c) {
             const int rmin = pass == 0 ? rmin_busy : (FMT == FTMOE_FMT_NVFP4 ? 8 : 1);
             for (int R = rmax; R >= rmin; R >>= 1) {
                 const int64_t wb = Seg<FMT, PHASE>::bytes(R, H, I);
-                if (wb > 80 * 1024) continue;
+                // weight bytes per stage: up to 80 KB (three or more stages), 100 KB for bf16
+                // down, whose 64 rows of 2I bytes give two stages of 16 warps x 4 rows
+                if (wb > (FMT == FTMOE_FMT_BF16 && PHASE == kDown ? 100 : 80) * 1024) continue;
                 const int64_t stage = ((wb + 127) & ~(int64_t)127) + (int64_t)tg * c.tok_bytes;
                 const int64_t stages = (int64_t)((kSmemCap - kSmemHeader) / (size_t)stage);
                 if (stages < 2) continue;
