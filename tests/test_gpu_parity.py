@@ -222,12 +222,14 @@ SCALED = [
     ("bf16", dict(E=6, H=1024, I=256, L=2, S=6)),
     ("nvfp4", dict(E=10, H=320, I=96, L=2, S=10)),
     ("nvfp4", dict(E=5, H=2048, I=512, L=2, S=5)),
+    ("nvfp4", dict(E=5, H=768, I=256, L=2, S=5)),   # gate_up rows whole in one stage
     ("mxfp4", dict(E=9, H=160, I=96, L=2, S=9)),
     ("mxfp4", dict(E=5, H=576, I=320, L=2, S=5)),
     ("fp8", dict(E=6, H=512, I=512, L=2, S=6)),
     ("fp8", dict(E=5, H=1024, I=1536, L=2, S=5)),
     ("q4_0", dict(E=6, H=512, I=256, L=2, S=6)),
     ("q4_0", dict(E=5, H=1024, I=768, L=2, S=5)),
+    ("q4_0", dict(E=5, H=768, I=512, L=2, S=5)),    # gate_up rows whole in one stage
 ]
 
 
