@@ -34,14 +34,15 @@ using namespace ffn;
 
 enum { kGateUp = 0, kDown = 1 };
 
-// Consumer warps per CTA (the producer warp comes after them). nvfp4 and bf16 down have 16:
-// their consumers are bound by instruction latency (one group of four rows per warp and
-// stage at 64-row items) and their registers fit a 544-thread CTA; the other kernels keep
-// 8, bound by registers (Q4_0 down) or by the rows one stage holds (gate_up: a warp per
-// neuron).
-constexpr int kDnWarpsNvfp4 = 16;
+// Consumer warps per CTA (the producer warp comes after them). Down has 16: its consumers are
+// bound by instruction latency (one group of kDnRR rows per warp and stage at 64-row items),
+// and with two rows per group Q4_0 fits the registers of a 544-thread CTA too. gate_up keeps
+// 8, bound by the rows one stage holds (a warp per neuron).
 template <int FMT, int PHASE>
-constexpr int kConsumerWarps = (FMT == FTMOE_FMT_NVFP4 || FMT == FTMOE_FMT_BF16) && PHASE == kDown ? kDnWarpsNvfp4 : 8;
+constexpr int kConsumerWarps = PHASE == kDown ? 16 : 8;
+// down rows sharing each h read (Q4_0: two, so that 16 warps fit the registers)
+template <int FMT>
+constexpr int kDnRR = FMT == FTMOE_FMT_Q4_0 ? 2 : 4;
 template <int FMT, int PHASE>
 constexpr int kTmaThreads = (kConsumerWarps<FMT, PHASE> + 1) * 32;
 constexpr int kMaxStages = 4;
@@ -296,7 +297,7 @@ __device__ __forceinline__ void dn_consume(const FfnParams &p, const TmaCfg &c, 
     const int64_t wr = Seg<FMT, kDown>::wrow(H, I), sr = Seg<FMT, kDown>::srow(H, I);
     const float4 *hs = reinterpret_cast<const float4 *>(st + c.tok_off);
     const int nh4 = I >> 2;
-    constexpr int RR = 4;  // rows sharing each h read
+    constexpr int RR = kDnRR<FMT>;  // rows sharing each h read
     for (int j0 = warp * RR; j0 < h.rows; j0 += kConsumerWarps<FMT, kDown> * RR) {
         const int nr = h.rows - j0 < RR ? h.rows - j0 : RR;
         float o[RR][NT];
@@ -603,7 +604,7 @@ bool make_cfg(const FfnParams &p, TmaCfg &c) {
     const int rmax = PHASE == kGateUp ? 16 : 64;
     // Prefer enough rows per item to keep all consumer warps busy (gate_up: one neuron per
     // warp; down: four rows per warp), then as many token slots as fit.
-    const int rmin_busy = PHASE == kGateUp ? kConsumerWarps<FMT, PHASE> : 4 * kConsumerWarps<FMT, PHASE>;
+    const int rmin_busy = PHASE == kGateUp ? kConsumerWarps<FMT, PHASE> : kDnRR<FMT> * kConsumerWarps<FMT, PHASE>;
     for (int pass = 0; pass < 2; pass++) {
         for (int tg = kMaxTok; tg >= 1; tg >>= 1) {
             // nvfp4 items stage their per-row f16 globals with bulk copies of 2R bytes: R >= 8
