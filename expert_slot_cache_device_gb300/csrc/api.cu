@@ -342,7 +342,8 @@ int ftmoe_set_ffn_kernels(ftmoe_cache_t *c, int32_t kind) {
 
 int ftmoe_ffn_kernels_for(ftmoe_cache_t *c, int32_t bs, int32_t topk, int32_t *kind) {
     if (!c || !kind) return fail(FTMOE_ERR_INVALID_ARG, "NULL argument");
-    if (bs < 0 || topk <= 0) return fail(FTMOE_ERR_INVALID_ARG, "bs=%d, topk=%d", bs, topk);
+    if (bs < 0 || topk <= 0 || (int64_t)bs * topk > FTMOE_MAX_IDS_PER_CALL)
+        return fail(FTMOE_ERR_INVALID_ARG, "bs=%d, topk=%d", bs, topk);
     if (!c->ffn) return fail(FTMOE_ERR_STATE, "the cache was created without FFN scratch");
     FfnParams p;
     memset(&p, 0, sizeof p);

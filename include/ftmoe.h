@@ -331,8 +331,9 @@ int ftmoe_set_ffn_kernels(ftmoe_cache_t *cache, int32_t kind);
 
 /* The kernel family (FTMOE_FFN_ROWS: CUDA cores, FTMOE_FFN_MMA: tensor cores) that
  * ftmoe_expert_ffn on this cache runs for a call of bs tokens x topk experts, under the
- * current ftmoe_set_ffn_kernels choice. FTMOE_ERR_INVALID_ARG for NULL or bs < 0 or
- * topk <= 0; FTMOE_ERR_STATE for a cache created without FFN scratch. Host only. */
+ * current ftmoe_set_ffn_kernels choice. FTMOE_ERR_INVALID_ARG for NULL, bs < 0, topk <= 0
+ * or bs * topk above FTMOE_MAX_IDS_PER_CALL; FTMOE_ERR_STATE for a cache created without
+ * FFN scratch. Host only. */
 int ftmoe_ffn_kernels_for(ftmoe_cache_t *cache, int32_t bs, int32_t topk, int32_t *kind);
 
 /* Read the state into host arrays h_owner[S] (flat id or -1), h_stamp[S], *h_clock.
