@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     extern __shared__ __align__(1024) unsigned char sm[];
     uint64_t *full = reinterpret_cast<uint64_t *>(sm);
     uint64_t *empty = full + kMxStagesMax;
-    uint64_t *rbar = empty + kMxStagesMax;  // [2] consumer barriers around the reduction
+    uint64_t *rbar = empty + kMxStagesMax;  // [3] consumer barriers around the reduction
     MxHdr *hdr = reinterpret_cast<MxHdr *>(sm + 256);
     // stages start at the first 1024-byte aligned shared address after the headers (the
     // 128-byte swizzle pattern of the code tiles repeats every 1024 bytes)
@@ -169,6 +169,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         }
         bar_init(&rbar[0], kCW);
         bar_init(&rbar[1], kCW);
+        bar_init(&rbar[2], kCW);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -321,13 +322,25 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             continue;
         }
 
-        // item end: the warps' partials meet in red [NM][kBlkPairs][kMxTokMax][kCols]
+        // item end: the warps' partials meet in red [NM][kBlkPairs][kMxTokMax][kCols]. Down
+        // puts them over the last stage's code tile (the same 32 KB), once every warp is done
+        // reading it, which leaves the shared memory for a fourth stage.
+        float *red_i = red;
+        if (PHASE == kDN) {
+            __syncwarp();
+            if (lane == 0) bar_arrive(&rbar[2]);
+            if (!bar_wait(&rbar[2], rphase)) {
+                if (lane == 0) atomicCAS(p.status, 0, FTMOE_ERR_STATE);
+                return;
+            }
+            red_i = reinterpret_cast<float *>(stage0 + (size_t)s * c.stage_bytes);
+        }
 #pragma unroll
         for (int m = 0; m < NM; m++)
 #pragma unroll
             for (int j = 0; j < 4; j++) {
                 const int col = 32 * (2 * hf + (j >> 1)) + 4 * g + 2 * (j & 1);
-                float *r = red + ((m * kBlkPairs + bp) * kMxTokMax) * kCols;
+                float *r = red_i + ((m * kBlkPairs + bp) * kMxTokMax) * kCols;
                 const int t0 = 2 * tig, t1 = 2 * tig + 1;
                 if (t0 < ntok) {
                     r[t0 * kCols + col] = acc[m][j][0];
@@ -362,7 +375,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             for (int m = 0; m < NM; m++) {
                 float sum = 0.f;
 #pragma unroll
-                for (int w = 0; w < kBlkPairs; w++) sum += red[((m * kBlkPairs + w) * kMxTokMax + t) * kCols + col];
+                for (int w = 0; w < kBlkPairs; w++) sum += red_i[((m * kBlkPairs + w) * kMxTokMax + t) * kCols + col];
                 v[m] = sum * xs_t;
             }
             const int q = hs.pairs[t];
@@ -407,7 +420,9 @@ bool make_mx_cfg(const FfnParams &p, int phase, MxCfg &c, size_t &smem) {
     c.tok_off = c.sc_off + NM * (kKp / 16) * kCols;
     c.bias_off = c.tok_off + c.tg * c.tok_stride;
     c.stage_bytes = (c.bias_off + NM * kCols * 2 + 1023) & ~1023;
-    const size_t red = (size_t)NM * kBlkPairs * kMxTokMax * kCols * 4;
+    // down's reduction reuses the last stage's code tile (NM * kKp * kCols bytes)
+    static_assert(kBlkPairs * kMxTokMax * kCols * 4 == kKp * kCols, "down partials fill one code tile");
+    const size_t red = phase == kDN ? 0 : (size_t)NM * kBlkPairs * kMxTokMax * kCols * 4;
     const size_t head = 256 + kMxStagesMax * sizeof(MxHdr) + 1024;  // + alignment slack
     const size_t cap = 227 * 1024;
     int stages = kMxStagesMax;
