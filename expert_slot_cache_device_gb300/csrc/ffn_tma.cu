@@ -1,21 +1,21 @@
-// Row-major expert FFN phases (bf16 and nvfp4 banks) as a persistent,
-// warp-specialised bulk-copy pipeline.
+// Row-major expert FFN phases (bf16, nvfp4 and GGUF Q4_0 banks) on the CUDA cores, as a
+// persistent, warp-specialised bulk-copy pipeline.
 //
 // Decode batches make the FFN a grouped GEMV that must stream every used expert's
 // weights from HBM exactly once. Work items (pass of a distinct slot u, tile of R output
 // rows) are dealt round-robin over the CTAs, so at any moment the CTAs read neighbouring
 // rows and the passes of one hot expert side by side (its second pass hits L2). One
-// producer thread fills a ring of shared-memory stages with 1-D bulk
-// asynchronous copies (cp.async.bulk, completion counted on an mbarrier): the item's
-// weight rows (gate and up rows of R neurons, or R down rows, plus the nvfp4 block
-// scales) and the token vectors the item needs (bf16 activations for gate_up, fp32
-// h rows for down). It also writes a small stage header (slot, rows, tokens). Eight
-// consumer warps (sixteen for nvfp4 down) wait on the stage's mbarrier, compute from
-// shared memory (a warp per row, or per group of four rows in down, lanes over 16-byte
-// chunks, warp-shuffle reductions, fp32 accumulation, nvfp4 and Q4_0 decoded in
-// registers) and release the stage. Several stages stay in flight
-// per SM, so the HBM stream never waits on a CTA's start-up latency; weight copies
-// carry an L2 evict-first policy because they are read once.
+// producer thread fills a ring of shared-memory stages with 1-D bulk asynchronous copies
+// (cp.async.bulk, completion counted on an mbarrier): the item's weight rows (gate and up
+// rows of R neurons, or R down rows, plus the nvfp4 block scales and row globals) and the
+// token vectors the item needs (bf16 activations, or their scaled f16 copy for nvfp4 and
+// Q4_0, for gate_up; fp32 h rows for down). It also writes a small stage header (slot,
+// rows, tokens). The consumer warps (8 for gate_up, 16 for down) wait on the stage's
+// mbarrier, compute from shared memory (a warp per neuron in gate_up, per group of rows in
+// down; lanes over 16-byte chunks or quantisation blocks, warp-shuffle reductions, fp32
+// accumulation, nvfp4 and Q4_0 decoded in registers) and release the stage. Several stages
+// stay in flight per SM, so the HBM stream never waits on a CTA's start-up latency; weight
+// copies carry an L2 evict-first policy because they are read once.
 //
 // The kernels are chained with programmatic dependent launch: gate_up waits for the
 // routing kernel, down's producer starts streaming its weights while gate_up drains
