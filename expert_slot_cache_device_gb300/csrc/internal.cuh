@@ -82,8 +82,8 @@ struct FfnScratch {
 
 // Pipelined FFN kernels split each slot's routed pairs into passes of at most
 // FfnParams::pass_tokens tokens; every (pass, tile) is a separate work item so hot experts
-// spread over the SMs. The row-major kernels use kPassTokens, the transposed mxfp4
-// kernels (tensor-core N = 8) kMxPassTokens.
+// spread over the SMs. The CUDA-core row-major kernels use kPassTokens, the tensor-core
+// kernels (mxfp4, block FP8, bf16; the MMA's N = 8) kMxPassTokens.
 constexpr int kPassTokens = 4;
 constexpr int kMxPassTokens = 8;
 
