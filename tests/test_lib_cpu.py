@@ -87,3 +87,22 @@ def test_null_handles(lib):
             call()
         assert e.value.code == F.ERR_INVALID_ARG
     F.ftmoe_cache_destroy(None)
+
+
+def test_binding_constants_match_the_header():
+    """Every integer constant of the header that the binding names has the same value there."""
+    text = open(HEADER).read()
+    defs = {}
+    for name, val in re.findall(r"^#define FTMOE_([A-Z0-9_]+)\s+\(?(-?\d+)u?\)?", text, flags=re.M):
+        defs[name] = int(val)
+    noalloc = re.search(r"^#define FTMOE_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", text, flags=re.M)
+    defs["NOALLOC_SCRATCH_BYTES"] = int(noalloc.group(1)) << int(noalloc.group(2))
+    checked = 0
+    for name, val in defs.items():
+        if hasattr(F, name):
+            assert getattr(F, name) == val, name
+            checked += 1
+    for family in ("ERR_", "FMT_", "DT_", "COPY_", "FFN_", "BACKEND_"):
+        names = [n for n in defs if n.startswith(family)]
+        assert names and all(hasattr(F, n) for n in names), family
+    assert checked >= 30
