@@ -32,9 +32,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-DEFAULT_CFG = "c2"
-DEFAULT_BS = 16
+DEFAULT_CFG = "c3"   # the largest single-GPU workload: nvfp4 layer, E 256, H 7168, I 2048
+DEFAULT_BS = 32
 DEFAULT_MR = 1.0
+# the other workloads measured in the same run (the `configs` block); the tiny bf16 layer
+# is a parity case only (GPU tests and smoke()), the decode trace has its own summary
+DEFAULT_OTHERS = "c2,c4,c6,c7,c5"
 METRIC = "per-layer expert copy GB/s & tok_ms vs bs/miss_rate; expert FFN us/layer"
 LINK_PROBE_BYTES = 1 << 30
 
@@ -50,6 +53,8 @@ def parse():
     ap.add_argument("--miss-rate", type=float, default=DEFAULT_MR)
     ap.add_argument("--repeat", type=int, default=25, help="repeats per sweep point (median)")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--configs", default=DEFAULT_OTHERS,
+                    help="comma list of other workloads swept in the same run ('none' to skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-hybrid", action="store_true", help="skip the hybrid-path measurements")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill-pipeline measurements")
@@ -158,6 +163,8 @@ TRAFFIC_SOURCES = {
     "copy": ["copy.cu", "internal.cuh"],
     "ffn_rows": ["ffn_tma.cu", "ffn_common.cuh", "internal.cuh"],      # CUDA-core pipelines
     "ffn_mma": ["ffn_rows_mma.cu", "pipeline.cuh", "ffn_common.cuh", "internal.cuh"],  # tensor-core
+    "ffn_mx": ["ffn_mx_tma.cu", "ffn_common.cuh", "internal.cuh"],     # mxfp4 tensor maps
+    "ffn_fp8": ["ffn_rows_mma.cu", "pipeline.cuh", "ffn_common.cuh", "internal.cuh"],  # block FP8
 }
 
 
@@ -172,23 +179,34 @@ def source_hash(kind: str) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str, kind: str):
-    """DRAM bytes (read + write) per launch of `kind` on `workload`, from the `traffic:`
-    lines of profiles/traffic_*.md, or None if none matches the current sources."""
+def recorded_traffic(workload: str, kind: str, units: int = 0):
+    """DRAM bytes (read + write) per launch of `kind` on `workload` ("<name>/bs<bs>/mr<mr>")
+    from the lines of profiles/traffic_*.md, or None if none matches the current sources.
+
+    `traffic: <workload> <kind> <hash> <read> <write>` is a capture of that exact point;
+    `traffic-per-unit: <name> <kind> <hash> <read> <write> <units>` is a capture of a smaller
+    case of the same layer (fewer experts) whose traffic grows in proportion to the units one
+    launch processes (missed experts for the copy, distinct experts for the FFN): it is scaled
+    by `units` / <units>."""
     pdir = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles")
     if not os.path.isdir(pdir):
         return None
     cur = source_hash(kind)
-    for name in sorted(os.listdir(pdir)):
-        if not (name.startswith("traffic_") and name.endswith(".md")):
+    name = workload.split("/")[0]
+    scaled = None
+    for fn in sorted(os.listdir(pdir)):
+        if not (fn.startswith("traffic_") and fn.endswith(".md")):
             continue
-        with open(os.path.join(pdir, name)) as f:
+        with open(os.path.join(pdir, fn)) as f:
             for ln in f:
                 parts = ln.split()
                 if len(parts) == 6 and parts[0] == "traffic:" and parts[1] == workload and parts[2] == kind \
                         and parts[3] == cur:
                     return int(parts[4]) + int(parts[5])
-    return None
+                if len(parts) == 7 and parts[0] == "traffic-per-unit:" and parts[1] == name and parts[2] == kind \
+                        and parts[3] == cur and units > 0:
+                    scaled = int(round((int(parts[4]) + int(parts[5])) * units / int(parts[6])))
+    return scaled
 
 
 def measured_peaks():
@@ -218,14 +236,16 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
-def oracle_sample(cfg, r, host_banks_np, threads, ffn_tokens=4, reps=None, budget_s=12.0):
+def oracle_sample(cfg, r, host_banks_np, threads, ffn_tokens=4, reps=None, budget_s=12.0, slot_bufs=None):
     """Time the CPU oracle on a bounded sample of one step: ensure + copy of the whole
-    step (the copy into a host-side slot buffer), and the FFN for `ffn_tokens` tokens.
-    Returns dict(copy GB/s, ensure+copy seconds per step, ffn seconds per token)."""
+    step (the copy into a host-side slot buffer, allocated once and touched before timing),
+    and the FFN for `ffn_tokens` tokens. Returns dict(copy GB/s, ensure+copy seconds per
+    step, ffn seconds per token)."""
     import oracle
 
     schema_bytes = [b.shape[1] for b in host_banks_np]
-    slot_bufs = [np.empty((cfg.S, n), np.uint8) for n in schema_bytes]
+    if slot_bufs is None:
+        slot_bufs = host_slot_buffers(cfg, schema_bytes)
     t_ec = []
     t0 = time.perf_counter()
     m = 0
@@ -247,6 +267,15 @@ def oracle_sample(cfg, r, host_banks_np, threads, ffn_tokens=4, reps=None, budge
     ec = statistics.median(t_ec)
     return {"copy_gbps": m * B / ec / 1e9, "ensure_copy_s": ec, "ffn_s_per_token": t_ffn, "reps": len(t_ec),
             "misses": m, "ffn_tokens": len(toks)}
+
+
+def host_slot_buffers(cfg, schema_bytes):
+    """Host-side slot banks of the oracle's copy, pages touched up front so that the timed
+    copies do not pay first-touch page faults."""
+    bufs = [np.empty((cfg.S, n), np.uint8) for n in schema_bytes]
+    for b in bufs:
+        b.fill(0)
+    return bufs
 
 
 # ------------------------------------------------------------------------------ reference arm
@@ -284,8 +313,9 @@ def run_reference(args):
     banks = reference_banks(cfg, wl)
     cores = cpu_cores()
     times = []
+    bufs = host_slot_buffers(cfg, [b.shape[1] for b in banks])
     for i in range(args.warmup + args.steps):
-        res = oracle_sample(cfg, r, banks, cores, ffn_tokens=1, reps=1)
+        res = oracle_sample(cfg, r, banks, cores, ffn_tokens=1, reps=1, slot_bufs=bufs)
         if i >= args.warmup:
             times.append(res)
     ec = sum(t["ensure_copy_s"] for t in times)
@@ -296,7 +326,7 @@ def run_reference(args):
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_OF[cfg.fmt], "data": "synthetic",
         "config": {"workload": f"{cfg.name} bs={args.bs} miss_rate={args.miss_rate}", "bs": args.bs,
                    "miss_rate": args.miss_rate, "misses": r.misses, "parallelism": "host cores"},
         "time_ms": ec / len(times) * 1e3, "tok_ms": ec / len(times) * 1e3 * cfg.L,
@@ -326,7 +356,7 @@ def run_gpu(args):
         dist.barrier()
     from expert_slot_cache_device_gb300 import ftmoe as F
     from expert_slot_cache_device_gb300 import workload as wl
-    from expert_slot_cache_device_gb300.cache import ExpertSlotCache
+    from expert_slot_cache_device_gb300.synthetic import release_memory, synthetic_cache
 
     dev = torch.cuda.current_device()
     stream = torch.cuda.Stream()
@@ -334,7 +364,7 @@ def run_gpu(args):
     if args.experts or args.slots:
         cfg = wl.scaled(cfg, E=args.experts or cfg.E, S=args.slots or cfg.S)
     if cfg.steps > 0:  # the multi-step decode trace has its own measurement
-        line = run_trace(cfg, stream, torch, F, wl, ExpertSlotCache)
+        line = run_trace(cfg, stream, torch, F, wl, synthetic_cache)
         line.update({"n_gpus": world, "steps": args.steps, "warmup": args.warmup})
         if rank == 0:
             print(json.dumps(line), flush=True)
@@ -344,12 +374,11 @@ def run_gpu(args):
     B = cfg.bytes_per_expert
     # every layer's host source aliases layer 0's bank (allowed by the per-layer source
     # lists) so that the prefill probe can stream any layer
-    cache = ExpertSlotCache(cfg, max(max(cfg.bs_list), bs, PREFILL_BS) * cfg.topk, alias_all=True, stream=stream)
+    cache = synthetic_cache(cfg, max(max(cfg.bs_list), bs, PREFILL_BS) * cfg.topk, alias_all=True, stream=stream)
     cache.set_copy_mode({"fused": F.COPY_FUSED, "per_bank": F.COPY_PER_BANK, "engine": F.COPY_ENGINE}[args.copy_mode])
     if args.ffn_kernels != "auto":
         cache.set_ffn_kernels({"rows": F.FFN_ROWS, "mma": F.FFN_MMA}[args.ffn_kernels])
-    # the FFN kernel family this call runs (CUDA-core rows pipelines or tensor-core pipelines)
-    ffn_kind = "ffn_mma" if F.ftmoe_ffn_kernels_for(cache.handle, bs, cfg.topk) == F.FFN_MMA else "ffn_rows"
+    ffn_kind = ffn_family(F, cache, cfg, bs)
     s = stream.cuda_stream
     d_ids = torch.from_numpy(r.topk_ids).cuda()
     d_slots = torch.empty_like(d_ids)
@@ -443,15 +472,17 @@ def run_gpu(args):
         copy_ach = r.misses * B / copy_s / 1e9 if r.misses else 0.0
         w_bytes = r.active * (cfg.bytes_per_expert) + 2 * bs * cfg.H * 2
         ffn_ach = w_bytes / ffn_s / 1e9
-        launches_per_step = 2 + 1 + (1 if args.copy_mode == "fused" else (cache.nb if args.copy_mode == "per_bank" else 0)) + 4
+        launches_per_step = 2 + 1 + (1 if args.copy_mode == "fused" else (cache.nb if args.copy_mode == "per_bank" else 0)) \
+            + ffn_launches(cfg, ffn_kind)
+        workload = f"{cfg.name} bs={bs} miss_rate={mr}"
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": agg_total / args.steps * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": f"{cfg.name} bs={bs} miss_rate={mr}", "E": cfg.E, "topk": cfg.topk, "H": cfg.H,
+            "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_OF[cfg.fmt], "data": "synthetic",
+            "config": {"workload": workload, "format": cfg.fmt, "E": cfg.E, "topk": cfg.topk, "H": cfg.H,
                        "I": cfg.I, "L": cfg.L, "S": cfg.S, "bs": bs, "miss_rate": mr, "active": r.active,
                        "misses": r.misses, "copy_MiB": r.misses * B / 2 ** 20, "copy_mode": args.copy_mode,
-                       "ffn_kernels": f"{args.ffn_kernels}: {'tensor cores' if ffn_kind == 'ffn_mma' else 'CUDA cores'}",
+                       "ffn_kernels": f"{args.ffn_kernels}: {FAMILY_NAMES[ffn_kind]}",
                        "l2": f"inputs larger than L2: {r.misses * B / 2**20:.0f} MiB copied and "
                              f"{r.active * B / 2**20:.0f} MiB of expert weights read per step",
                        "parallelism": f"replicas x{world}",
@@ -461,29 +492,30 @@ def run_gpu(args):
             "tok_ms": time_ms * cfg.L, "ffn_us": ffn_s * 1e6,
             "roofline": {"bound": "host_link", "kernel": "copy_missing_kernel", "achieved": copy_ach, "peak": link,
                          "unit": "GB/s", "frac": copy_ach / link if link else None,
-                         "traffic": recorded_traffic(f"{cfg.name}/bs{bs}/mr{mr}", "copy"),
+                         "traffic": recorded_traffic(f"{cfg.name}/bs{bs}/mr{mr}", "copy", units=r.misses),
                          "peak_source": f"measured in this run: max(1 GiB pinned->device cudaMemcpyAsync "
                                         f"{links['memcpy']:.1f}, SM zero-copy read {links['sm_read']:.1f}) GB/s"},
-            "roofline_ffn": {"bound": "hbm", "kernel": "expert FFN (route + gate_up + down + combine)",
+            "roofline_ffn": {"bound": "hbm", "kernel": "expert FFN (all kernels of one call)",
                              "achieved": ffn_ach, "peak": hbm_peak, "unit": "GB/s", "frac": ffn_ach / hbm_peak,
-                             "traffic": recorded_traffic(f"{cfg.name}/bs{bs}/mr{mr}", ffn_kind),
+                             "traffic": recorded_traffic(f"{cfg.name}/bs{bs}/mr{mr}", ffn_kind, units=r.active),
                              "peak_source": hbm_src},
             "link_peak_GBps": links,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
         }
+        configs = {}
         if not args.no_sweep:
-            line["sweep"] = sweep(args, cfg, cache, stream, torch, F, wl)
+            configs[cfg.name] = {"key": cfg.key, "format": cfg.fmt,
+                                 "points": sweep(args, cfg, cache, stream, torch, F, wl, link, hbm_peak)}
         if not args.no_hybrid:
             line["hybrid"] = hybrid_probe(args, cfg, cache, stream, torch, F, wl, link, cpu_cores())
         if not args.no_prefill:
             line["prefill"] = prefill_probe(cfg, cache, torch, F)
         if not args.no_graph:
             line["graph"] = graph_probe(cfg, cache, torch, F, wl)
-    cache.close()
     if rank == 0 and not args.no_cpu_baseline:
-        hb = [cache.host[b][0].numpy() for b in range(cache.nb)]
+        hb = [cache.host_tensor(b, 0).numpy() for b in range(cache.nb)]
         cores = cpu_cores()
         res = oracle_sample(cfg, r, hb, cores, ffn_tokens=2)
         line["cpu_baseline"] = {"value": res["copy_gbps"], "unit": "GB/s", "cores": cores, "kind": "oracle",
@@ -492,11 +524,68 @@ def run_gpu(args):
                                           f"{res['ffn_tokens']} of {bs} tokens on {cores} threads: "
                                           f"{res['ffn_s_per_token'] * 1e3:.1f} ms/token",
                                 "ffn_us_per_layer_est": res["ffn_s_per_token"] * bs * 1e6}
+        del hb
+    cache.close(release=True)
+    del cache, d_ids, d_slots, d_w, d_x, d_y, h_ids, h_w, h_x, h_y
+    release_memory()
     if rank == 0:
+        # every other workload of the metric, one after another (each one's banks freed before
+        # the next is built): all (bs, miss_rate) points, or the decode trace's summary
+        others = [] if args.configs in ("", "none") else [k for k in args.configs.split(",") if k != args.config]
+        for key in others:
+            ocfg = wl.CONFIGS[key]
+            t0 = time.perf_counter()
+            if ocfg.steps > 0:
+                tr = run_trace(ocfg, stream, torch, F, wl, synthetic_cache)
+                entry = {"key": key, "format": ocfg.fmt, "trace": tr["trace"], "trace_value_GBps": tr["value"],
+                         "copy_frac_of_link": tr["value"] / link, "clocks": tr["clocks"]}
+            else:
+                entry = {"key": key, "format": ocfg.fmt,
+                         "points": sweep_workload(args, ocfg, stream, torch, F, wl, synthetic_cache, link, hbm_peak)}
+            entry["wall_s"] = time.perf_counter() - t0
+            configs[ocfg.name] = entry
+            release_memory()
+        tiny = wl.CONFIGS["c1"]
+        configs[tiny.name] = {"key": "c1", "format": tiny.fmt,
+                              "parity_only": "checked against the oracle by the GPU tests and smoke(); 384 KiB of "
+                                             "weights, too small to time"}
+        line["configs"] = configs
         print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+# weight format the FFN computes from (the copy moves bytes); every format accumulates in fp32
+DTYPE_OF = {"bf16": "bf16", "nvfp4": "nvfp4", "mxfp4": "mxfp4", "fp8": "e4m3", "q4_0": "q4_0", "raw": "u8"}
+FAMILY_NAMES = {"ffn_rows": "CUDA-core bulk-copy pipeline", "ffn_mma": "tensor-core pipeline (mma.sync)",
+                "ffn_mx": "mxfp4 tensor-map pipeline (mma.sync)", "ffn_fp8": "block-FP8 tensor-map pipeline (mma.sync)"}
+
+
+def ffn_family(F, cache, cfg, bs):
+    """Kernel family one FFN call of `bs` tokens runs (keys of TRAFFIC_SOURCES)."""
+    if cfg.fmt == "mxfp4":
+        return "ffn_mx"
+    if cfg.fmt == "fp8":
+        return "ffn_fp8"
+    if cfg.fmt == "bf16" and F.ftmoe_ffn_kernels_for(cache.handle, bs, cfg.topk) == F.FFN_MMA:
+        return "ffn_mma"
+    return "ffn_rows"
+
+
+def ffn_launches(cfg, kind):
+    """Kernels one FFN call launches: routing, gate_up, down and combine."""
+    return 4
+
+
+def sweep_workload(args, cfg, stream, torch, F, wl, synthetic_cache, link, hbm_peak):
+    """All (bs, miss_rate) points of one workload on a cache of its own (freed afterwards)."""
+    cache = synthetic_cache(cfg, max(cfg.bs_list) * cfg.topk, alias_all=True, stream=stream)
+    try:
+        return sweep(args, cfg, cache, stream, torch, F, wl, link, hbm_peak)
+    finally:
+        cache.close(release=True)
+        del cache
 
 
 PREFILL_BS = 64      # tokens of the prefill batch of the pipeline probe
@@ -636,7 +725,7 @@ def wl_bits(a):
     return wl.f32_to_bf16_bits(a).view(np.int16)
 
 
-def run_trace(cfg, stream, torch, F, wl, ExpertSlotCache):
+def run_trace(cfg, stream, torch, F, wl, make_cache):
     """The multi-step decode trace: every (step, layer) call of cfg.steps steps x cfg.L
     layers at bs 1, from a cold cache, each call ensure + copy_missing + expert FFN on one
     stream. All inputs are generated and moved to the device before the timed region.
@@ -650,7 +739,7 @@ def run_trace(cfg, stream, torch, F, wl, ExpertSlotCache):
         for layer in range(cfg.L):
             i = step * cfg.L + layer
             ids[i], ws[i], xs[i] = wl.trace_call(cfg, step, layer)
-    cache = ExpertSlotCache(cfg, k, alias_all=True, stream=stream)
+    cache = make_cache(cfg, k, alias_all=True, stream=stream)
     d_ids = torch.from_numpy(ids).cuda()
     d_w = torch.from_numpy(ws).cuda()
     d_x = torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16).cuda()
@@ -679,7 +768,10 @@ def run_trace(cfg, stream, torch, F, wl, ExpertSlotCache):
     ffn = np.array([ev[i][1].elapsed_time(ev[i][2]) for i in range(n)]).reshape(cfg.steps, cfg.L)
     B = cfg.bytes_per_expert
     step_ms = fetch.sum(1)
-    cache.close()
+    cache.close(release=True)
+    del cache, d_ids, d_w, d_x
+    hbm_peak, _ = measured_peaks()
+    ffn_bytes_per_call = k * B + 2 * cfg.H * 2  # k distinct experts per call at bs 1, plus x and y
     return {
         "metric": METRIC, "value": misses * B / (fetch.sum() / 1e3) / 1e9, "unit": "GB/s",
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -691,7 +783,9 @@ def run_trace(cfg, stream, torch, F, wl, ExpertSlotCache):
                   "ffn_ms_total": float(ffn.sum()),
                   "tok_ms": {"mean": float(step_ms.mean()), "p50": float(np.percentile(step_ms, 50)),
                              "p99": float(np.percentile(step_ms, 99)), "first_step": float(step_ms[0])},
-                  "ffn_ms_per_token": float(ffn.sum(1).mean())},
+                  "ffn_ms_per_token": float(ffn.sum(1).mean()),
+                  "ffn_us_per_call_p50": float(np.percentile(ffn, 50) * 1e3),
+                  "ffn_frac_of_hbm": ffn_bytes_per_call * n / (ffn.sum() / 1e3) / 1e9 / hbm_peak},
         "clocks": clocks,
     }
 
@@ -760,7 +854,7 @@ def hybrid_probe(args, cfg, cache, stream, torch, F, wl, link_gbps, cores):
     return out
 
 
-def sweep(args, cfg, cache, stream, torch, F, wl):
+def sweep(args, cfg, cache, stream, torch, F, wl, link=None, hbm_peak=None):
     """Every (bs, miss_rate) point of the workload: median of `repeat` ensure+copy times
     and FFN times (each repeat from the prepared state)."""
     out = []
@@ -792,10 +886,14 @@ def sweep(args, cfg, cache, stream, torch, F, wl):
                     tf.append(ev[1].elapsed_time(ev[2]))
             t = statistics.median(tec)
             f = statistics.median(tf)
+            bw = r.misses * B / (t / 1e3) / 1e9
+            fg = (r.active * B + 2 * bs * cfg.H * 2) / (f / 1e3) / 1e9
             out.append({"bs": bs, "active": r.active, "miss_rate": mr, "misses": r.misses, "time_ms": t,
-                        "copy_MiB": r.misses * B / 2 ** 20, "bw_GBps": r.misses * B / (t / 1e3) / 1e9,
-                        "tok_ms": t * cfg.L, "ffn_us": f * 1e3,
-                        "ffn_GBps": (r.active * B + 2 * bs * cfg.H * 2) / (f / 1e3) / 1e9})
+                        "copy_MiB": r.misses * B / 2 ** 20, "bw_GBps": bw,
+                        "copy_frac_of_link": bw / link if (link and r.misses) else None,
+                        "tok_ms": t * cfg.L, "ffn_us": f * 1e3, "ffn_GBps": fg,
+                        "ffn_frac_of_hbm": fg / hbm_peak if hbm_peak else None,
+                        "ffn_kernels": ffn_family(F, cache, cfg, bs)})
     return out
 
 

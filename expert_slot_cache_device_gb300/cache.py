@@ -1,16 +1,21 @@
-"""Python-side owner of one expert slot cache: PyTorch provides the page-locked host
-banks, the device slot banks and the workspace; every step runs in libftmoe through
-the C-ABI binding (``ftmoe``). Nothing here computes any part of the decode step.
+"""Python-side owner of one expert slot cache over the caller's banks.
+
+The caller supplies the page-locked host banks (per bank, one tensor per layer, entries may
+alias or be None for layers that are never driven) and, optionally, the device slot banks;
+PyTorch provides whatever device memory the caller did not (slot banks, workspace). Every
+step of the decode path runs in libftmoe through the C-ABI binding (``ftmoe``); nothing here
+computes any part of it. Synthetic banks for tests and benchmarks are built by
+``synthetic.synthetic_cache``.
 """
 from __future__ import annotations
 
-from typing import List, Optional, Sequence
+import dataclasses
+from typing import List, Optional, Sequence, Union
 
 import numpy as np
 import torch
 
 from . import ftmoe as F
-from . import workload as wl
 
 
 def _stream(stream) -> int:
@@ -19,56 +24,124 @@ def _stream(stream) -> int:
     return stream if isinstance(stream, int) else stream.cuda_stream
 
 
-class ExpertSlotCache:
-    """A cache over the banks of ``cfg`` (one workload geometry).
+@dataclasses.dataclass(frozen=True)
+class Bank:
+    """Per-expert geometry of one bank, as declared to the library: one expert occupies
+    ``rows * row_bytes`` bytes. ``dtype`` is a key of ``ftmoe.DTYPES`` (informative; the
+    FFN formats check each bank's per-expert bytes against their schema)."""
+    name: str
+    dtype: str
+    rows: int
+    row_bytes: int
 
-    host_layers: which layers get their own host bank (default: layer 0 only, as the
-    copy benchmark drives a single layer); ``alias_all`` makes every layer point at
-    one shared host bank (used for long multi-layer traces).
+    @property
+    def bytes(self) -> int:
+        return self.rows * self.row_bytes
+
+
+def _as_bank(g) -> Bank:
+    return g if isinstance(g, Bank) else Bank(g.name, g.dtype, int(g.rows), int(g.row_bytes))
+
+
+def check_banks(fmt: Union[str, int], E: int, L: int, S: int, banks: Sequence, host_sources: Sequence[Sequence],
+                slot_banks: Optional[Sequence] = None) -> List[Bank]:
+    """Host-side validation of caller banks before they reach the library: per bank, L host
+    entries, each None or a contiguous uint8 tensor holding E experts of the bank's bytes
+    (shape [E, bytes] or any shape with E * bytes elements) on the host; slot banks, when
+    given, contiguous uint8 device tensors with S * bytes elements. Raises ValueError."""
+    if isinstance(fmt, str):
+        if fmt not in F.FORMATS:
+            raise ValueError(f"unknown format {fmt!r}")
+    elif fmt not in F.FORMATS.values():
+        raise ValueError(f"unknown format code {fmt}")
+    banks = [_as_bank(g) for g in banks]
+    if not 1 <= len(banks) <= F.MAX_BANKS:
+        raise ValueError(f"{len(banks)} banks (1..{F.MAX_BANKS})")
+    if len(host_sources) != len(banks):
+        raise ValueError(f"host_sources has {len(host_sources)} entries for {len(banks)} banks")
+    for b, (g, src) in enumerate(zip(banks, host_sources)):
+        if g.dtype not in F.DTYPES:
+            raise ValueError(f"bank {g.name}: unknown dtype {g.dtype!r}")
+        if g.rows <= 0 or g.row_bytes <= 0:
+            raise ValueError(f"bank {g.name}: rows and row_bytes must be positive")
+        if len(src) != L:
+            raise ValueError(f"bank {g.name}: {len(src)} host entries for {L} layers")
+        for l, t in enumerate(src):
+            if t is None:
+                continue
+            if not isinstance(t, torch.Tensor) or t.dtype != torch.uint8:
+                raise ValueError(f"bank {g.name} layer {l}: host source must be a uint8 tensor")
+            if t.device.type != "cpu" or not t.is_contiguous():
+                raise ValueError(f"bank {g.name} layer {l}: host source must be a contiguous host tensor")
+            if t.numel() != E * g.bytes:
+                raise ValueError(f"bank {g.name} layer {l}: {t.numel()} bytes, expected E * {g.bytes}")
+    if slot_banks is not None:
+        if len(slot_banks) != len(banks):
+            raise ValueError(f"slot_banks has {len(slot_banks)} entries for {len(banks)} banks")
+        for g, t in zip(banks, slot_banks):
+            if t.dtype != torch.uint8 or not t.is_contiguous() or t.numel() != S * g.bytes:
+                raise ValueError(f"slot bank {g.name}: needs a contiguous uint8 tensor of S * {g.bytes} bytes")
+    return banks
+
+
+class ExpertSlotCache:
+    """A cache over caller-owned banks.
+
+    fmt           "bf16" | "nvfp4" | "mxfp4" | "fp8" | "q4_0" | "raw" (or an FTMOE_FMT_* code)
+    banks         per-bank geometry (``Bank`` or any object with name, dtype, rows, row_bytes),
+                  in the schema order of the format
+    host_sources  host_sources[b][l]: page-locked uint8 tensor of layer l's E experts of
+                  bank b (pin_memory, cudaHostRegister'ed memory), or None for a layer whose
+                  bank is not filled; entries may alias (the same tensor for several layers)
+    slot_banks    optional device uint8 tensors [S, bytes_b]; allocated here when omitted
+    max_pairs     routed pairs (bs * topk) of the largest FFN call (0: no FFN scratch)
     """
 
-    def __init__(self, cfg: wl.Config, max_pairs: int, host_layers: Sequence[int] = (0,), alias_all: bool = False,
-                 fill: bool = True, device: str = "cuda", stream=None, gen: str = "device"):
+    def __init__(self, fmt: Union[str, int], E: int, L: int, S: int, H: int, I: int, banks: Sequence,
+                 host_sources: Sequence[Sequence[Optional[torch.Tensor]]], max_pairs: int,
+                 slot_banks: Optional[Sequence[torch.Tensor]] = None, device: str = "cuda", stream=None):
         F.lib()
-        self.cfg = cfg
-        self.schema = wl.bank_schema(cfg)
+        self.schema = check_banks(fmt, E, L, S, banks, host_sources, slot_banks)
+        self.fmt = fmt if isinstance(fmt, str) else {v: k for k, v in F.FORMATS.items()}[fmt]
+        self.E, self.L, self.S, self.H, self.I = E, L, S, H, I
         self.nb = len(self.schema)
         self.device = torch.device(device)
         self.max_pairs = max_pairs
-        E, L, S = cfg.E, cfg.L, cfg.S
-        # host banks: one pinned tensor per (bank, filled layer)
-        self.host: List[dict] = [dict() for _ in range(self.nb)]
-        layers = [0] if alias_all else list(host_layers)
-        for b, g in enumerate(self.schema):
-            for l in layers:
-                t = torch.empty((E, g.bytes), dtype=torch.uint8, pin_memory=True)
-                if fill and gen == "device":
-                    wl.fill_bank_device(cfg, b, t, device=str(self.device))
-                elif fill:
-                    wl.fill_bank(cfg, b, t.numpy())
-                self.host[b][l] = t
-        self.host_ptrs = []
-        for b in range(self.nb):
-            if alias_all:
-                ptrs = [self.host[b][0].data_ptr()] * L
-            else:
-                ptrs = [self.host[b][l].data_ptr() if l in self.host[b] else 0 for l in range(L)]
-            self.host_ptrs.append(ptrs)
-        self.slots = [torch.empty((S, g.bytes), dtype=torch.uint8, device=self.device) for g in self.schema]
-        fmt = F.FORMATS[cfg.fmt]
-        self.ws_bytes = F.ftmoe_cache_workspace_bytes(fmt, self.nb, E, L, S, cfg.H, cfg.I, max_pairs)
+        self.cfg = None  # set by the synthetic builder (workload geometry of test caches)
+        # host[b]: layer -> tensor for the distinct tensors of bank b (first layer naming each)
+        self.host: List[dict] = []
+        self.host_ptrs: List[List[int]] = []
+        for src in host_sources:
+            seen, d = {}, {}
+            for l, t in enumerate(src):
+                if t is not None and t.data_ptr() not in seen:
+                    seen[t.data_ptr()] = l
+                    d[l] = t
+            self.host.append(d)
+            self.host_ptrs.append([t.data_ptr() if t is not None else 0 for t in src])
+        self._host_sources = [list(src) for src in host_sources]  # keep the caller's tensors alive
+        if slot_banks is None:
+            slot_banks = [torch.empty((S, g.bytes), dtype=torch.uint8, device=self.device) for g in self.schema]
+        self.slots = [t.view(S, g.bytes) for t, g in zip(slot_banks, self.schema)]
+        code = F.FORMATS[self.fmt]
+        self.ws_bytes = F.ftmoe_cache_workspace_bytes(code, self.nb, E, L, S, H, I, max_pairs)
         self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
         specs = [dict(name=g.name, dtype=F.DTYPES[g.dtype], rows=g.rows, row_bytes=g.row_bytes,
                       host_src=self.host_ptrs[b], dev_slots=self.slots[b].data_ptr())
                  for b, g in enumerate(self.schema)]
         self._specs, self._keep = F.make_bank_specs(specs)
-        self.handle = F.ftmoe_cache_create(self._specs, self.nb, fmt, E, L, S, cfg.H, cfg.I, max_pairs,
+        self.handle = F.ftmoe_cache_create(self._specs, self.nb, code, E, L, S, H, I, max_pairs,
                                            self.workspace.data_ptr(), self.ws_bytes, _stream(stream))
 
-    def close(self):
+    def close(self, release: bool = False):
+        """Destroy the library handle; ``release`` also drops the references this object holds
+        to the host banks, slot banks and workspace (so their memory can be freed)."""
         if getattr(self, "handle", None):
             F.ftmoe_cache_destroy(self.handle)
             self.handle = None
+        if release:
+            self.host, self.host_ptrs, self._host_sources = [], [], []
+            self.slots, self.workspace = [], None
 
     def __del__(self):
         try:
@@ -109,7 +182,7 @@ class ExpertSlotCache:
 
     # ------------------------------------------------------------------ state
     def get_state(self, stream=None):
-        S = self.cfg.S
+        S = self.S
         owner = np.empty(S, np.int32)
         stamp = np.empty(S, np.uint32)
         clock = np.zeros(1, np.uint32)
@@ -122,7 +195,7 @@ class ExpertSlotCache:
         F.ftmoe_cache_set_state(self.handle, owner.ctypes.data, stamp.ctypes.data, int(clock), _stream(stream))
 
     def miss_list(self, stream=None):
-        cap = max(1, min(self.cfg.E, self.cfg.S))
+        cap = max(1, min(self.E, self.S))
         ids = np.empty(cap, np.int32)
         slots = np.empty(cap, np.int32)
         m = np.zeros(1, np.int32)
@@ -139,9 +212,15 @@ class ExpertSlotCache:
         return int(st[0])
 
     # ------------------------------------------------------------------ views
+    def host_tensor(self, b: int, layer: int) -> torch.Tensor:
+        """Layer `layer`'s host bank b viewed as [E, bytes_b]."""
+        t = self._host_sources[b][layer]
+        if t is None:
+            raise ValueError(f"bank {b} of layer {layer} is not filled")
+        return t.view(self.E, self.schema[b].bytes)
+
     def host_expert_bytes(self, b: int, layer: int, e: int) -> np.ndarray:
-        key = 0 if len(self.host[b]) == 1 and layer not in self.host[b] else layer
-        return self.host[b][key][e].numpy()
+        return self.host_tensor(b, layer)[e].numpy()
 
     def expert_host_ptrs(self, layer: int, e: int) -> List[int]:
         """Host addresses of expert e's bytes in every bank of `layer` (for the oracle)."""

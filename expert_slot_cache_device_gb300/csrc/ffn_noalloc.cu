@@ -73,8 +73,13 @@ extern "C" int ftmoe_expert_ffn_noalloc(int32_t format, const void *const *d_slo
     if (H <= 0 || I <= 0 || H % q || I % q) return report_error(FTMOE_ERR_INVALID_ARG, "H and I must be positive multiples of 8 (bf16) or 32 (fp4)");
     if (S <= 0 || S > FTMOE_MAX_SLOTS) return report_error(FTMOE_ERR_INVALID_ARG, "S outside [1, FTMOE_MAX_SLOTS]");
     if (bs < 0 || topk <= 0) return report_error(FTMOE_ERR_INVALID_ARG, "bs >= 0 and topk > 0 required");
+    if (bs > 65535) return report_error(FTMOE_ERR_INVALID_ARG, "bs above 65535 (one grid row per token)");
     const int64_t P = (int64_t)bs * topk;
     if (P == 0) return FTMOE_OK;
+    // P fits the fixed scratch only if P * (H + I) * 4 < its size: checked before any size
+    // is formed, so no product below can wrap
+    if (P > (int64_t)(kStaticScratchBytes / (4 * ((uint64_t)H + (uint64_t)I))))
+        return report_error(FTMOE_ERR_INVALID_ARG, "bs * topk * (H + I) too large for the fixed FFN scratch (FTMOE_NOALLOC_SCRATCH_BYTES)");
     if (!d_x_bf16 || !d_slots || !d_weights || !d_y_bf16) return report_error(FTMOE_ERR_INVALID_ARG, "NULL FFN argument");
     if (((uintptr_t)d_x_bf16 | (uintptr_t)d_y_bf16) % 16) return report_error(FTMOE_ERR_INVALID_ARG, "x and y must be 16-byte aligned");
     for (int b = 0; b < num_banks; b++)

@@ -372,18 +372,25 @@ int ftmoe_h2d_stream_copy(void *d_dst, const void *h_src, size_t bytes, void *st
  * accounting), and code on a latency-critical path that must not pay for
  * cudaMalloc/cudaFree and the device synchronisation they can cause.
  *
- * Computes exactly what ftmoe_expert_ffn computes, without a cache handle: the caller
- * passes its slot banks d_slot_banks[num_banks] (device [S, per-expert bytes] each, in
- * the schema order of `format`, FTMOE_FMT_BF16/NVFP4/MXFP4), the activations, slots,
- * router weights and the output, with the same layouts as ftmoe_expert_ffn. The
- * routing tables and fp32 intermediates live in one file-scope device array of
+ * Computes the FFN of ftmoe_expert_ffn, without a cache handle, to within the FFN
+ * tolerance of that call (max abs 2e-2, relative L2 1e-2 on bf16 outputs; it runs the
+ * general register-path kernels, not the bulk-copy or tensor-core pipelines, so it is
+ * slower at decode sizes and its rounding differs). Formats FTMOE_FMT_BF16, NVFP4 and
+ * MXFP4 only (block FP8 and Q4_0 have no register-path kernels): FTMOE_ERR_INVALID_ARG
+ * otherwise. The caller passes its slot banks d_slot_banks[num_banks] (device
+ * [S, per-expert bytes] each, in the schema order of `format`), the activations, slots,
+ * router weights and the output, with the same layouts as ftmoe_expert_ffn; a slot of
+ * -1 marks a position computed elsewhere, which contributes nothing. The routing tables
+ * and fp32 intermediates live in one file-scope device array of
  * FTMOE_NOALLOC_SCRATCH_BYTES that every GPU loading the library reserves until the
- * process exits; calls needing more (about bs * topk * (H + I) * 4 bytes) fail with
- * FTMOE_ERR_INVALID_ARG. The first call on a device looks up that array's device
- * address (cudaGetSymbolAddress); make that first call before any stream capture.
- * All calls share the array and it keeps the previous call's contents: calls that
- * overlap on the GPU race on it and must be serialised by the caller. A slot outside
- * [0, S) leaves d_y_bf16 unwritten (there is no status to read back). */
+ * process exits; calls needing more (about bs * topk * (H + I) * 4 bytes), or with bs
+ * above 65535, fail with FTMOE_ERR_INVALID_ARG. The first call on a device looks up that
+ * array's device address (cudaGetSymbolAddress) and keeps it for the life of the
+ * process, so a device reset (cudaDeviceReset, or a reset of the primary context) while
+ * the library is loaded is not supported; make that first call before any stream
+ * capture. All calls share the array and it keeps the previous call's contents: calls
+ * that overlap on the GPU race on it and must be serialised by the caller. A slot
+ * outside [-1, S) leaves d_y_bf16 unwritten (there is no status to read back). */
 int ftmoe_expert_ffn_noalloc(int32_t format, const void *const *d_slot_banks, int32_t num_banks,
                              int32_t S, int32_t H, int32_t I, const void *d_x_bf16, int32_t bs,
                              const int32_t *d_slots, const float *d_weights, int32_t topk,

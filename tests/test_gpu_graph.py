@@ -11,7 +11,7 @@ import torch
 
 from expert_slot_cache_device_gb300 import ftmoe as F
 from expert_slot_cache_device_gb300 import workload as wl
-from expert_slot_cache_device_gb300.cache import ExpertSlotCache
+from expert_slot_cache_device_gb300.synthetic import synthetic_cache
 from gpu_helpers import to_dev, x_dev
 
 pytestmark = [pytest.mark.gpu,
@@ -41,7 +41,7 @@ def _calls(cfg, bs, steps, seed):
 def test_decode_calls_replay_from_a_graph(bs):
     # E = 16, topk 8: bs 2 routes 16 pairs (CUDA-core FFN), bs 4 routes 32 (tensor-core FFN)
     cfg = wl.scaled(wl.CONFIGS["c2"], E=16, L=3, S=24)
-    cache = ExpertSlotCache(cfg, bs * cfg.topk, host_layers=range(cfg.L))
+    cache = synthetic_cache(cfg, bs * cfg.topk, host_layers=range(cfg.L))
     expect = F.FFN_ROWS if bs == 2 else F.FFN_MMA
     assert F.ftmoe_ffn_kernels_for(cache.handle, bs, cfg.topk) == expect
     calls = _calls(cfg, bs, steps=2, seed=bs)

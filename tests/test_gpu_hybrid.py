@@ -12,7 +12,7 @@ import torch
 import oracle
 from expert_slot_cache_device_gb300 import ftmoe as F
 from expert_slot_cache_device_gb300 import workload as wl
-from expert_slot_cache_device_gb300.cache import ExpertSlotCache
+from expert_slot_cache_device_gb300.synthetic import synthetic_cache
 from gpu_helpers import assert_ffn_close, bf16_to_f64, oracle_ffn, to_dev, x_dev
 
 pytestmark = [pytest.mark.gpu,
@@ -33,7 +33,7 @@ def test_hybrid_ensure_random_traces(seed):
     E, L, k = int(rng.integers(8, 40)), int(rng.integers(1, 4)), int(rng.integers(2, 6))
     S = int(rng.integers(k, k + 16))
     cfg = wl.Config("raw", "raw", 9, "raw", E, 1, 64, 0, L, S, (1,), (1.0,), "uniform", 0.0, seed)
-    cache = ExpertSlotCache(cfg, 0, host_layers=range(L))
+    cache = synthetic_cache(cfg, 0, host_layers=range(L))
     orc = oracle.Cache(E, L, S)
     d_slots = torch.empty((2, k), dtype=torch.int32, device="cuda")
     d_counts = torch.zeros(2, dtype=torch.int32, device="cuda")
@@ -66,7 +66,7 @@ CASES = [("c2", dict(), 16, 0.5, 24), ("c3", dict(E=64, S=96), 8, 1.0, 20), ("c4
 @pytest.mark.parametrize("key,geo,bs,mr,max_fetch", CASES)
 def test_hybrid_step_matches_oracle(key, geo, bs, mr, max_fetch):
     cfg = wl.scaled(wl.CONFIGS[key], **geo)
-    cache = ExpertSlotCache(cfg, bs * cfg.topk)
+    cache = synthetic_cache(cfg, bs * cfg.topk)
     r = wl.make_route(cfg, bs, mr)
     for i, e in enumerate(sorted(int(v) for v in r.hits)):
         for b in range(cache.nb):

@@ -14,7 +14,7 @@ import torch
 import oracle
 from expert_slot_cache_device_gb300 import ftmoe as F
 from expert_slot_cache_device_gb300 import workload as wl
-from expert_slot_cache_device_gb300.cache import ExpertSlotCache
+from expert_slot_cache_device_gb300.synthetic import synthetic_cache
 from gpu_helpers import assert_ffn_close, bf16_to_f64, oracle_ffn, to_dev, x_dev
 
 pytestmark = pytest.mark.gpu
@@ -29,7 +29,7 @@ CASES = {
 
 
 def make_cache(cfg, bs):
-    cache = ExpertSlotCache(cfg, max_pairs=bs * cfg.topk, host_layers=range(cfg.L))
+    cache = synthetic_cache(cfg, max_pairs=bs * cfg.topk, host_layers=range(cfg.L))
     # make every layer's bank different: layer l holds layer 0's experts rolled by l
     for b in range(cache.nb):
         base = cache.host[b][0].clone()

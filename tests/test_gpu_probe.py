@@ -6,7 +6,7 @@ import torch
 
 from expert_slot_cache_device_gb300 import ftmoe as F
 from expert_slot_cache_device_gb300 import workload as wl
-from expert_slot_cache_device_gb300.cache import ExpertSlotCache
+from expert_slot_cache_device_gb300.synthetic import synthetic_cache
 
 pytestmark = pytest.mark.gpu
 
@@ -21,7 +21,7 @@ def test_link_probe_and_decision():
     assert bool((dst == 3).all())  # the probe really moved the bytes
 
     cfg = wl.scaled(wl.CONFIGS["c2"], E=16, H=256, I=128, L=2, S=16)
-    cache = ExpertSlotCache(cfg, max_pairs=8)
+    cache = synthetic_cache(cfg, max_pairs=8)
     ptrs = [cache.host_ptrs[b][0] for b in range(cache.nb)]
     cpu = F.ftmoe_measure_cpu_moe(F.FMT_BF16, cfg.H, cfg.I, cfg.E, ptrs, [g.bytes for g in cache.schema], 8, 0, 2)
     be, fr = F.ftmoe_moe_backend_decision(F.FMT_BF16, max(mc, sm), cpu)
