@@ -9,6 +9,7 @@
 // so the compiler can vectorise the inner loops for the host's SIMD units, and split
 // over std::thread workers (gate_up + SiLU * up for every CPU pair, then down).
 #include <algorithm>
+#include <chrono>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -16,6 +17,9 @@
 #include <vector>
 
 #include "ftmoe.h"
+
+// records the library's thread-local error message (defined with the other entry points)
+int ftmoe_probe_report(int code, const char *msg);
 
 namespace {
 
@@ -208,5 +212,43 @@ extern "C" int ftmoe_cpu_expert_ffn(int32_t format, int32_t H, int32_t I, int32_
         const float w = h_weights[p];
         for (int64_t n = 0; n < H; n++) h_y[t * H + n] += w * os[i * H + n];
     }
+    return FTMOE_OK;
+}
+
+// STREAM-style read ceiling of the host memory the CPU executor reads (benchmark guide,
+// section 5.2: the bandwidth probe reports the CPU's memory read ceiling beside the link's).
+// Each worker sums its contiguous share of the buffer as 64-bit words into eight independent
+// accumulators (no dependency chain, so the loads stream at the memory system's rate); the
+// result is folded into a volatile sink so the reads cannot be dropped.
+extern "C" int ftmoe_measure_cpu_read(const void *h_buf, size_t bytes, int32_t threads, int32_t reps,
+                                      double *gbps) {
+    if (!h_buf || !gbps || bytes < 64 || reps <= 0)
+        return ftmoe_probe_report(FTMOE_ERR_INVALID_ARG, "measure_cpu_read: NULL pointer, bytes < 64 or reps <= 0");
+    if (threads <= 0) threads = static_cast<int>(std::max(1u, std::thread::hardware_concurrency()));
+    const uint64_t *w = static_cast<const uint64_t *>(h_buf);
+    const int64_t nw = static_cast<int64_t>(bytes / 64) * 8;  // whole 64-byte lines
+    static volatile uint64_t sink;
+    double best = 1e30;
+    for (int r = 0; r < reps; r++) {
+        std::vector<uint64_t> part(static_cast<size_t>(threads), 0);
+        const auto t0 = std::chrono::steady_clock::now();
+        parallel_for(threads, threads, [&](int64_t a, int64_t b) {
+            for (int64_t t = a; t < b; t++) {
+                const int64_t lo = nw / 8 * t / threads * 8, hi = nw / 8 * (t + 1) / threads * 8;
+                uint64_t s0 = 0, s1 = 0, s2 = 0, s3 = 0, s4 = 0, s5 = 0, s6 = 0, s7 = 0;
+                for (int64_t i = lo; i < hi; i += 8) {
+                    s0 += w[i]; s1 += w[i + 1]; s2 += w[i + 2]; s3 += w[i + 3];
+                    s4 += w[i + 4]; s5 += w[i + 5]; s6 += w[i + 6]; s7 += w[i + 7];
+                }
+                part[static_cast<size_t>(t)] = s0 ^ s1 ^ s2 ^ s3 ^ s4 ^ s5 ^ s6 ^ s7;
+            }
+        });
+        const auto t1 = std::chrono::steady_clock::now();
+        uint64_t x = 0;
+        for (uint64_t v : part) x ^= v;
+        sink = x;
+        best = std::min(best, std::chrono::duration<double>(t1 - t0).count());
+    }
+    *gbps = static_cast<double>(nw) * 8.0 / best / 1e9;
     return FTMOE_OK;
 }

@@ -25,6 +25,7 @@
 // FTMOE_ERR_STATE in the status word and leaves, and the producer waits (again
 // bounded) for its own copies in flight before it exits.
 #include "ffn_common.cuh"
+#include "ffn_fold.cuh"
 #include "internal.cuh"
 
 namespace ftmoe {
@@ -50,7 +51,7 @@ constexpr int kMaxTok = 4;  // tokens per stage
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any healthy wait
 
 struct StageHdr {
-    int32_t slot, n0, rows, ntok, done, pad0, pad1, pad2;
+    int32_t slot, n0, rows, ntok, done, tile, pad1, pad2;
     int32_t pairs[kMaxTok];
     int32_t texp[kMaxTok];  // per-token exponent of the f16 activations (nvfp4 gate_up)
 };
@@ -430,6 +431,7 @@ __global__ void __launch_bounds__(kTmaThreads<FMT, PHASE>, 1) ffn_rows_tma_kerne
     uint64_t *full = reinterpret_cast<uint64_t *>(sm);
     uint64_t *empty = full + kMaxStages;
     StageHdr *hdr = reinterpret_cast<StageHdr *>(sm + 128);
+    __shared__ int s_done_warps[kMaxStages];  // folded combine: consumer warps done with each stage
     unsigned char *stage0 = sm + 128 + kMaxStages * sizeof(StageHdr);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -437,6 +439,7 @@ __global__ void __launch_bounds__(kTmaThreads<FMT, PHASE>, 1) ffn_rows_tma_kerne
         for (int s = 0; s < c.stages; s++) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumerWarps<FMT, PHASE>);
+            s_done_warps[s] = 0;
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -453,6 +456,7 @@ __global__ void __launch_bounds__(kTmaThreads<FMT, PHASE>, 1) ffn_rows_tma_kerne
         const int npass = nu > 0 ? *p.s.n_passes : 0;
         const int items = npass * c.tiles;
         const int first = blockIdx.x;
+        bool prefetched = PHASE != kGateUp;
         const uint64_t pol = evict_first_policy();
         const int H = p.H, I = p.I, R = c.R;
         const int nout = PHASE == kGateUp ? I : H;
@@ -478,7 +482,7 @@ __global__ void __launch_bounds__(kTmaThreads<FMT, PHASE>, 1) ffn_rows_tma_kerne
                     break;
                 }
                 StageHdr &hh = hdr[s];
-                hh.slot = slot; hh.n0 = n0; hh.rows = rows; hh.ntok = ntok; hh.done = 0;
+                hh.slot = slot; hh.n0 = n0; hh.rows = rows; hh.ntok = ntok; hh.done = 0; hh.tile = tile;
                 for (int i = 0; i < ntok; i++) {
                     hh.pairs[i] = p.s.upairs[off + g0 + i];
                     hh.texp[i] = (PHASE == kGateUp && kF16Act<FMT>) ? p.s.xexp[hh.pairs[i] / p.topk] : 0;
@@ -539,8 +543,13 @@ __global__ void __launch_bounds__(kTmaThreads<FMT, PHASE>, 1) ffn_rows_tma_kerne
                     bulk_g2s_plain(st + c.tok_off + i * c.tok_bytes, src, (uint32_t)c.tok_bytes, &full[s]);
                 }
                 issued++;
+                if (!prefetched) {  // once this CTA's weight stream has started
+                    fold::prefetch_down(p, nu);
+                    prefetched = true;
+                }
             }
         }
+        if (ok && !prefetched) fold::prefetch_down(p, nu);
         if (ok) {  // end marker
             const int s = issued % c.stages;
             if (mbar_wait(&empty[s], ((issued / c.stages) & 1) ^ 1)) {
@@ -586,6 +595,27 @@ __global__ void __launch_bounds__(kTmaThreads<FMT, PHASE>, 1) ffn_rows_tma_kerne
                 case 2: dn_consume<FMT, 2>(p, c, st, h); break;
                 case 3: dn_consume<FMT, 3>(p, c, st, h); break;
                 default: dn_consume<FMT, 4>(p, c, st, h); break;
+            }
+            if (p.s.ycnt) {
+                // folded combine: the last consumer warp done with the stage counts its tokens'
+                // o rows of the tile, and forms y of every token whose count is complete
+                __threadfence();  // this warp's o rows, before the stage is counted
+                __syncwarp();
+                int last = 0;
+                if (lane == 0) {
+                    last = atomicAdd(&s_done_warps[s], 1) == kConsumerWarps<FMT, PHASE> - 1;
+                    if (last) {
+                        s_done_warps[s] = 0;  // ready for the stage's next round
+                        __threadfence();
+                    }
+                }
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last) {
+                    uint32_t fin = lane == 0 ? fold::count_pairs(p, h.pairs, h.ntok, h.tile) : 0u;
+                    fin = __shfl_sync(0xffffffffu, fin, 0);
+                    for (int i = 0; i < h.ntok; i++)
+                        if (fin >> i & 1) fold::combine_rows(p, h.pairs[i] / p.topk, h.n0, h.n0 + h.rows, lane, 32);
+                }
             }
         }
         __syncwarp();
@@ -664,6 +694,15 @@ bool ffn_rows_tma_supported(const FfnParams &p) {
         return p.H % 256 == 0 && p.I % 256 == 0 && p.s.x16 && p.s.xexp && p.s.hmax &&
                make_cfg<FTMOE_FMT_Q4_0, kGateUp>(p, c) && make_cfg<FTMOE_FMT_Q4_0, kDown>(p, c);
     return false;
+}
+
+int ffn_rows_tma_down_rows(const FfnParams &p) {
+    TmaCfg c;
+    bool ok = false;
+    if (p.fmt == FTMOE_FMT_BF16) ok = make_cfg<FTMOE_FMT_BF16, kDown>(p, c);
+    else if (p.fmt == FTMOE_FMT_NVFP4) ok = make_cfg<FTMOE_FMT_NVFP4, kDown>(p, c);
+    else if (p.fmt == FTMOE_FMT_Q4_0) ok = make_cfg<FTMOE_FMT_Q4_0, kDown>(p, c);
+    return ok ? c.R : 0;
 }
 
 cudaError_t launch_ffn_rows_tma(const FfnParams &p, int num_sms, cudaStream_t st) {

@@ -34,7 +34,7 @@ EXPORTS = [
     "ftmoe_last_error", "ftmoe_expert_ffn_noalloc", "ftmoe_ensure_experts_hybrid", "ftmoe_hybrid_fetch_fraction",
     "ftmoe_expert_ffn_hybrid", "ftmoe_cpu_expert_ffn", "ftmoe_prefetch_layer", "ftmoe_prefill_layers",
     "ftmoe_measure_link", "ftmoe_measure_cpu_moe", "ftmoe_moe_backend_decision", "ftmoe_get_counters",
-    "ftmoe_set_ffn_kernels", "ftmoe_ffn_kernels_for",
+    "ftmoe_set_ffn_kernels", "ftmoe_ffn_kernels_for", "ftmoe_measure_cpu_read",
 ]
 BACKEND_OFFLOAD, BACKEND_HYBRID = 0, 1
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -94,6 +94,7 @@ def lib() -> ctypes.CDLL:
         "ftmoe_prefill_layers": [P, i32, P, P, i32, i32, P, P, P, P, P],
         "ftmoe_measure_link": [P, P, sz, i32, P, P, P],
         "ftmoe_measure_cpu_moe": [i32, i32, i32, i32, P, P, i32, i32, i32, P],
+        "ftmoe_measure_cpu_read": [P, sz, i32, i32, P],
         "ftmoe_moe_backend_decision": [i32, ctypes.c_double, ctypes.c_double, ctypes.c_double, P, P],
         "ftmoe_get_counters": [P, P, i32, P],
     }
@@ -263,6 +264,13 @@ def ftmoe_measure_cpu_moe(fmt: int, H: int, I: int, E: int, layer_banks: Sequenc
     _check(lib().ftmoe_measure_cpu_moe(fmt, H, I, E, (ctypes.c_void_p * nb)(*layer_banks),
                                        (ctypes.c_int64 * nb)(*bank_bytes), experts, threads, reps,
                                        ctypes.byref(out)))
+    return out.value
+
+
+def ftmoe_measure_cpu_read(h_buf: int, nbytes: int, threads: int, reps: int) -> float:
+    """STREAM-style host memory read ceiling (GB/s) over the host buffer at h_buf."""
+    out = ctypes.c_double(0)
+    _check(lib().ftmoe_measure_cpu_read(h_buf, nbytes, threads, reps, ctypes.byref(out)))
     return out.value
 
 

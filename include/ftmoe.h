@@ -311,6 +311,14 @@ int ftmoe_measure_cpu_moe(int32_t format, int32_t H, int32_t I, int32_t E, const
                           const int64_t *bank_bytes, int32_t experts, int32_t threads, int32_t reps,
                           double *gbps);
 
+/* CPU memory read ceiling (benchmark guide, section 5.2: the bandwidth probe reports the
+ * host CPU's memory read ceiling, the bound of the CPU MoE kernel, beside the link's).
+ * `threads` workers (<= 0: all hardware threads) each sum a contiguous share of the host
+ * buffer h_buf (whole 64-byte lines of its first `bytes` bytes; any host memory, e.g. a
+ * layer's bank) as 64-bit words; best of `reps`; *gbps = bytes read / time / 1e9. Host
+ * only, synchronous. FTMOE_ERR_INVALID_ARG for NULL pointers, bytes < 64 or reps <= 0. */
+int ftmoe_measure_cpu_read(const void *h_buf, size_t bytes, int32_t threads, int32_t reps, double *gbps);
+
 /* Backend decision (benchmark guide, section 5.2): FTMOE_BACKEND_HYBRID when the format has
  * a CPU MoE path and cpu_gbps > threshold * link_gbps (threshold <= 0: the default 2.0),
  * with *fetch_fraction from ftmoe_hybrid_fetch_fraction; otherwise FTMOE_BACKEND_OFFLOAD

@@ -100,7 +100,6 @@ def test_hybrid_step_matches_oracle(key, geo, bs, mr, max_fetch):
     F.ftmoe_expert_ffn_hybrid(cache.handle, d_x.data_ptr(), bs, d_slots.data_ptr(), d_w.data_ptr(), cfg.topk,
                               d_add.data_ptr(), d_y.data_ptr(), st)
     assert cache.status() == F.OK
-    toks = list(range(min(bs, 4)))
-    ref = oracle_ffn(cache, 0, r.topk_ids, r.weights, r.x, toks)
-    assert_ffn_close(bf16_to_f64(d_y)[toks], ref, f"hybrid {key} bs={bs}")
+    ref = oracle_ffn(cache, 0, r.topk_ids, r.weights, r.x)
+    assert_ffn_close(bf16_to_f64(d_y), ref, f"hybrid {key} bs={bs}")
     cache.close()

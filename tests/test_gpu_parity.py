@@ -274,6 +274,63 @@ def test_ffn_small_geometries(fmt, geo):
     cache.close()
 
 
+FOLD = [
+    ("bf16", F.FFN_ROWS, dict(E=6, H=1024, I=256, L=2, S=6), 3),
+    ("bf16", F.FFN_MMA, dict(E=6, H=1024, I=256, L=2, S=6), 3),
+    ("bf16", F.FFN_MMA, dict(E=20, H=512, I=768, L=2, S=20), 30),   # 120 pairs: no split
+    ("nvfp4", F.FFN_AUTO, dict(E=5, H=2048, I=512, L=2, S=5), 4),
+    ("q4_0", F.FFN_AUTO, dict(E=6, H=512, I=256, L=2, S=6), 4),
+    ("mxfp4", F.FFN_AUTO, dict(E=5, H=576, I=320, L=2, S=5), 4),
+    ("mxfp4", F.FFN_AUTO, dict(E=9, H=2880, I=2880, L=2, S=9), 1),  # mxfp4 layer shape at one token
+    ("fp8", F.FFN_AUTO, dict(E=5, H=1024, I=1536, L=2, S=5), 4),
+]
+
+
+@pytest.mark.parametrize("fmt,kind,geo,bs", FOLD)
+def test_ffn_folded_combine_and_split(fmt, kind, geo, bs):
+    """The weighted combine formed inside the down kernels and the split reduction axis of
+    small calls: a token with every position computed elsewhere (y = its addend), a token
+    routed twice to one expert, the other positions on the GPU, against the oracle plus the
+    addend; two calls in a row give identical bits (the arrival counters start from zero
+    every call)."""
+    base = {"bf16": "c2", "nvfp4": "c3", "mxfp4": "c4", "fp8": "c6", "q4_0": "c7"}[fmt]
+    cfg = wl.scaled(wl.CONFIGS[base], topk=3, **geo)
+    cache = synthetic_cache(cfg, bs * cfg.topk)
+    if kind != F.FFN_AUTO:
+        cache.set_ffn_kernels(kind)
+    rng = np.random.default_rng(geo["E"] * 131 + bs)
+    ids = np.stack([rng.choice(cfg.E, cfg.topk, replace=False) for _ in range(bs)]).astype(np.int32)
+    if bs > 1:
+        ids[1] = [ids[1, 0]] * cfg.topk  # the same expert three times
+    w = rng.random((bs, cfg.topk)).astype(np.float32)
+    x = wl.f32_to_bf16_bits(rng.standard_normal((bs, cfg.H)).astype(np.float32))
+    slot_of = _install_all(cache, cfg, rng)
+    slots = np.vectorize(slot_of.get)(ids).astype(np.int32)
+    if bs > 2:
+        slots[2] = -1  # every position of token 2 elsewhere
+        slots[0, 1] = -1
+    add = (rng.standard_normal((bs, cfg.H)) * 0.1).astype(np.float32)
+    outs = []
+    for _ in range(2):
+        d_y = torch.empty((bs, cfg.H), dtype=torch.bfloat16, device="cuda")
+        d_add = to_dev(add)
+        d_x, d_s, d_w = x_dev(x), to_dev(slots), to_dev(w)
+        F.ftmoe_expert_ffn_hybrid(cache.handle, d_x.data_ptr(), bs, d_s.data_ptr(), d_w.data_ptr(), cfg.topk,
+                                  d_add.data_ptr(), d_y.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+        assert cache.status() == F.OK
+        outs.append(d_y.clone())
+    assert torch.equal(outs[0], outs[1])
+    w_gpu = np.where(slots >= 0, w, 0.0).astype(np.float32)
+    ref = oracle_ffn(cache, 0, ids, w_gpu, x) + add.astype(np.float64)
+    y = bf16_to_f64(outs[0])
+    assert_ffn_close(y, ref, f"{fmt} kind={kind} {geo} bs={bs}")
+    if bs > 2:  # the addend alone, rounded once
+        want = torch.from_numpy(add[2]).to(torch.bfloat16).float().numpy()
+        assert np.array_equal(outs[0][2].float().cpu().numpy(), want)
+    cache.close()
+
+
 def _install_all(cache, cfg, rng):
     perm = rng.permutation(cfg.S)
     slot_of = {e: int(perm[e]) for e in range(cfg.E)}
