@@ -808,8 +808,14 @@ def hybrid_probe(args, cfg, cache, stream, torch, F, wl, link_gbps, cores):
     # (ftmoe_moe_backend_decision, default threshold 2x)
     k = cfg.topk
     cpu_gbps = F.ftmoe_measure_cpu_moe(fmt, cfg.H, cfg.I, cfg.E, bank_ptrs, bank_bytes, 2 * k, cores, 3)
+    # STREAM-style read ceiling of the host memory the executor reads (the layer's largest bank)
+    big = max(range(cache.nb), key=lambda b: bank_bytes[b])
+    read_bytes = min(cfg.E * bank_bytes[big], 2 << 30)
+    cpu_read = F.ftmoe_measure_cpu_read(bank_ptrs[big], read_bytes, cores, 3)
     backend, frac = F.ftmoe_moe_backend_decision(fmt, link_gbps, cpu_gbps, 0.0)
-    out = {"cpu_moe_GBps": cpu_gbps, "link_GBps": link_gbps, "cores": cores,
+    out = {"cpu_moe_GBps": cpu_gbps, "cpu_read_ceiling_GBps": cpu_read,
+           "cpu_moe_frac_of_read_ceiling": cpu_gbps / cpu_read if cpu_read > 0 else None,
+           "link_GBps": link_gbps, "cores": cores,
            "decision": "hybrid" if backend == F.BACKEND_HYBRID else "offload",
            "fetch_fraction": F.ftmoe_hybrid_fetch_fraction(link_gbps, cpu_gbps)}
 

@@ -68,3 +68,15 @@ def test_fetch_fraction_helper(lib):
     assert F.ftmoe_hybrid_fetch_fraction(0.0, 800.0) == 0.0
     with pytest.raises(F.FtmoeError):
         F.ftmoe_cpu_expert_ffn(9, 64, 32, 1, 1, 0, 0, [0, 0], [1, 1], 0, 0, 0, 1)
+
+
+def test_cpu_read_ceiling_probe(lib):
+    """The STREAM-style host read probe runs on the host cores: a positive rate for a real
+    buffer, host-side argument errors otherwise."""
+    buf = np.arange(1 << 22, dtype=np.uint8)
+    gbps = F.ftmoe_measure_cpu_read(buf.ctypes.data, buf.nbytes, 2, 2)
+    assert 0.1 < gbps < 1e5
+    for args in ((0, buf.nbytes, 1, 1), (buf.ctypes.data, 32, 1, 1), (buf.ctypes.data, buf.nbytes, 1, 0)):
+        with pytest.raises(F.FtmoeError) as e:
+            F.ftmoe_measure_cpu_read(*args)
+        assert e.value.code == F.ERR_INVALID_ARG
