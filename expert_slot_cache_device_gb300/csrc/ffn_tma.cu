@@ -219,14 +219,17 @@ __device__ __forceinline__ void gu_consume(const FfnParams &p, const TmaCfg &c, 
                 }
             }
         } else if (FMT == FTMOE_FMT_Q4_0) {
-            // lane step = one 32-element Q4_0 block of the gate and of the up row: nibbles ->
-            // exact f16x2 (nibble - 8), 32 exact f16 products summed in two f16 halves of
-            // sixteen, the block's binary16 scale applied in fp32. Activations are staged in
-            // the swz_q4x16 layout: unit u of this lane's block sits at u ^ ((b >> 1) & 3).
+            // lane step = one 32-element Q4_0 block of the gate and of the up row (blocks in
+            // the q4_lane_block order): nibbles -> exact f16x2 (nibble - 8), 32 exact f16
+            // products summed in two f16 halves of sixteen, the block's binary16 scale applied
+            // in fp32. Activations are staged in the swz_q4x16 layout: unit u of block b sits
+            // at u ^ ((b >> 2) & 3).
             const unsigned char *rg = st + j * wr, *ru = st + (R + j) * wr;
             const int nb = H >> 5;
-            const int rot = (lane >> 1) & 3;
-            for (int b = lane; b < nb; b += 32) {
+            for (int bi = 0; bi < ((nb + 63) & ~63); bi += 32) {
+                const int b = (bi & ~63) + q4_lane_block(lane, (bi >> 5) & 1);
+                if (b >= nb) continue;
+                const int rot = (b >> 2) & 3;
                 uint32_t dg, du, qg[4], qu[4], fa[16], fb[16];
                 q4_block(rg, b, dg, qg);
                 q4_block(ru, b, du, qu);
@@ -337,16 +340,19 @@ __device__ __forceinline__ void dn_consume(const FfnParams &p, const TmaCfg &c, 
                 }
             }
         } else if (FMT == FTMOE_FMT_Q4_0) {
-            // lane step = one 32-element Q4_0 block of RR rows; h is converted once per
-            // block and token to f16 with the token's power-of-two scale (max |h| < 2^8),
-            // shared by the RR rows. The h rows are staged in the swz_q4h32 layout: unit u of
-            // this lane's block sits at u ^ (b & 7), so the 8 lanes of a phase hit 8 units.
+            // lane step = one 32-element Q4_0 block of RR rows (blocks in the q4_lane_block
+            // order); h is converted once per block and token to f16 with the token's
+            // power-of-two scale (max |h| < 2^8), shared by the RR rows. The h rows are staged
+            // in the swz_q4h32 layout: unit u of block b sits at u ^ ((b >> 1) & 7), so the 8
+            // lanes of a phase hit 8 units.
             const int nb = I >> 5;
-            const int rot = lane & 7;
             float hsc[NT];
 #pragma unroll
             for (int t = 0; t < NT; t++) hsc[t] = ldexpf(1.f, -h.texp[t]);
-            for (int b = lane; b < nb; b += 32) {
+            for (int bi = 0; bi < ((nb + 63) & ~63); bi += 32) {
+                const int b = (bi & ~63) + q4_lane_block(lane, (bi >> 5) & 1);
+                if (b >= nb) continue;
+                const int rot = (b >> 1) & 7;
                 uint32_t fw[RR][16], dr[RR];
 #pragma unroll
                 for (int r = 0; r < RR; r++) {
