@@ -303,6 +303,7 @@ def test_ffn_folded_combine_and_split(fmt, kind, geo, bs):
     if bs > 1:
         ids[1] = [ids[1, 0]] * cfg.topk  # the same expert three times
     w = rng.random((bs, cfg.topk)).astype(np.float32)
+    w /= w.sum(axis=1, keepdims=True)  # router probabilities: |y| stays O(1), as the tolerance assumes
     x = wl.f32_to_bf16_bits(rng.standard_normal((bs, cfg.H)).astype(np.float32))
     slot_of = _install_all(cache, cfg, rng)
     slots = np.vectorize(slot_of.get)(ids).astype(np.int32)
