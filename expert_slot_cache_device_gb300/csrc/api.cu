@@ -36,7 +36,7 @@ size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 struct Layout {
     size_t hdr, id2slot, owner, stamp, miss_ids, miss_slots, all_ids, pf_slots;
     size_t n_unique, uslot, ucnt, uoff, upairs, h, o, x16, xexp, hmax, upoff, pipe_slots;
-    size_t gcnt, ycnt, part, kcnt;
+    size_t gcnt, ycnt;
     size_t total;
     bool ffn;
 };
@@ -118,12 +118,9 @@ Layout make_layout(int fmt, int E, int L, int S, int H, int I, int max_pairs) {
         l.upoff = off; off += align256(P * 4);
         l.pipe_slots = off; off += 2 * align256(P * 4);  // two routed-slot buffers of the prefill pipeline
         // folded combine: pairs with a slot per token, arrival counts per (token, row tile of
-        // at least 8 rows); split items: partial sums and arrival counts per (pass, tile)
-        const size_t wide = (size_t)(2 * I > H ? 2 * I : H);
+        // at least 8 rows)
         l.gcnt = off; off += align256(P * 4);
         l.ycnt = off; off += align256(P * (size_t)((H + 7) / 8) * 4);
-        l.part = off; off += align256((size_t)kSplitMax * kSplitPairs * wide * 4);
-        l.kcnt = off; off += align256(2 * (size_t)kSplitPairs * ((wide + 31) / 32) * 4);
     }
     l.total = off;
     return l;
@@ -294,8 +291,6 @@ int ftmoe_cache_create(const ftmoe_bank_spec *banks, int32_t num_banks, int32_t 
         c->s.n_passes = c->s.n_unique + 1;  // second word of the 256-byte n_unique block
         c->s.gcnt = reinterpret_cast<int32_t *>(ws + lay.gcnt);
         c->s.ycnt = reinterpret_cast<int32_t *>(ws + lay.ycnt);
-        c->s.part = reinterpret_cast<float *>(ws + lay.part);
-        c->s.kcnt = reinterpret_cast<int32_t *>(ws + lay.kcnt);
     }
     if (format == FTMOE_FMT_MXFP4 && lay.ffn) {
         const unsigned char *sb[6];

@@ -43,9 +43,6 @@ constexpr int kGuNeurons = 16; // gate_up rows kernel: neurons per CTA (2 per wa
 constexpr int kDnRows = 32;    // down rows kernel: output rows per CTA
 constexpr int kColTile = 128;  // transposed kernels: columns per CTA (4 per lane)
 constexpr int kYTileMin = 8;   // smallest down row tile with a folded combine (ycnt holds H / 8 per token)
-// Down weights of a call prefetched into L2 while gate_up runs when they total at most this
-// (about three quarters of the 126 MB L2; gate_up streams its weights with evict-first).
-constexpr int64_t kL2PrefetchBytes = 96ll << 20;
 
 // ------------------------------------------------------------------------ route
 
@@ -125,11 +122,9 @@ __global__ void __launch_bounds__(1024) ffn_route_kernel(FfnParams p) {
     for (int s = tid; s < p.S; s += nt) cnt[s] = 0;
     if (p.s.hmax)
         for (int q = tid; q < p.P; q += nt) p.s.hmax[q] = 0u;
-    // arrival counters of the folded combine and of split items start every call at zero
+    // arrival counters of the folded combine start every call at zero
     if (p.s.ycnt)
-        for (int i = tid; i < p.ysplit_words; i += nt) p.s.ycnt[i] = 0;
-    if (p.s.kcnt)
-        for (int i = tid; i < 2 * p.kcnt_words; i += nt) p.s.kcnt[i] = 0;
+        for (int i = tid; i < p.ycnt_words; i += nt) p.s.ycnt[i] = 0;
     __syncthreads();
     for (int q = tid; q < p.P; q += nt) {
         int s = p.slots[q];
@@ -798,42 +793,16 @@ cudaError_t launch_ffn(const FfnParams &p_in, int num_sms, cudaStream_t st, cons
     p.x16_swz = fp4_rows_tma && p.fmt == FTMOE_FMT_NVFP4 ? 1 : (fp4_rows_tma && p.fmt == FTMOE_FMT_Q4_0 ? 2 : 0);
     p.pass_tokens = (mx_tma || fp8_tma || bf16_mma) ? kMxPassTokens : kPassTokens;
     const bool pipeline = bf16_mma || fp4_rows_tma || mx_tma || fp8_tma;
-    // Folded combine: the down items' row tile (the last item to finish a token's tile forms y)
-    int ytile = 0, tiles[2] = {0, 0}, kst[2] = {0, 0};
-    for (int ph = 0; ph < 2; ph++) {
-        if (bf16_mma || fp8_tma) ffn_rows_mma_shape(p, ph, tiles[ph], kst[ph], ytile);
-        else if (mx_tma) ffn_mx_tma_shape(p, ph, tiles[ph], kst[ph], ytile);
-    }
-    if (fp4_rows_tma) ytile = ffn_rows_tma_down_rows(p);
+    // Folded combine: the down kernel's item rows are the tile of its arrival counts (the CTA
+    // completing a token's tile forms y there at exit); other kernels use the combine kernel
+    const int ytile = (bf16_mma || fp8_tma) ? ffn_rows_mma_down_rows()
+                      : mx_tma              ? ffn_mx_tma_down_rows()
+                      : fp4_rows_tma        ? ffn_rows_tma_down_rows(p)
+                                            : 0;
     const bool fold = pipeline && p.s.gcnt && p.s.ycnt && ytile >= kYTileMin;
     p.ytiles = fold ? (p.H + ytile - 1) / ytile : 0;
-    p.ysplit_words = fold ? p.bs * p.ytiles : 0;
+    p.ycnt_words = fold ? p.bs * p.ytiles : 0;
     if (!fold) p.s.gcnt = p.s.ycnt = nullptr;
-    // Split reduction axis of the tensor-map pipelines when a call has fewer items than about
-    // two per SM: the smallest split (at most kSplitMax chunks, at least one stage each) that
-    // reaches it, counting one pass per routed pair (an upper bound on the passes)
-    p.ksplit_gu = p.ksplit_dn = 1;
-    p.kcnt_words = 0;
-    p.split_row = 2 * p.I > p.H ? 2 * p.I : p.H;
-    if ((bf16_mma || fp8_tma || mx_tma) && p.s.part && p.s.kcnt && p.P <= kSplitPairs) {
-        const int64_t npass_max = p.P < p.S ? p.P : p.S;
-        int ks[2];
-        for (int ph = 0; ph < 2; ph++) {
-            ks[ph] = 1;
-            while (ks[ph] < kSplitMax && ks[ph] < kst[ph] && npass_max * tiles[ph] * ks[ph] < 2 * (int64_t)num_sms)
-                ks[ph]++;
-        }
-        p.ksplit_gu = ks[0];
-        p.ksplit_dn = ks[1];
-        if (ks[0] > 1 || ks[1] > 1) p.kcnt_words = kSplitPairs * (tiles[0] > tiles[1] ? tiles[0] : tiles[1]);
-    }
-    // L2 prefetch of the down weights by gate_up (small calls; see fold::prefetch_down)
-    p.l2_prefetch = pipeline ? kL2PrefetchBytes : 0;
-    switch (p.fmt) {
-        case FTMOE_FMT_BF16: case FTMOE_FMT_Q4_0: p.dn_b0 = 1; p.dn_nb = 1; break;
-        case FTMOE_FMT_FP8: p.dn_b0 = 2; p.dn_nb = 2; break;
-        default: p.dn_b0 = 3; p.dn_nb = 3; break;  // nvfp4, mxfp4
-    }
     {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(1 + (want_x16 ? p.bs : 0));

@@ -56,8 +56,7 @@ static_assert(kMxTokMax == kMxPassTokens, "the routing kernel cuts passes of kMx
 enum { kGU = 0, kDN = 1 };
 
 struct MxHdr {
-    int32_t slot, n0, kstage, rows, ntok, last, done, kc;
-    int32_t item, tile, pad0, pad1;  // (pass, tile) index and column tile of the item
+    int32_t slot, n0, kstage, rows, ntok, last, done, pad;
     int32_t pairs[kMxTokMax];
     int32_t texp[kMxTokMax];
 };
@@ -67,7 +66,6 @@ struct MxHdr {
 // bias [NM][kCols] bf16 at bias_off (filled on an item's last stage).
 struct MxCfg {
     int32_t tiles, kst, stages, stage_bytes, tok_off, tok_stride, sc_off, tg, red_off, bias_off;
-    int32_t ksplit;  // chunks of the reduction axis per (pass, tile) (1: whole items)
 };
 
 // Shared-memory byte of logical (row, byte) of a 128-byte-swizzled code tile whose base
@@ -153,7 +151,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     extern __shared__ __align__(1024) unsigned char sm[];
     uint64_t *full = reinterpret_cast<uint64_t *>(sm);
     uint64_t *empty = full + kMxStagesMax;
-    uint64_t *rbar = empty + kMxStagesMax;  // [5] consumer barriers around the reduction
+    uint64_t *rbar = empty + kMxStagesMax;  // [5] consumer barriers: reduction [0..2], exit [3..4]
     MxHdr *hdr = reinterpret_cast<MxHdr *>(sm + 256);
     // stages start at the first 1024-byte aligned shared address after the headers (the
     // 128-byte swizzle pattern of the code tiles repeats every 1024 bytes)
@@ -173,7 +171,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         for (int b = 0; b < 5; b++) bar_init(&rbar[b], kCW);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    __shared__ int s_last;  // split items: this CTA's chunk was the last of its item to arrive
+    __shared__ fold::ExitQueue s_q;  // down: rows of y this CTA forms at exit
     __syncthreads();
     if (PHASE == kGU) asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" :::);
@@ -182,8 +180,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         if (lane != 0) return;
         const int nu = *p.s.n_unique;
         const int npass = nu > 0 ? *p.s.n_passes : 0;
-        const int items = npass * c.tiles * c.ksplit;
-        bool prefetched = PHASE != kGU;
+        const int items = npass * c.tiles;
         // items are dealt round-robin, so at any moment the CTAs hold neighbouring column
         // tiles of the same expert rows and a 128-byte line shared by two tiles (the up
         // half starts 64 bytes into a line when I is an odd multiple of 64) is still in L2
@@ -193,13 +190,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         int issued = 0;
         const uint64_t pol = evict_first_l2();  // weights are read once
         const uint32_t box_bytes = NM * (kKp * kCols + (kKp / 16) * kCols);
-        int u = items > first ? pass_owner(p.s.upoff, nu, first / (c.tiles * c.ksplit)) : 0;
+        int u = items > first ? pass_owner(p.s.upoff, nu, first / c.tiles) : 0;
         int cur_pi = -1, slot = 0, cnt = 0;
         int pairs_c[kMxTokMax], texp_c[kMxTokMax];
         for (int it = first; it < items && ok; it += gridDim.x) {
-            // the chunks of one (pass, tile) are adjacent items, so they run side by side
-            const int kc = it % c.ksplit, it2 = it / c.ksplit;
-            const int pi = it2 / c.tiles, tile = it2 - pi * c.tiles;
+            const int pi = it / c.tiles, tile = it - pi * c.tiles;
             if (pi != cur_pi) {  // new pass: advance the owner and cache its tokens
                 while (u + 1 < nu && p.s.upoff[u + 1] <= pi) u++;
                 cur_pi = pi;
@@ -232,8 +227,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             const int n0 = tile * kCols;
             {
                 const int ntok = cnt;
-                const int ks0 = kc * c.kst / c.ksplit, ks1 = (kc + 1) * c.kst / c.ksplit;
-                for (int ks = ks0; ks < ks1 && ok; ks++) {
+                for (int ks = 0; ks < c.kst && ok; ks++) {
                     const int s = issued % c.stages;
                     if (!bar_wait(&empty[s], ((issued / c.stages) & 1) ^ 1)) {
                         ok = false;
@@ -242,7 +236,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                     MxHdr &hh = hdr[s];
                     const int rows = K2 - ks * kKp < kKp ? K2 - ks * kKp : kKp;
                     hh.slot = slot; hh.n0 = n0; hh.kstage = ks; hh.rows = rows; hh.ntok = ntok;
-                    hh.last = ks == ks1 - 1; hh.done = 0; hh.kc = kc; hh.item = it2; hh.tile = tile;
+                    hh.last = ks == c.kst - 1; hh.done = 0;
                     for (int i = 0; i < kMxTokMax; i++) {
                         if (i >= ntok) break;
                         hh.pairs[i] = pairs_c[i];
@@ -278,14 +272,9 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                                    (uint32_t)(ncol * 2), &full[s]);
                     }
                     issued++;
-                    if (!prefetched) {  // once this CTA's weight stream has started
-                        fold::prefetch_down(p, nu);
-                        prefetched = true;
-                    }
                 }
             }
         }
-        if (ok && !prefetched) fold::prefetch_down(p, nu);
         if (ok) {
             const int s = issued % c.stages;
             if (bar_wait(&empty[s], ((issued / c.stages) & 1) ^ 1)) {
@@ -321,7 +310,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             return;
         }
         const MxHdr &hs = hdr[s];  // stays valid until this warp releases the stage
-        if (hs.done) return;
+        if (hs.done) {
+            if (PHASE == kDN && p.s.ycnt)  // the weighted combine of the tokens this CTA completes
+                fold::fold_at_exit(p, c.tiles, kCols, kMxTokMax, &rbar[3], &rbar[4], 0, &s_q, threadIdx.x, kCW * 32);
+            return;
+        }
         const int ntok = hs.ntok, rows = hs.rows;
         const bool last = hs.last;
         const unsigned char *st = stage0 + (size_t)s * c.stage_bytes;
@@ -371,81 +364,39 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             return;
         }
         const uint16_t *bias = reinterpret_cast<const uint16_t *>(st + c.bias_off);  // [NM][kCols], staged
-        const int n0 = hs.n0, kc = hs.kc, item = hs.item, tile = hs.tile;
-        int pr[kMxTokMax];  // the item's routed pairs (the header is reused once the stage is released)
-#pragma unroll
-        for (int i = 0; i < kMxTokMax; i++) pr[i] = i < ntok ? hs.pairs[i] : 0;
-        // outputs of this thread: (token t, column col) for i = threadIdx.x + r * kCW * 32; a
-        // warp's 32 threads share one token (ntok * kCols and the stride are multiples of 32)
-        float v[2][NM];
-#pragma unroll
-        for (int r = 0; r < 2; r++) {
-            const int i = threadIdx.x + r * kCW * 32;
-            if (i >= ntok * kCols) break;
+        const int n0 = hs.n0;
+        // ntok * kCols and the stride are multiples of 32, so a warp's 32 threads share
+        // one token t here and take the max |h| over their columns before a single
+        // atomic (every column doing its own atomic on the pair's word serialised on
+        // one L2 slice)
+        for (int i = threadIdx.x; i < ntok * kCols; i += kCW * 32) {
             const int t = i / kCols, col = i - t * kCols;
+            const int n = n0 + col;
+            const bool valid = n < nout;
             const float xs_t = ldexpf(1.f, hs.texp[t]);
+            float v[NM];
 #pragma unroll
             for (int m = 0; m < NM; m++) {
                 float sum = 0.f;
 #pragma unroll
                 for (int w = 0; w < kBlkPairs; w++) sum += red_i[((m * kBlkPairs + w) * kMxTokMax + t) * kCols + col];
-                v[r][m] = sum * xs_t;
-                if (c.ksplit > 1 && n0 + col < nout)  // this chunk's partial sum
-                    p.s.part[fold::part_index(p, kc, pr[t], m * nout + n0 + col)] = v[r][m];
+                v[m] = sum * xs_t;
             }
-        }
-        bool finish = true;
-        if (c.ksplit > 1) {
-            // the last chunk of the item to arrive adds every chunk's partials in chunk order
-            __threadfence();
-            if (!fold::consumer_sync(&rbar[3], rphase, p.status)) return;
-            if (threadIdx.x == 0)
-                s_last = fold::chunk_arrive(p.s.kcnt + PHASE * p.kcnt_words + item, c.ksplit);
-            if (!fold::consumer_sync(&rbar[4], rphase, p.status)) return;
-            finish = *reinterpret_cast<volatile int *>(&s_last) != 0;
-            if (finish) {
-#pragma unroll
-                for (int r = 0; r < 2; r++) {
-                    const int i = threadIdx.x + r * kCW * 32;
-                    if (i >= ntok * kCols) break;
-                    const int t = i / kCols, col = i - t * kCols;
-                    if (n0 + col >= nout) continue;
-#pragma unroll
-                    for (int m = 0; m < NM; m++) {
-                        float sum = 0.f;
-                        for (int k2 = 0; k2 < c.ksplit; k2++)
-                            sum += __ldcg(p.s.part + fold::part_index(p, k2, pr[t], m * nout + n0 + col));
-                        v[r][m] = sum;
-                    }
+            const int q = hs.pairs[t];
+            if (PHASE == kGU) {
+                float hv = 0.f;
+                if (valid) {
+                    const float gg = v[0] + __uint_as_float((uint32_t)bias[col] << 16);
+                    const float uu = v[NM - 1] + __uint_as_float((uint32_t)bias[(NM - 1) * kCols + col] << 16);
+                    hv = silu(gg) * uu;
+                    p.s.h[(int64_t)q * I + n] = hv;
                 }
+                const uint32_t wm = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv)));
+                if (lane == 0 && wm) atomicMax(&p.s.hmax[q], wm);
+            } else if (valid) {
+                p.s.o[(int64_t)q * H + n] = v[0] + __uint_as_float((uint32_t)bias[col] << 16);
             }
         }
-        if (finish) {
-#pragma unroll
-            for (int r = 0; r < 2; r++) {
-                const int i = threadIdx.x + r * kCW * 32;
-                if (i >= ntok * kCols) break;
-                const int t = i / kCols, col = i - t * kCols;
-                const int n = n0 + col;
-                const bool valid = n < nout;
-                const int q = pr[t];
-                if (PHASE == kGU) {
-                    float hv = 0.f;
-                    if (valid) {
-                        const float gg = v[r][0] + __uint_as_float((uint32_t)bias[col] << 16);
-                        const float uu = v[r][NM - 1] + __uint_as_float((uint32_t)bias[(NM - 1) * kCols + col] << 16);
-                        hv = silu(gg) * uu;
-                        p.s.h[(int64_t)q * I + n] = hv;
-                    }
-                    const uint32_t wm = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv)));
-                    if (lane == 0 && wm) atomicMax(&p.s.hmax[q], wm);
-                } else if (valid) {
-                    p.s.o[(int64_t)q * H + n] = v[r][0] + __uint_as_float((uint32_t)bias[col] << 16);
-                }
-            }
-        }
-        const bool fold_y = PHASE == kDN && p.s.ycnt && finish;
-        if (fold_y) __threadfence();  // this thread's o rows, before the item is counted
         __syncwarp();
         if (lane == 0) {
             bar_arrive(&rbar[1]);
@@ -454,15 +405,6 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         if (!bar_wait(&rbar[1], rphase)) {
             if (lane == 0) atomicCAS(p.status, 0, FTMOE_ERR_STATE);
             return;
-        }
-        if (fold_y && warp == 0) {
-            // the weighted combine of every token whose last routed pair for this column tile
-            // was this item's
-            uint32_t fin = lane == 0 ? fold::count_pairs(p, pr, ntok, tile) : 0u;
-            fin = __shfl_sync(0xffffffffu, fin, 0);
-            const int n1 = n0 + kCols < H ? n0 + kCols : H;
-            for (int i = 0; i < ntok; i++)
-                if (fin >> i & 1) fold::combine_rows(p, pr[i] / p.topk, n0, n1, lane, 32);
         }
         rphase ^= 1;
     }
@@ -475,9 +417,6 @@ bool make_mx_cfg(const FfnParams &p, int phase, MxCfg &c, size_t &smem) {
     c.tiles = (nout + kCols - 1) / kCols;
     c.kst = (K2 + kKp - 1) / kKp;
     c.tg = kMxTokMax;
-    c.ksplit = phase == kGU ? p.ksplit_gu : p.ksplit_dn;
-    if (c.ksplit < 1) c.ksplit = 1;
-    if (c.ksplit > c.kst) c.ksplit = c.kst;
     // token rows: 4 bytes (f16 pair) or 8 bytes (fp32 pair) per k-pair row; the stride is
     // padded by 32 / 64 bytes so the B-fragment loads of eight tokens hit distinct banks
     c.tok_stride = phase == kGU ? kKp * 4 + 32 : kKp * 8 + 64;
@@ -489,7 +428,8 @@ bool make_mx_cfg(const FfnParams &p, int phase, MxCfg &c, size_t &smem) {
     static_assert(kBlkPairs * kMxTokMax * kCols * 4 == kKp * kCols, "down partials fill one code tile");
     const size_t red = phase == kDN ? 0 : (size_t)NM * kBlkPairs * kMxTokMax * kCols * 4;
     const size_t head = 256 + kMxStagesMax * sizeof(MxHdr) + 1024;  // + alignment slack
-    const size_t cap = 227 * 1024 - 64;  // dynamic shared memory, leaving room for the static words
+    // dynamic shared memory; the static exit queue takes 3 KB (padded to the 1024-byte alignment)
+    const size_t cap = 227 * 1024 - 4096;
     int stages = kMxStagesMax;
     while (stages >= 2 && head + (size_t)stages * c.stage_bytes + red > cap) stages--;
     if (stages < 2) return false;
@@ -530,12 +470,7 @@ bool ffn_mx_tma_supported(const FfnParams &p, const MxTmaMaps *maps) {
            p.H % 32 == 0 && p.I % 32 == 0;
 }
 
-void ffn_mx_tma_shape(const FfnParams &p, int phase, int &tiles, int &kst, int &row_tile) {
-    const int K2 = (phase == kGU ? p.H : p.I) / 2, nout = phase == kGU ? p.I : p.H;
-    tiles = (nout + kCols - 1) / kCols;
-    kst = (K2 + kKp - 1) / kKp;
-    row_tile = kCols;
-}
+int ffn_mx_tma_down_rows() { return kCols; }
 
 cudaError_t launch_ffn_mx_tma(const FfnParams &p, const MxTmaMaps &maps, int num_sms, cudaStream_t st) {
     cudaError_t e = launch_mx<kGU>(p, maps, num_sms, st);

@@ -77,8 +77,7 @@ static_assert(kFTok * kFRows <= kFCW * 32, "one epilogue output per consumer thr
 enum { kGU = 0, kDN = 1 };
 
 struct F8Hdr {
-    int32_t slot, n0, kstage, ntok, last, done, kc, item;  // item: (pass, tile) index
-    int32_t tile, pad0, pad1, pad2;
+    int32_t slot, n0, kstage, ntok, last, done, pad0, pad1;
     int32_t pairs[kFTok];
     int32_t texp[kFTok];
 };
@@ -88,7 +87,6 @@ struct F8Hdr {
 // padded stride (bf16 down: planes hi and lo, tok_plane bytes apart).
 struct F8Cfg {
     int32_t tiles, kst, stages, stage_bytes, sc_off, sc_bytes, tok_off, tok_stride, tok_plane, red_off;
-    int32_t ksplit;  // chunks of the reduction axis per (pass, tile) (1: whole items)
 };
 
 __device__ __forceinline__ int swz(int row, int byte) { return row * kFBox + (byte ^ ((row & 7) << 4)); }
@@ -251,7 +249,7 @@ __device__ __forceinline__ void rows_mma_body(const FfnParams &p, const F8Cfg &c
     extern __shared__ __align__(1024) unsigned char sm[];
     uint64_t *full = reinterpret_cast<uint64_t *>(sm);
     uint64_t *empty = full + kFStagesMax;
-    uint64_t *rbar = empty + kFStagesMax;  // [4] consumer barriers around the reduction
+    uint64_t *rbar = empty + kFStagesMax;  // [4] consumer barriers: reduction [0..1], exit [2..3]
     F8Hdr *hdr = reinterpret_cast<F8Hdr *>(sm + 256);
     const uint32_t hdr_end = su32(sm) + 256 + kFStagesMax * sizeof(F8Hdr);
     unsigned char *stage0 = sm + (((hdr_end + 1023u) & ~1023u) - su32(sm));
@@ -269,7 +267,7 @@ __device__ __forceinline__ void rows_mma_body(const FfnParams &p, const F8Cfg &c
         for (int b = 0; b < 4; b++) bar_init(&rbar[b], kFCW);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    __shared__ int s_last;  // split items: this CTA's chunk was the last of its item to arrive
+    __shared__ fold::ExitQueue s_q;  // down: rows of y this CTA forms at exit
     __syncthreads();
     if (PHASE == kGU) asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" :::);
@@ -278,10 +276,9 @@ __device__ __forceinline__ void rows_mma_body(const FfnParams &p, const F8Cfg &c
         if (lane != 0) return;
         const int nu = *p.s.n_unique;
         const int npass = nu > 0 ? *p.s.n_passes : 0;
-        const int items = npass * c.tiles * c.ksplit;
+        const int items = npass * c.tiles;
         // items dealt round-robin: the passes of one expert run side by side and share L2
         const int first = blockIdx.x;
-        bool prefetched = PHASE != kGU;
         bool waited = PHASE == kGU, ok = true;
         int issued = 0;
         const uint64_t pol = evict_first_l2();  // weights are read once
@@ -289,15 +286,13 @@ __device__ __forceinline__ void rows_mma_body(const FfnParams &p, const F8Cfg &c
         // token bytes per stage and plane: f16 x / fp32 h (block FP8), bf16 x / h terms (bf16)
         const uint32_t tb = WK == kWE4M3 ? kFKs * (PHASE == kGU ? 2u : 4u) : kFKs * 2u;
         const int planes = WK == kWBF16 && PHASE == kDN ? 2 : 1;
-        int u = items > first ? pass_owner(p.s.upoff, nu, first / (c.tiles * c.ksplit)) : 0;
+        int u = items > first ? pass_owner(p.s.upoff, nu, first / c.tiles) : 0;
         int cur_pi = -1, slot = 0, cnt = 0;
         int pairs_c[kFTok], texp_c[kFTok];
         const unsigned char *scb = WK == kWE4M3 ? p.bank[PHASE == kGU ? 1 : 3] : nullptr;
         const int64_t scb_bytes = WK == kWE4M3 ? p.bank_bytes[PHASE == kGU ? 1 : 3] : 0;
         for (int it = first; it < items && ok; it += gridDim.x) {
-            // the chunks of one (pass, tile) are adjacent items, so they run side by side
-            const int kc = it % c.ksplit, it2 = it / c.ksplit;
-            const int pi = it2 / c.tiles, tile = it2 - pi * c.tiles;
+            const int pi = it / c.tiles, tile = it - pi * c.tiles;
             if (pi != cur_pi) {  // new pass: advance the owner and cache its tokens
                 while (u + 1 < nu && p.s.upoff[u + 1] <= pi) u++;
                 cur_pi = pi;
@@ -330,8 +325,7 @@ __device__ __forceinline__ void rows_mma_body(const FfnParams &p, const F8Cfg &c
                 }
             }
             const int n0 = tile * kFRows;
-            const int ks0 = kc * c.kst / c.ksplit, ks1 = (kc + 1) * c.kst / c.ksplit;
-            for (int ks = ks0; ks < ks1 && ok; ks++) {
+            for (int ks = 0; ks < c.kst && ok; ks++) {
                 const int s = issued % c.stages;
                 if (!bar_wait(&empty[s], ((issued / c.stages) & 1) ^ 1)) {
                     ok = false;
@@ -339,7 +333,7 @@ __device__ __forceinline__ void rows_mma_body(const FfnParams &p, const F8Cfg &c
                 }
                 F8Hdr &hh = hdr[s];
                 hh.slot = slot; hh.n0 = n0; hh.kstage = ks; hh.ntok = cnt;
-                hh.last = ks == ks1 - 1; hh.done = 0; hh.kc = kc; hh.item = it2; hh.tile = tile;
+                hh.last = ks == c.kst - 1; hh.done = 0;
                 for (int i = 0; i < kFTok; i++) {
                     if (i >= cnt) break;
                     hh.pairs[i] = pairs_c[i];
@@ -373,13 +367,8 @@ __device__ __forceinline__ void rows_mma_body(const FfnParams &p, const F8Cfg &c
                     }
                 }
                 issued++;
-                if (!prefetched) {  // once this CTA's weight stream has started
-                    fold::prefetch_down(p, nu);
-                    prefetched = true;
-                }
             }
         }
-        if (ok && !prefetched) fold::prefetch_down(p, nu);
         if (ok) {
             const int s = issued % c.stages;
             if (bar_wait(&empty[s], ((issued / c.stages) & 1) ^ 1)) {
@@ -416,7 +405,11 @@ __device__ __forceinline__ void rows_mma_body(const FfnParams &p, const F8Cfg &c
             return;
         }
         const F8Hdr &hs = hdr[s];  // stays valid until this warp releases the stage
-        if (hs.done) return;
+        if (hs.done) {
+            if (PHASE == kDN && p.s.ycnt)  // the weighted combine of the tokens this CTA completes
+                fold::fold_at_exit(p, c.tiles, kFRows, kFTok, &rbar[2], &rbar[3], 0, &s_q, threadIdx.x, kFCW * 32);
+            return;
+        }
         const int ntok = hs.ntok;
         const bool last = hs.last;
         const unsigned char *st = stage0 + (size_t)s * c.stage_bytes;
@@ -464,62 +457,25 @@ __device__ __forceinline__ void rows_mma_body(const FfnParams &p, const F8Cfg &c
         const int n0 = hs.n0, i = threadIdx.x, t = i / kFRows, row = i - t * kFRows;
         const bool has = i < ntok * kFRows;  // whole warps: ntok * kFRows is a multiple of 32
         const int q_t = has ? hs.pairs[t] : 0, e_t = has ? hs.texp[t] : 0;
-        const int kc = hs.kc, item = hs.item, tile = hs.tile;
-        const int nout = PHASE == kGU ? I : H;
-        int pr[kFTok];  // the item's routed pairs (the header is reused once the stage is released)
-#pragma unroll
-        for (int j = 0; j < kFTok; j++) pr[j] = j < ntok ? hs.pairs[j] : 0;
         __syncwarp();
         if (lane == 0) bar_arrive(&empty[s]);
-        float v[NM];
         if (has) {
             const float xs_t = WK == kWE4M3 ? ldexpf(1.f, e_t) : 1.f;
+            float v[NM];
 #pragma unroll
             for (int m = 0; m < NM; m++) {
                 float sum = 0.f;
 #pragma unroll
                 for (int q4 = 0; q4 < NPART; q4++) sum += red[((m * NPART + q4) * kFTok + t) * kRedStride + row];
                 v[m] = sum * xs_t;
-                if (c.ksplit > 1 && n0 + row < nout)  // this chunk's partial sum
-                    p.s.part[fold::part_index(p, kc, q_t, m * nout + n0 + row)] = v[m];
             }
+            rows_mma_store<WK, PHASE, NM>(p, q_t, n0 + row, v, lane);
         }
-        bool finish = true;
-        if (c.ksplit > 1) {
-            // the last chunk of the item to arrive adds every chunk's partials in chunk order
-            __threadfence();
-            if (!fold::consumer_sync(&rbar[2], rphase, p.status)) return;
-            if (threadIdx.x == 0)
-                s_last = fold::chunk_arrive(p.s.kcnt + PHASE * p.kcnt_words + item, c.ksplit);
-            if (!fold::consumer_sync(&rbar[3], rphase, p.status)) return;
-            finish = *reinterpret_cast<volatile int *>(&s_last) != 0;
-            if (finish && has && n0 + row < nout) {
-#pragma unroll
-                for (int m = 0; m < NM; m++) {
-                    float sum = 0.f;
-                    for (int k2 = 0; k2 < c.ksplit; k2++)
-                        sum += __ldcg(p.s.part + fold::part_index(p, k2, q_t, m * nout + n0 + row));
-                    v[m] = sum;
-                }
-            }
-        }
-        if (finish && has) rows_mma_store<WK, PHASE, NM>(p, q_t, n0 + row, v, lane);
-        const bool fold_y = PHASE == kDN && p.s.ycnt && finish;
-        if (fold_y) __threadfence();  // this thread's o row, before the item is counted
         __syncwarp();
         if (lane == 0) bar_arrive(&rbar[1]);
         if (!bar_wait(&rbar[1], rphase)) {
             if (lane == 0) atomicCAS(p.status, 0, FTMOE_ERR_STATE);
             return;
-        }
-        if (fold_y && warp == 0) {
-            // the weighted combine of every token whose last routed pair for this row tile was
-            // this item's
-            uint32_t fin = lane == 0 ? fold::count_pairs(p, pr, ntok, tile) : 0u;
-            fin = __shfl_sync(0xffffffffu, fin, 0);
-            const int n1 = n0 + kFRows < H ? n0 + kFRows : H;
-            for (int j = 0; j < ntok; j++)
-                if (fin >> j & 1) fold::combine_rows(p, pr[j] / p.topk, n0, n1, lane, 32);
         }
         rphase ^= 1;
     }
@@ -545,9 +501,6 @@ bool make_f8_cfg(const FfnParams &p, int wk, int phase, F8Cfg &c, size_t &smem) 
     if (K % kFKs || nout % kFRows) return false;
     c.tiles = nout / kFRows;
     c.kst = K / kFKs;
-    c.ksplit = phase == kGU ? p.ksplit_gu : p.ksplit_dn;
-    if (c.ksplit < 1) c.ksplit = 1;
-    if (c.ksplit > c.kst) c.ksplit = c.kst;
     c.sc_bytes = wk == kWE4M3 ? (K / 128) * 4 : 0;  // one block-scale row (a multiple of 16 bytes)
     c.sc_off = NM * kFStageBytes * kFRows;
     // token rows, padded so that the eight tokens' B loads hit distinct banks: by 32 / 64
@@ -564,7 +517,8 @@ bool make_f8_cfg(const FfnParams &p, int wk, int phase, F8Cfg &c, size_t &smem) 
     const int npart = wk == kWE4M3 && phase == kDN ? 16 : 4;  // partial sums per output
     const size_t red = (size_t)NM * npart * kFTok * kRedStride * 4;
     const size_t head = 256 + kFStagesMax * sizeof(F8Hdr) + 1024;  // + alignment slack
-    const size_t cap = 227 * 1024 - 64;  // dynamic shared memory, leaving room for the static words
+    // dynamic shared memory; the static exit queue takes 3 KB (padded to the 1024-byte alignment)
+    const size_t cap = 227 * 1024 - 4096;
     int stages = kFStagesMax;
     while (stages >= 2 && head + (size_t)stages * c.stage_bytes + red > cap) stages--;
     if (stages < 2) return false;
@@ -620,13 +574,7 @@ bool ffn_bf16_mma_supported(const FfnParams &p, const MxTmaMaps *maps) {
     return make_f8_cfg(p, kWBF16, kGU, c, smem) && make_f8_cfg(p, kWBF16, kDN, c, smem);
 }
 
-void ffn_rows_mma_shape(const FfnParams &p, int phase, int &tiles, int &kst, int &row_tile) {
-    const int K = phase == kGU ? p.H : p.I, nout = phase == kGU ? p.I : p.H;
-    const int ks = p.fmt == FTMOE_FMT_FP8 ? kfks<kWE4M3>() : kfks<kWBF16>();
-    tiles = nout / kFRows;
-    kst = K / ks;
-    row_tile = kFRows;
-}
+int ffn_rows_mma_down_rows() { return kFRows; }
 
 cudaError_t launch_ffn_bf16_mma(const FfnParams &p, const MxTmaMaps &maps, int num_sms, cudaStream_t st) {
     cudaError_t e = launch_f8<kWBF16, kGU>(p, maps, num_sms, st);

@@ -436,8 +436,9 @@ __global__ void __launch_bounds__(kTmaThreads<FMT, PHASE>, 1) ffn_rows_tma_kerne
     extern __shared__ __align__(128) unsigned char sm[];
     uint64_t *full = reinterpret_cast<uint64_t *>(sm);
     uint64_t *empty = full + kMaxStages;
+    uint64_t *xbar = empty + kMaxStages;  // [2] consumer barriers of the folded combine at exit
     StageHdr *hdr = reinterpret_cast<StageHdr *>(sm + 128);
-    __shared__ int s_done_warps[kMaxStages];  // folded combine: consumer warps done with each stage
+    __shared__ fold::ExitQueue s_q;  // down: rows of y this CTA forms at exit
     unsigned char *stage0 = sm + 128 + kMaxStages * sizeof(StageHdr);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -445,8 +446,9 @@ __global__ void __launch_bounds__(kTmaThreads<FMT, PHASE>, 1) ffn_rows_tma_kerne
         for (int s = 0; s < c.stages; s++) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumerWarps<FMT, PHASE>);
-            s_done_warps[s] = 0;
         }
+        mbar_init(&xbar[0], kConsumerWarps<FMT, PHASE>);
+        mbar_init(&xbar[1], kConsumerWarps<FMT, PHASE>);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -462,7 +464,6 @@ __global__ void __launch_bounds__(kTmaThreads<FMT, PHASE>, 1) ffn_rows_tma_kerne
         const int npass = nu > 0 ? *p.s.n_passes : 0;
         const int items = npass * c.tiles;
         const int first = blockIdx.x;
-        bool prefetched = PHASE != kGateUp;
         const uint64_t pol = evict_first_policy();
         const int H = p.H, I = p.I, R = c.R;
         const int nout = PHASE == kGateUp ? I : H;
@@ -549,13 +550,8 @@ __global__ void __launch_bounds__(kTmaThreads<FMT, PHASE>, 1) ffn_rows_tma_kerne
                     bulk_g2s_plain(st + c.tok_off + i * c.tok_bytes, src, (uint32_t)c.tok_bytes, &full[s]);
                 }
                 issued++;
-                if (!prefetched) {  // once this CTA's weight stream has started
-                    fold::prefetch_down(p, nu);
-                    prefetched = true;
-                }
             }
         }
-        if (ok && !prefetched) fold::prefetch_down(p, nu);
         if (ok) {  // end marker
             const int s = issued % c.stages;
             if (mbar_wait(&empty[s], ((issued / c.stages) & 1) ^ 1)) {
@@ -585,6 +581,9 @@ __global__ void __launch_bounds__(kTmaThreads<FMT, PHASE>, 1) ffn_rows_tma_kerne
         const StageHdr h = hdr[s];
         if (h.done) {
             hm.flush(p);
+            if (PHASE == kDown && p.s.ycnt)  // the weighted combine of the tokens this CTA completes
+                fold::fold_at_exit(p, c.tiles, c.R, kPassTokens, &xbar[0], &xbar[1], 0, &s_q, threadIdx.x,
+                                   kConsumerWarps<FMT, PHASE> * 32);
             return;
         }
         const unsigned char *st = stage0 + (size_t)s * c.stage_bytes;
@@ -602,27 +601,6 @@ __global__ void __launch_bounds__(kTmaThreads<FMT, PHASE>, 1) ffn_rows_tma_kerne
                 case 3: dn_consume<FMT, 3>(p, c, st, h); break;
                 default: dn_consume<FMT, 4>(p, c, st, h); break;
             }
-            if (p.s.ycnt) {
-                // folded combine: the last consumer warp done with the stage counts its tokens'
-                // o rows of the tile, and forms y of every token whose count is complete
-                __threadfence();  // this warp's o rows, before the stage is counted
-                __syncwarp();
-                int last = 0;
-                if (lane == 0) {
-                    last = atomicAdd(&s_done_warps[s], 1) == kConsumerWarps<FMT, PHASE> - 1;
-                    if (last) {
-                        s_done_warps[s] = 0;  // ready for the stage's next round
-                        __threadfence();
-                    }
-                }
-                last = __shfl_sync(0xffffffffu, last, 0);
-                if (last) {
-                    uint32_t fin = lane == 0 ? fold::count_pairs(p, h.pairs, h.ntok, h.tile) : 0u;
-                    fin = __shfl_sync(0xffffffffu, fin, 0);
-                    for (int i = 0; i < h.ntok; i++)
-                        if (fin >> i & 1) fold::combine_rows(p, h.pairs[i] / p.topk, h.n0, h.n0 + h.rows, lane, 32);
-                }
-            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
@@ -630,7 +608,7 @@ __global__ void __launch_bounds__(kTmaThreads<FMT, PHASE>, 1) ffn_rows_tma_kerne
 }
 
 constexpr size_t kSmemHeader = 128 + kMaxStages * sizeof(StageHdr);
-constexpr size_t kSmemCap = 220 * 1024;
+constexpr size_t kSmemCap = 220 * 1024;  // dynamic; the exit queue and the static words fit beside it
 
 template <int FMT, int PHASE>
 bool make_cfg(const FfnParams &p, TmaCfg &c) {

@@ -84,18 +84,7 @@ struct FfnScratch {
     // the separate combine kernel runs).
     int32_t *gcnt;
     int32_t *ycnt;
-    // Split reduction axis of the tensor-map pipelines for calls with few work items: the
-    // ksplit items of one (pass, tile) write their partial sums to part [ksplit][kSplitPairs]
-    // [kSplitRow] and the last of them to arrive (kcnt [2][kSplitPairs * tiles] counters,
-    // gate_up then down) sums them in chunk order and finishes the item (nullptr: no split).
-    float *part;
-    int32_t *kcnt;
 };
-
-// Largest call (routed pairs) whose tensor-map items may be split along the reduction axis,
-// and the most chunks one item is split into.
-constexpr int kSplitPairs = 64;
-constexpr int kSplitMax = 4;
 
 // Pipelined FFN kernels split each slot's routed pairs into passes of at most
 // FfnParams::pass_tokens tokens; every (pass, tile) is a separate work item so hot experts
@@ -121,13 +110,7 @@ struct FfnParams {
     int32_t x16_swz;   // f16 activation copy layout: 0 plain, 1 swz_x16 (nvfp4), 2 swz_q4x16 (Q4_0)
     int32_t pass_tokens;  // tokens per pass of the pipelined kernels (kPassTokens / kMxPassTokens)
     int32_t ytiles;       // row tiles of the down kernel per token (folded combine; 0: combine kernel)
-    int32_t ysplit_words; // words of s.ycnt the routing kernel clears (bs * ytiles)
-    int32_t kcnt_words;   // words of s.kcnt per phase the routing kernel clears (0: no split)
-    int32_t split_row;    // floats per pair and chunk in s.part (>= 2I and >= H)
-    int32_t ksplit_gu, ksplit_dn;  // chunks of the reduction axis per item (1: no split)
-    int32_t dn_b0, dn_nb;          // slot banks holding the down weights (bank[dn_b0 .. +dn_nb))
-    int64_t l2_prefetch;           // down weights of a call prefetched into L2 by gate_up when the
-                                   // call's distinct experts hold at most this many down bytes (0: off)
+    int32_t ycnt_words;   // words of s.ycnt the routing kernel clears (bs * ytiles)
 };
 
 // Tensor maps (CUtensorMap, 128 bytes each) of the tensor-map pipelines: the transposed
@@ -157,10 +140,9 @@ cudaError_t launch_ffn_mx_tma(const FfnParams &p, const MxTmaMaps &maps, int num
 bool make_fp8_tma_maps(MxTmaMaps &m, const unsigned char *const *banks, int S, int H, int I);
 bool ffn_fp8_tma_supported(const FfnParams &p, const MxTmaMaps *maps);
 cudaError_t launch_ffn_fp8_tma(const FfnParams &p, const MxTmaMaps &maps, int num_sms, cudaStream_t st);
-// Work-item shape of the tensor-map pipelines for phase 0 (gate_up) or 1 (down): items per
-// pass (tiles), stages along the reduction axis (kst) and output rows per item (row_tile).
-void ffn_mx_tma_shape(const FfnParams &p, int phase, int &tiles, int &kst, int &row_tile);
-void ffn_rows_mma_shape(const FfnParams &p, int phase, int &tiles, int &kst, int &row_tile);
+// Output rows (columns) per down item of the tensor-map pipelines: their folded-combine tile.
+int ffn_mx_tma_down_rows();
+int ffn_rows_mma_down_rows();
 // Tensor-core pipeline for bf16 (weight maps in gu_blocks / dn_blocks; H, I multiples of 256).
 bool make_bf16_tma_maps(MxTmaMaps &m, const unsigned char *const *banks, int S, int H, int I);
 bool ffn_bf16_mma_supported(const FfnParams &p, const MxTmaMaps *maps);
