@@ -574,9 +574,8 @@ def ffn_family(F, cache, cfg, bs):
 
 
 def ffn_launches(cfg, kind):
-    """Kernels one FFN call launches: routing, gate_up and down (which forms y: the weighted
-    combine is folded into it in every pipelined kernel family)."""
-    return 3
+    """Kernels one FFN call launches: routing, gate_up, down and the weighted combine."""
+    return 4
 
 
 def sweep_workload(args, cfg, stream, torch, F, wl, synthetic_cache, link, hbm_peak):

@@ -36,7 +36,6 @@ size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 struct Layout {
     size_t hdr, id2slot, owner, stamp, miss_ids, miss_slots, all_ids, pf_slots;
     size_t n_unique, uslot, ucnt, uoff, upairs, h, o, x16, xexp, hmax, upoff, pipe_slots;
-    size_t gcnt, ycnt;
     size_t total;
     bool ffn;
 };
@@ -117,10 +116,6 @@ Layout make_layout(int fmt, int E, int L, int S, int H, int I, int max_pairs) {
         l.hmax = off; off += align256(P * 4);
         l.upoff = off; off += align256(P * 4);
         l.pipe_slots = off; off += 2 * align256(P * 4);  // two routed-slot buffers of the prefill pipeline
-        // folded combine: pairs with a slot per token, arrival counts per (token, row tile of
-        // at least 8 rows)
-        l.gcnt = off; off += align256(P * 4);
-        l.ycnt = off; off += align256(P * (size_t)((H + 7) / 8) * 4);
     }
     l.total = off;
     return l;
@@ -289,8 +284,6 @@ int ftmoe_cache_create(const ftmoe_bank_spec *banks, int32_t num_banks, int32_t 
         c->s.hmax = reinterpret_cast<uint32_t *>(ws + lay.hmax);
         c->s.upoff = reinterpret_cast<int32_t *>(ws + lay.upoff);
         c->s.n_passes = c->s.n_unique + 1;  // second word of the 256-byte n_unique block
-        c->s.gcnt = reinterpret_cast<int32_t *>(ws + lay.gcnt);
-        c->s.ycnt = reinterpret_cast<int32_t *>(ws + lay.ycnt);
     }
     if (format == FTMOE_FMT_MXFP4 && lay.ffn) {
         const unsigned char *sb[6];

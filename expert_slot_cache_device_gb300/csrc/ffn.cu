@@ -42,7 +42,6 @@ constexpr int kColsDnTgMax = 4;  // tokens per pass, transposed down kernel
 constexpr int kGuNeurons = 16; // gate_up rows kernel: neurons per CTA (2 per warp)
 constexpr int kDnRows = 32;    // down rows kernel: output rows per CTA
 constexpr int kColTile = 128;  // transposed kernels: columns per CTA (4 per lane)
-constexpr int kYTileMin = 8;   // smallest down row tile with a folded combine (ycnt holds H / 8 per token)
 
 // ------------------------------------------------------------------------ route
 
@@ -122,9 +121,6 @@ __global__ void __launch_bounds__(1024) ffn_route_kernel(FfnParams p) {
     for (int s = tid; s < p.S; s += nt) cnt[s] = 0;
     if (p.s.hmax)
         for (int q = tid; q < p.P; q += nt) p.s.hmax[q] = 0u;
-    // arrival counters of the folded combine start every call at zero
-    if (p.s.ycnt)
-        for (int i = tid; i < p.ycnt_words; i += nt) p.s.ycnt[i] = 0;
     __syncthreads();
     for (int q = tid; q < p.P; q += nt) {
         int s = p.slots[q];
@@ -169,28 +165,6 @@ __global__ void __launch_bounds__(1024) ffn_route_kernel(FfnParams p) {
         if (s < 0) continue;
         int pos = atomicAdd(&cnt[s], 1);
         p.s.upairs[pos] = q;
-    }
-    if (p.s.gcnt) {
-        // folded combine: routed pairs with a slot per token; a token with none gets its y
-        // here (the addend, or zero), since no down item will form it
-        for (int t = tid; t < p.bs; t += nt) {
-            int g = 0;
-            for (int j = 0; j < p.topk; j++) g += p.slots[t * p.topk + j] >= 0;
-            p.s.gcnt[t] = g;
-        }
-        __syncthreads();  // gcnt written above is read back by other threads of this CTA
-        for (int i = tid; i < p.bs * (p.H >> 1); i += nt) {
-            const int t = i / (p.H >> 1), n = 2 * (i - t * (p.H >> 1));
-            if (p.s.gcnt[t]) continue;
-            float a0 = 0.f, a1 = 0.f;
-            if (p.addend) {
-                a0 = p.addend[(int64_t)t * p.H + n];
-                a1 = p.addend[(int64_t)t * p.H + n + 1];
-            }
-            const uint32_t v = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a0)) |
-                               ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a1)) << 16);
-            reinterpret_cast<uint32_t *>(p.y + (int64_t)t * p.H)[n >> 1] = v;
-        }
     }
     if (tid == 0) *p.s.n_unique = base_u;
 }
@@ -792,17 +766,6 @@ cudaError_t launch_ffn(const FfnParams &p_in, int num_sms, cudaStream_t st, cons
     p.x16_emax = p.fmt == FTMOE_FMT_MXFP4 ? 9 : (p.fmt == FTMOE_FMT_Q4_0 ? 8 : 10);
     p.x16_swz = fp4_rows_tma && p.fmt == FTMOE_FMT_NVFP4 ? 1 : (fp4_rows_tma && p.fmt == FTMOE_FMT_Q4_0 ? 2 : 0);
     p.pass_tokens = (mx_tma || fp8_tma || bf16_mma) ? kMxPassTokens : kPassTokens;
-    const bool pipeline = bf16_mma || fp4_rows_tma || mx_tma || fp8_tma;
-    // Folded combine: the down kernel's item rows are the tile of its arrival counts (the CTA
-    // completing a token's tile forms y there at exit); other kernels use the combine kernel
-    const int ytile = (bf16_mma || fp8_tma) ? ffn_rows_mma_down_rows()
-                      : mx_tma              ? ffn_mx_tma_down_rows()
-                      : fp4_rows_tma        ? ffn_rows_tma_down_rows(p)
-                                            : 0;
-    const bool fold = pipeline && p.s.gcnt && p.s.ycnt && ytile >= kYTileMin;
-    p.ytiles = fold ? (p.H + ytile - 1) / ytile : 0;
-    p.ycnt_words = fold ? p.bs * p.ytiles : 0;
-    if (!fold) p.s.gcnt = p.s.ycnt = nullptr;
     {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(1 + (want_x16 ? p.bs : 0));
@@ -865,7 +828,6 @@ cudaError_t launch_ffn(const FfnParams &p_in, int num_sms, cudaStream_t st, cons
                        tiles_dn, tg_dn);
         if (e != cudaSuccess) return e;
     }
-    if (fold) return cudaSuccess;  // y is formed by the down kernel
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((p.H / 4 + kThreads - 1) / kThreads, p.bs);
     cfg.blockDim = dim3(kThreads);

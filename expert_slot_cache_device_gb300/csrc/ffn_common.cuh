@@ -313,7 +313,8 @@ __host__ __device__ __forceinline__ int swz_q4h32(int n) { return n ^ ((n >> 4) 
 // the two blocks of residue L of each 64-block window, the even one first when L is even and
 // the odd one first otherwise: the 32 lanes of every word load then hit 32 distinct banks,
 // and with the swizzles above each quarter-warp's 16-byte activation or h loads hit 8 distinct
-// 16-byte bank groups. step 0 or 1; returns the block within the window.
+// 16-byte bank groups. step 0 or 1; returns the block within the window. (A row whose block
+// count is not a multiple of 64 reads its last, shorter window consecutively.)
 __device__ __forceinline__ int q4_lane_block(int lane, int step) {
     const int be = 2 * ((25 * lane) & 31), bo = 2 * ((25 * (lane - 4)) & 31) + 1;  // 25 = 9^-1 mod 32
     return ((lane & 1) ^ step) ? bo : be;

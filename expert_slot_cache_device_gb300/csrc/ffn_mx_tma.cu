@@ -33,7 +33,6 @@
 #include <cuda.h>
 
 #include "ffn_common.cuh"
-#include "ffn_fold.cuh"
 #include "internal.cuh"
 #include "pipeline.cuh"
 
@@ -151,7 +150,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     extern __shared__ __align__(1024) unsigned char sm[];
     uint64_t *full = reinterpret_cast<uint64_t *>(sm);
     uint64_t *empty = full + kMxStagesMax;
-    uint64_t *rbar = empty + kMxStagesMax;  // [5] consumer barriers: reduction [0..2], exit [3..4]
+    uint64_t *rbar = empty + kMxStagesMax;  // [3] consumer barriers around the reduction
     MxHdr *hdr = reinterpret_cast<MxHdr *>(sm + 256);
     // stages start at the first 1024-byte aligned shared address after the headers (the
     // 128-byte swizzle pattern of the code tiles repeats every 1024 bytes)
@@ -168,10 +167,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             bar_init(&full[s], 1);
             bar_init(&empty[s], kCW);
         }
-        for (int b = 0; b < 5; b++) bar_init(&rbar[b], kCW);
+        bar_init(&rbar[0], kCW);
+        bar_init(&rbar[1], kCW);
+        bar_init(&rbar[2], kCW);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    __shared__ fold::ExitQueue s_q;  // down: rows of y this CTA forms at exit
     __syncthreads();
     if (PHASE == kGU) asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" :::);
@@ -310,11 +310,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             return;
         }
         const MxHdr &hs = hdr[s];  // stays valid until this warp releases the stage
-        if (hs.done) {
-            if (PHASE == kDN && p.s.ycnt)  // the weighted combine of the tokens this CTA completes
-                fold::fold_at_exit(p, c.tiles, kCols, kMxTokMax, &rbar[3], &rbar[4], 0, &s_q, threadIdx.x, kCW * 32);
-            return;
-        }
+        if (hs.done) return;
         const int ntok = hs.ntok, rows = hs.rows;
         const bool last = hs.last;
         const unsigned char *st = stage0 + (size_t)s * c.stage_bytes;
@@ -428,8 +424,7 @@ bool make_mx_cfg(const FfnParams &p, int phase, MxCfg &c, size_t &smem) {
     static_assert(kBlkPairs * kMxTokMax * kCols * 4 == kKp * kCols, "down partials fill one code tile");
     const size_t red = phase == kDN ? 0 : (size_t)NM * kBlkPairs * kMxTokMax * kCols * 4;
     const size_t head = 256 + kMxStagesMax * sizeof(MxHdr) + 1024;  // + alignment slack
-    // dynamic shared memory; the static exit queue takes 3 KB (padded to the 1024-byte alignment)
-    const size_t cap = 227 * 1024 - 4096;
+    const size_t cap = 227 * 1024;
     int stages = kMxStagesMax;
     while (stages >= 2 && head + (size_t)stages * c.stage_bytes + red > cap) stages--;
     if (stages < 2) return false;
@@ -469,8 +464,6 @@ bool ffn_mx_tma_supported(const FfnParams &p, const MxTmaMaps *maps) {
            p.s.n_passes &&
            p.H % 32 == 0 && p.I % 32 == 0;
 }
-
-int ffn_mx_tma_down_rows() { return kCols; }
 
 cudaError_t launch_ffn_mx_tma(const FfnParams &p, const MxTmaMaps &maps, int num_sms, cudaStream_t st) {
     cudaError_t e = launch_mx<kGU>(p, maps, num_sms, st);

@@ -46,7 +46,6 @@
 #include <cuda.h>
 
 #include "ffn_common.cuh"
-#include "ffn_fold.cuh"
 #include "internal.cuh"
 #include "pipeline.cuh"
 
@@ -249,7 +248,7 @@ __device__ __forceinline__ void rows_mma_body(const FfnParams &p, const F8Cfg &c
     extern __shared__ __align__(1024) unsigned char sm[];
     uint64_t *full = reinterpret_cast<uint64_t *>(sm);
     uint64_t *empty = full + kFStagesMax;
-    uint64_t *rbar = empty + kFStagesMax;  // [4] consumer barriers: reduction [0..1], exit [2..3]
+    uint64_t *rbar = empty + kFStagesMax;  // [2] consumer barriers around the reduction
     F8Hdr *hdr = reinterpret_cast<F8Hdr *>(sm + 256);
     const uint32_t hdr_end = su32(sm) + 256 + kFStagesMax * sizeof(F8Hdr);
     unsigned char *stage0 = sm + (((hdr_end + 1023u) & ~1023u) - su32(sm));
@@ -264,10 +263,10 @@ __device__ __forceinline__ void rows_mma_body(const FfnParams &p, const F8Cfg &c
             bar_init(&full[s], 1);
             bar_init(&empty[s], kFCW);
         }
-        for (int b = 0; b < 4; b++) bar_init(&rbar[b], kFCW);
+        bar_init(&rbar[0], kFCW);
+        bar_init(&rbar[1], kFCW);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    __shared__ fold::ExitQueue s_q;  // down: rows of y this CTA forms at exit
     __syncthreads();
     if (PHASE == kGU) asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" :::);
@@ -405,11 +404,7 @@ __device__ __forceinline__ void rows_mma_body(const FfnParams &p, const F8Cfg &c
             return;
         }
         const F8Hdr &hs = hdr[s];  // stays valid until this warp releases the stage
-        if (hs.done) {
-            if (PHASE == kDN && p.s.ycnt)  // the weighted combine of the tokens this CTA completes
-                fold::fold_at_exit(p, c.tiles, kFRows, kFTok, &rbar[2], &rbar[3], 0, &s_q, threadIdx.x, kFCW * 32);
-            return;
-        }
+        if (hs.done) return;
         const int ntok = hs.ntok;
         const bool last = hs.last;
         const unsigned char *st = stage0 + (size_t)s * c.stage_bytes;
@@ -517,8 +512,7 @@ bool make_f8_cfg(const FfnParams &p, int wk, int phase, F8Cfg &c, size_t &smem) 
     const int npart = wk == kWE4M3 && phase == kDN ? 16 : 4;  // partial sums per output
     const size_t red = (size_t)NM * npart * kFTok * kRedStride * 4;
     const size_t head = 256 + kFStagesMax * sizeof(F8Hdr) + 1024;  // + alignment slack
-    // dynamic shared memory; the static exit queue takes 3 KB (padded to the 1024-byte alignment)
-    const size_t cap = 227 * 1024 - 4096;
+    const size_t cap = 227 * 1024;
     int stages = kFStagesMax;
     while (stages >= 2 && head + (size_t)stages * c.stage_bytes + red > cap) stages--;
     if (stages < 2) return false;
@@ -573,8 +567,6 @@ bool ffn_bf16_mma_supported(const FfnParams &p, const MxTmaMaps *maps) {
     size_t smem;
     return make_f8_cfg(p, kWBF16, kGU, c, smem) && make_f8_cfg(p, kWBF16, kDN, c, smem);
 }
-
-int ffn_rows_mma_down_rows() { return kFRows; }
 
 cudaError_t launch_ffn_bf16_mma(const FfnParams &p, const MxTmaMaps &maps, int num_sms, cudaStream_t st) {
     cudaError_t e = launch_f8<kWBF16, kGU>(p, maps, num_sms, st);

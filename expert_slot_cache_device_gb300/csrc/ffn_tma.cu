@@ -25,7 +25,6 @@
 // FTMOE_ERR_STATE in the status word and leaves, and the producer waits (again
 // bounded) for its own copies in flight before it exits.
 #include "ffn_common.cuh"
-#include "ffn_fold.cuh"
 #include "internal.cuh"
 
 namespace ftmoe {
@@ -51,7 +50,7 @@ constexpr int kMaxTok = 4;  // tokens per stage
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any healthy wait
 
 struct StageHdr {
-    int32_t slot, n0, rows, ntok, done, tile, pad1, pad2;
+    int32_t slot, n0, rows, ntok, done, pad0, pad1, pad2;
     int32_t pairs[kMaxTok];
     int32_t texp[kMaxTok];  // per-token exponent of the f16 activations (nvfp4 gate_up)
 };
@@ -225,10 +224,11 @@ __device__ __forceinline__ void gu_consume(const FfnParams &p, const TmaCfg &c, 
             // in fp32. Activations are staged in the swz_q4x16 layout: unit u of block b sits
             // at u ^ ((b >> 2) & 3).
             const unsigned char *rg = st + j * wr, *ru = st + (R + j) * wr;
-            const int nb = H >> 5;
-            for (int bi = 0; bi < ((nb + 63) & ~63); bi += 32) {
-                const int b = (bi & ~63) + q4_lane_block(lane, (bi >> 5) & 1);
-                if (b >= nb) continue;
+            const int nb = H >> 5, nwin = nb & ~63;
+            for (int bi = lane; bi < nb; bi += 32) {
+                // whole 64-block windows in the conflict-free order; a shorter tail window
+                // consecutively (every lane busy)
+                const int b = bi < nwin ? (bi & ~63) + q4_lane_block(lane, (bi >> 5) & 1) : bi;
                 const int rot = (b >> 2) & 3;
                 uint32_t dg, du, qg[4], qu[4], fa[16], fb[16];
                 q4_block(rg, b, dg, qg);
@@ -349,9 +349,11 @@ __device__ __forceinline__ void dn_consume(const FfnParams &p, const TmaCfg &c, 
             float hsc[NT];
 #pragma unroll
             for (int t = 0; t < NT; t++) hsc[t] = ldexpf(1.f, -h.texp[t]);
-            for (int bi = 0; bi < ((nb + 63) & ~63); bi += 32) {
-                const int b = (bi & ~63) + q4_lane_block(lane, (bi >> 5) & 1);
-                if (b >= nb) continue;
+            const int nwin = nb & ~63;
+            for (int bi = lane; bi < nb; bi += 32) {
+                // whole 64-block windows in the conflict-free order; a shorter tail window
+                // consecutively (every lane busy)
+                const int b = bi < nwin ? (bi & ~63) + q4_lane_block(lane, (bi >> 5) & 1) : bi;
                 const int rot = (b >> 1) & 7;
                 uint32_t fw[RR][16], dr[RR];
 #pragma unroll
@@ -436,9 +438,7 @@ __global__ void __launch_bounds__(kTmaThreads<FMT, PHASE>, 1) ffn_rows_tma_kerne
     extern __shared__ __align__(128) unsigned char sm[];
     uint64_t *full = reinterpret_cast<uint64_t *>(sm);
     uint64_t *empty = full + kMaxStages;
-    uint64_t *xbar = empty + kMaxStages;  // [2] consumer barriers of the folded combine at exit
     StageHdr *hdr = reinterpret_cast<StageHdr *>(sm + 128);
-    __shared__ fold::ExitQueue s_q;  // down: rows of y this CTA forms at exit
     unsigned char *stage0 = sm + 128 + kMaxStages * sizeof(StageHdr);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -447,8 +447,6 @@ __global__ void __launch_bounds__(kTmaThreads<FMT, PHASE>, 1) ffn_rows_tma_kerne
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumerWarps<FMT, PHASE>);
         }
-        mbar_init(&xbar[0], kConsumerWarps<FMT, PHASE>);
-        mbar_init(&xbar[1], kConsumerWarps<FMT, PHASE>);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -489,7 +487,7 @@ __global__ void __launch_bounds__(kTmaThreads<FMT, PHASE>, 1) ffn_rows_tma_kerne
                     break;
                 }
                 StageHdr &hh = hdr[s];
-                hh.slot = slot; hh.n0 = n0; hh.rows = rows; hh.ntok = ntok; hh.done = 0; hh.tile = tile;
+                hh.slot = slot; hh.n0 = n0; hh.rows = rows; hh.ntok = ntok; hh.done = 0;
                 for (int i = 0; i < ntok; i++) {
                     hh.pairs[i] = p.s.upairs[off + g0 + i];
                     hh.texp[i] = (PHASE == kGateUp && kF16Act<FMT>) ? p.s.xexp[hh.pairs[i] / p.topk] : 0;
@@ -581,9 +579,6 @@ __global__ void __launch_bounds__(kTmaThreads<FMT, PHASE>, 1) ffn_rows_tma_kerne
         const StageHdr h = hdr[s];
         if (h.done) {
             hm.flush(p);
-            if (PHASE == kDown && p.s.ycnt)  // the weighted combine of the tokens this CTA completes
-                fold::fold_at_exit(p, c.tiles, c.R, kPassTokens, &xbar[0], &xbar[1], 0, &s_q, threadIdx.x,
-                                   kConsumerWarps<FMT, PHASE> * 32);
             return;
         }
         const unsigned char *st = stage0 + (size_t)s * c.stage_bytes;
@@ -608,7 +603,7 @@ __global__ void __launch_bounds__(kTmaThreads<FMT, PHASE>, 1) ffn_rows_tma_kerne
 }
 
 constexpr size_t kSmemHeader = 128 + kMaxStages * sizeof(StageHdr);
-constexpr size_t kSmemCap = 220 * 1024;  // dynamic; the exit queue and the static words fit beside it
+constexpr size_t kSmemCap = 220 * 1024;
 
 template <int FMT, int PHASE>
 bool make_cfg(const FfnParams &p, TmaCfg &c) {

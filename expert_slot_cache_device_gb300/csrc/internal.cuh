@@ -78,12 +78,6 @@ struct FfnScratch {
     uint32_t *hmax;     // [P] bit pattern of max |h| per pair (order-independent atomicMax)
     int32_t *upoff;     // [P] first pass (group of pass_tokens pairs) of each distinct slot
     int32_t *n_passes;  // [1] passes over all distinct slots
-    // Weighted combine folded into the down kernels (the last down item to finish a
-    // (token, row tile) forms that part of y): gcnt [bs] = routed pairs with a slot per token,
-    // ycnt [bs, ytiles] = pairs of the token whose o rows of the tile are final (nullptr:
-    // the separate combine kernel runs).
-    int32_t *gcnt;
-    int32_t *ycnt;
 };
 
 // Pipelined FFN kernels split each slot's routed pairs into passes of at most
@@ -109,8 +103,6 @@ struct FfnParams {
     int32_t x16_emax;  // f16 activation copy keeps max |x| < 2^x16_emax
     int32_t x16_swz;   // f16 activation copy layout: 0 plain, 1 swz_x16 (nvfp4), 2 swz_q4x16 (Q4_0)
     int32_t pass_tokens;  // tokens per pass of the pipelined kernels (kPassTokens / kMxPassTokens)
-    int32_t ytiles;       // row tiles of the down kernel per token (folded combine; 0: combine kernel)
-    int32_t ycnt_words;   // words of s.ycnt the routing kernel clears (bs * ytiles)
 };
 
 // Tensor maps (CUtensorMap, 128 bytes each) of the tensor-map pipelines: the transposed
@@ -131,8 +123,6 @@ cudaError_t launch_ffn(const FfnParams &p, int num_sms, cudaStream_t st, const M
 // Persistent bulk-copy pipeline for the row-major formats (bf16; nvfp4 with H, I multiples of 256).
 bool ffn_rows_tma_supported(const FfnParams &p);
 cudaError_t launch_ffn_rows_tma(const FfnParams &p, int num_sms, cudaStream_t st);
-// Output rows per down item of that pipeline (its folded-combine row tile), 0 if unsupported.
-int ffn_rows_tma_down_rows(const FfnParams &p);
 // 2-D tensor-map pipeline for the transposed mxfp4 format.
 bool ffn_mx_tma_supported(const FfnParams &p, const MxTmaMaps *maps);
 cudaError_t launch_ffn_mx_tma(const FfnParams &p, const MxTmaMaps &maps, int num_sms, cudaStream_t st);
@@ -140,9 +130,6 @@ cudaError_t launch_ffn_mx_tma(const FfnParams &p, const MxTmaMaps &maps, int num
 bool make_fp8_tma_maps(MxTmaMaps &m, const unsigned char *const *banks, int S, int H, int I);
 bool ffn_fp8_tma_supported(const FfnParams &p, const MxTmaMaps *maps);
 cudaError_t launch_ffn_fp8_tma(const FfnParams &p, const MxTmaMaps &maps, int num_sms, cudaStream_t st);
-// Output rows (columns) per down item of the tensor-map pipelines: their folded-combine tile.
-int ffn_mx_tma_down_rows();
-int ffn_rows_mma_down_rows();
 // Tensor-core pipeline for bf16 (weight maps in gu_blocks / dn_blocks; H, I multiples of 256).
 bool make_bf16_tma_maps(MxTmaMaps &m, const unsigned char *const *banks, int S, int H, int I);
 bool ffn_bf16_mma_supported(const FfnParams &p, const MxTmaMaps *maps);

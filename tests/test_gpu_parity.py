@@ -277,7 +277,7 @@ def test_ffn_small_geometries(fmt, geo):
 FOLD = [
     ("bf16", F.FFN_ROWS, dict(E=6, H=1024, I=256, L=2, S=6), 3),
     ("bf16", F.FFN_MMA, dict(E=6, H=1024, I=256, L=2, S=6), 3),
-    ("bf16", F.FFN_MMA, dict(E=20, H=512, I=768, L=2, S=20), 30),   # 120 pairs: no split
+    ("bf16", F.FFN_MMA, dict(E=20, H=512, I=768, L=2, S=20), 30),   # 90 pairs, several passes
     ("nvfp4", F.FFN_AUTO, dict(E=5, H=2048, I=512, L=2, S=5), 4),
     ("q4_0", F.FFN_AUTO, dict(E=6, H=512, I=256, L=2, S=6), 4),
     ("mxfp4", F.FFN_AUTO, dict(E=5, H=576, I=320, L=2, S=5), 4),
@@ -287,12 +287,11 @@ FOLD = [
 
 
 @pytest.mark.parametrize("fmt,kind,geo,bs", FOLD)
-def test_ffn_folded_combine_and_split(fmt, kind, geo, bs):
-    """The weighted combine formed inside the down kernels and the split reduction axis of
-    small calls: a token with every position computed elsewhere (y = its addend), a token
-    routed twice to one expert, the other positions on the GPU, against the oracle plus the
-    addend; two calls in a row give identical bits (the arrival counters start from zero
-    every call)."""
+def test_ffn_combine_edge_cases(fmt, kind, geo, bs):
+    """The weighted combine in every pipelined kernel family at small and larger calls: a
+    token with every position computed elsewhere (y = its addend, rounded once), a token
+    routed three times to one expert, the other positions on the GPU, against the oracle plus
+    the addend; two calls in a row give identical bits."""
     base = {"bf16": "c2", "nvfp4": "c3", "mxfp4": "c4", "fp8": "c6", "q4_0": "c7"}[fmt]
     cfg = wl.scaled(wl.CONFIGS[base], topk=3, **geo)
     cache = synthetic_cache(cfg, bs * cfg.topk)
