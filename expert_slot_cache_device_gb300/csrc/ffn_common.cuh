@@ -301,24 +301,10 @@ __device__ __forceinline__ void q4_decode(const uint32_t (&qs)[4], uint32_t (&w)
 //   fp32 h rows (64-byte blocks, four 16-byte quarters): quarter q of block b is stored
 //   at quarter q ^ ((b >> 1) & 3).
 __host__ __device__ __forceinline__ int swz_x16(int k) { return k ^ ((k >> 3) & 8); }
-// Q4_0 (32-element blocks, read in the q4_lane_block order below): f16 activations,
-// 16-byte unit u of block b stored at u ^ ((b >> 2) & 3); fp32 h rows, unit u of block b
-// stored at u ^ ((b >> 1) & 7).
-__host__ __device__ __forceinline__ int swz_q4x16(int k) { return k ^ ((k >> 4) & 0x18); }
-__host__ __device__ __forceinline__ int swz_q4h32(int n) { return n ^ ((n >> 4) & 0x1C); }
-
-// Q4_0 blocks are 18 bytes, so block b starts at 32-bit word floor(4.5 b), and over any 64
-// consecutive blocks every bank residue occurs exactly twice: once at an even block (b = 2c
-// with 9c = r mod 32) and once at an odd one (b = 2c + 1 with 9c + 4 = r mod 32). Lane L takes
-// the two blocks of residue L of each 64-block window, the even one first when L is even and
-// the odd one first otherwise: the 32 lanes of every word load then hit 32 distinct banks,
-// and with the swizzles above each quarter-warp's 16-byte activation or h loads hit 8 distinct
-// 16-byte bank groups. step 0 or 1; returns the block within the window. (A row whose block
-// count is not a multiple of 64 reads its last, shorter window consecutively.)
-__device__ __forceinline__ int q4_lane_block(int lane, int step) {
-    const int be = 2 * ((25 * lane) & 31), bo = 2 * ((25 * (lane - 4)) & 31) + 1;  // 25 = 9^-1 mod 32
-    return ((lane & 1) ^ step) ? bo : be;
-}
+// Q4_0 (32-element blocks): f16 activations, 16-byte unit u of block b stored at
+// u ^ ((b >> 1) & 3); fp32 h rows, unit u of block b stored at u ^ (b & 7).
+__host__ __device__ __forceinline__ int swz_q4x16(int k) { return k ^ ((k >> 3) & 0x18); }
+__host__ __device__ __forceinline__ int swz_q4h32(int n) { return n ^ ((n >> 3) & 0x1C); }
 
 __host__ __device__ __forceinline__ int swz_h32(int n) { return n ^ ((n >> 3) & 12); }
 

@@ -218,18 +218,14 @@ __device__ __forceinline__ void gu_consume(const FfnParams &p, const TmaCfg &c, 
                 }
             }
         } else if (FMT == FTMOE_FMT_Q4_0) {
-            // lane step = one 32-element Q4_0 block of the gate and of the up row (blocks in
-            // the q4_lane_block order): nibbles -> exact f16x2 (nibble - 8), 32 exact f16
-            // products summed in two f16 halves of sixteen, the block's binary16 scale applied
-            // in fp32. Activations are staged in the swz_q4x16 layout: unit u of block b sits
-            // at u ^ ((b >> 2) & 3).
+            // lane step = one 32-element Q4_0 block of the gate and of the up row: nibbles ->
+            // exact f16x2 (nibble - 8), 32 exact f16 products summed in two f16 halves of
+            // sixteen, the block's binary16 scale applied in fp32. Activations are staged in
+            // the swz_q4x16 layout: unit u of this lane's block sits at u ^ ((b >> 1) & 3).
             const unsigned char *rg = st + j * wr, *ru = st + (R + j) * wr;
-            const int nb = H >> 5, nwin = nb & ~63;
-            for (int bi = lane; bi < nb; bi += 32) {
-                // whole 64-block windows in the conflict-free order; a shorter tail window
-                // consecutively (every lane busy)
-                const int b = bi < nwin ? (bi & ~63) + q4_lane_block(lane, (bi >> 5) & 1) : bi;
-                const int rot = (b >> 2) & 3;
+            const int nb = H >> 5;
+            const int rot = (lane >> 1) & 3;
+            for (int b = lane; b < nb; b += 32) {
                 uint32_t dg, du, qg[4], qu[4], fa[16], fb[16];
                 q4_block(rg, b, dg, qg);
                 q4_block(ru, b, du, qu);
@@ -340,21 +336,16 @@ __device__ __forceinline__ void dn_consume(const FfnParams &p, const TmaCfg &c, 
                 }
             }
         } else if (FMT == FTMOE_FMT_Q4_0) {
-            // lane step = one 32-element Q4_0 block of RR rows (blocks in the q4_lane_block
-            // order); h is converted once per block and token to f16 with the token's
-            // power-of-two scale (max |h| < 2^8), shared by the RR rows. The h rows are staged
-            // in the swz_q4h32 layout: unit u of block b sits at u ^ ((b >> 1) & 7), so the 8
-            // lanes of a phase hit 8 units.
+            // lane step = one 32-element Q4_0 block of RR rows; h is converted once per
+            // block and token to f16 with the token's power-of-two scale (max |h| < 2^8),
+            // shared by the RR rows. The h rows are staged in the swz_q4h32 layout: unit u of
+            // this lane's block sits at u ^ (b & 7), so the 8 lanes of a phase hit 8 units.
             const int nb = I >> 5;
+            const int rot = lane & 7;
             float hsc[NT];
 #pragma unroll
             for (int t = 0; t < NT; t++) hsc[t] = ldexpf(1.f, -h.texp[t]);
-            const int nwin = nb & ~63;
-            for (int bi = lane; bi < nb; bi += 32) {
-                // whole 64-block windows in the conflict-free order; a shorter tail window
-                // consecutively (every lane busy)
-                const int b = bi < nwin ? (bi & ~63) + q4_lane_block(lane, (bi >> 5) & 1) : bi;
-                const int rot = (b >> 1) & 7;
+            for (int b = lane; b < nb; b += 32) {
                 uint32_t fw[RR][16], dr[RR];
 #pragma unroll
                 for (int r = 0; r < RR; r++) {
@@ -673,15 +664,6 @@ bool ffn_rows_tma_supported(const FfnParams &p) {
         return p.H % 256 == 0 && p.I % 256 == 0 && p.s.x16 && p.s.xexp && p.s.hmax &&
                make_cfg<FTMOE_FMT_Q4_0, kGateUp>(p, c) && make_cfg<FTMOE_FMT_Q4_0, kDown>(p, c);
     return false;
-}
-
-int ffn_rows_tma_down_rows(const FfnParams &p) {
-    TmaCfg c;
-    bool ok = false;
-    if (p.fmt == FTMOE_FMT_BF16) ok = make_cfg<FTMOE_FMT_BF16, kDown>(p, c);
-    else if (p.fmt == FTMOE_FMT_NVFP4) ok = make_cfg<FTMOE_FMT_NVFP4, kDown>(p, c);
-    else if (p.fmt == FTMOE_FMT_Q4_0) ok = make_cfg<FTMOE_FMT_Q4_0, kDown>(p, c);
-    return ok ? c.R : 0;
 }
 
 cudaError_t launch_ffn_rows_tma(const FfnParams &p, int num_sms, cudaStream_t st) {
