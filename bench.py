@@ -60,7 +60,7 @@ def parse():
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill-pipeline measurements")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay measurement")
     ap.add_argument("--copy-mode", default="fused", choices=["fused", "per_bank", "engine"])
-    ap.add_argument("--ffn-kernels", default="auto", choices=["auto", "rows", "mma"],
+    ap.add_argument("--ffn-kernels", default="auto", choices=["auto", "rows", "mma", "tc05"],
                     help="FFN kernel family of bf16 layers (auto: chosen per call)")
     ap.add_argument("--experts", type=int, default=0, help="override E (smaller profiling cases)")
     ap.add_argument("--slots", type=int, default=0, help="override S (smaller profiling cases)")
@@ -165,6 +165,7 @@ TRAFFIC_SOURCES = {
     "ffn_mma": ["ffn_rows_mma.cu", "pipeline.cuh", "ffn_common.cuh", "internal.cuh"],  # tensor-core
     "ffn_mx": ["ffn_mx_tma.cu", "ffn_common.cuh", "internal.cuh"],     # mxfp4 tensor maps
     "ffn_fp8": ["ffn_rows_mma.cu", "pipeline.cuh", "ffn_common.cuh", "internal.cuh"],  # block FP8
+    "ffn_tc05": ["ffn_tc05.cu", "pipeline.cuh", "ffn_common.cuh", "internal.cuh"],  # bf16 tcgen05
 }
 
 
@@ -377,7 +378,7 @@ def run_gpu(args):
     cache = synthetic_cache(cfg, max(max(cfg.bs_list), bs, PREFILL_BS) * cfg.topk, alias_all=True, stream=stream)
     cache.set_copy_mode({"fused": F.COPY_FUSED, "per_bank": F.COPY_PER_BANK, "engine": F.COPY_ENGINE}[args.copy_mode])
     if args.ffn_kernels != "auto":
-        cache.set_ffn_kernels({"rows": F.FFN_ROWS, "mma": F.FFN_MMA}[args.ffn_kernels])
+        cache.set_ffn_kernels({"rows": F.FFN_ROWS, "mma": F.FFN_MMA, "tc05": F.FFN_TC05}[args.ffn_kernels])
     ffn_kind = ffn_family(F, cache, cfg, bs)
     s = stream.cuda_stream
     d_ids = torch.from_numpy(r.topk_ids).cuda()
@@ -559,6 +560,7 @@ def run_gpu(args):
 # weight format the FFN computes from (the copy moves bytes); every format accumulates in fp32
 DTYPE_OF = {"bf16": "bf16", "nvfp4": "nvfp4", "mxfp4": "mxfp4", "fp8": "e4m3", "q4_0": "q4_0", "raw": "u8"}
 FAMILY_NAMES = {"ffn_rows": "CUDA-core bulk-copy pipeline", "ffn_mma": "tensor-core pipeline (mma.sync)",
+                "ffn_tc05": "tcgen05 pipeline (TMEM accumulators)",
                 "ffn_mx": "mxfp4 tensor-map pipeline (mma.sync)", "ffn_fp8": "block-FP8 tensor-map pipeline (mma.sync)"}
 
 
@@ -568,8 +570,12 @@ def ffn_family(F, cache, cfg, bs):
         return "ffn_mx"
     if cfg.fmt == "fp8":
         return "ffn_fp8"
-    if cfg.fmt == "bf16" and F.ftmoe_ffn_kernels_for(cache.handle, bs, cfg.topk) == F.FFN_MMA:
-        return "ffn_mma"
+    if cfg.fmt == "bf16":
+        kind = F.ftmoe_ffn_kernels_for(cache.handle, bs, cfg.topk)
+        if kind == F.FFN_TC05:
+            return "ffn_tc05"
+        if kind == F.FFN_MMA:
+            return "ffn_mma"
     return "ffn_rows"
 
 

@@ -330,12 +330,14 @@ int ftmoe_set_copy_mode(ftmoe_cache_t *c, int32_t mode) {
 
 int ftmoe_set_ffn_kernels(ftmoe_cache_t *c, int32_t kind) {
     if (!c) return fail(FTMOE_ERR_INVALID_ARG, "cache is NULL");
-    if (kind != FTMOE_FFN_AUTO && kind != FTMOE_FFN_ROWS && kind != FTMOE_FFN_MMA)
+    if (kind != FTMOE_FFN_AUTO && kind != FTMOE_FFN_ROWS && kind != FTMOE_FFN_MMA && kind != FTMOE_FFN_TC05)
         return fail(FTMOE_ERR_INVALID_ARG, "unknown FFN kernel kind %d", kind);
     if (kind != FTMOE_FFN_AUTO && c->fmt != FTMOE_FMT_BF16)
-        return fail(FTMOE_ERR_FORMAT, "only bf16 caches have two FFN kernel families");
+        return fail(FTMOE_ERR_FORMAT, "only bf16 caches have several FFN kernel families");
     if (kind == FTMOE_FFN_MMA && !c->mx.valid)
         return fail(FTMOE_ERR_FORMAT, "no tensor-core FFN for this cache (H, I multiples of 256 and FFN scratch)");
+    if (kind == FTMOE_FFN_TC05 && !c->mx.tc_valid)
+        return fail(FTMOE_ERR_FORMAT, "no tcgen05 FFN for this cache (H, I multiples of 256 and FFN scratch)");
     c->ffn_kernels = kind;
     return FTMOE_OK;
 }
@@ -351,7 +353,7 @@ int ftmoe_ffn_kernels_for(ftmoe_cache_t *c, int32_t bs, int32_t topk, int32_t *k
     p.fmt = c->fmt; p.H = c->H; p.I = c->I; p.S = c->S; p.bs = bs; p.topk = topk; p.P = bs * topk;
     p.E = c->E;
     if (c->fmt == FTMOE_FMT_BF16)
-        *kind = ffn_bf16_uses_mma(p, c->num_sms, &c->mx, c->ffn_kernels) ? FTMOE_FFN_MMA : FTMOE_FFN_ROWS;
+        *kind = ffn_bf16_family(p, c->num_sms, &c->mx, c->ffn_kernels);
     else  // block FP8 and mxfp4 run on the tensor cores, nvfp4 and Q4_0 on the CUDA cores
         *kind = (c->fmt == FTMOE_FMT_FP8 || (c->fmt == FTMOE_FMT_MXFP4 && c->mx.valid)) ? FTMOE_FFN_MMA
                                                                                         : FTMOE_FFN_ROWS;

@@ -738,13 +738,16 @@ cudaError_t launch_dyn(K kernel, int grid, size_t smem, cudaStream_t st, const F
 
 }  // namespace
 
-bool ffn_bf16_uses_mma(const FfnParams &p, int num_sms, const MxTmaMaps *mx, int kernels) {
-    // AUTO: the tensor-core pipeline, except around one routed token per expert (E/4 <= P <
+int ffn_bf16_family(const FfnParams &p, int num_sms, const MxTmaMaps *mx, int kernels) {
+    if (num_sms <= 0 || p.fmt != FTMOE_FMT_BF16) return FTMOE_FFN_ROWS;
+    if (kernels == FTMOE_FFN_TC05 && ffn_bf16_tc05_supported(p, mx)) return FTMOE_FFN_TC05;
+    // AUTO: the mma.sync pipeline, except around one routed token per expert (E/4 <= P <
     // 2E), where the CUDA-core pipeline, which needs no cross-warp reduction per item, is
     // about 1% faster; from two tokens per expert up the tensor cores win by 10-35%
     const bool one_per_expert = 4 * (int64_t)p.P >= p.E && p.P < 2 * (int64_t)p.E;
-    return num_sms > 0 && kernels != FTMOE_FFN_ROWS && ffn_bf16_mma_supported(p, mx) &&
-           (kernels == FTMOE_FFN_MMA || !one_per_expert);
+    const bool mma = kernels != FTMOE_FFN_ROWS && ffn_bf16_mma_supported(p, mx) &&
+                     (kernels == FTMOE_FFN_MMA || kernels == FTMOE_FFN_TC05 || !one_per_expert);
+    return mma ? FTMOE_FFN_MMA : FTMOE_FFN_ROWS;
 }
 
 cudaError_t launch_ffn(const FfnParams &p_in, int num_sms, cudaStream_t st, const MxTmaMaps *mx, int kernels) {
@@ -755,8 +758,10 @@ cudaError_t launch_ffn(const FfnParams &p_in, int num_sms, cudaStream_t st, cons
         e = cudaFuncSetAttribute(ffn_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)route_smem);
         if (e != cudaSuccess) return e;
     }
-    const bool bf16_mma = ffn_bf16_uses_mma(p, num_sms, mx, kernels);
-    const bool fp4_rows_tma = num_sms > 0 && !bf16_mma && ffn_rows_tma_supported(p);
+    const int bf16_family = ffn_bf16_family(p, num_sms, mx, kernels);
+    const bool bf16_tc05 = bf16_family == FTMOE_FFN_TC05;
+    const bool bf16_mma = bf16_family == FTMOE_FFN_MMA;
+    const bool fp4_rows_tma = num_sms > 0 && !bf16_mma && !bf16_tc05 && ffn_rows_tma_supported(p);
     const bool mx_tma = num_sms > 0 && ffn_mx_tma_supported(p, mx);
     const bool fp8_tma = num_sms > 0 && ffn_fp8_tma_supported(p, mx);
     if (p.fmt == FTMOE_FMT_FP8 && !fp8_tma) return cudaErrorNotSupported;  // block FP8 has one pipeline only
@@ -765,7 +770,7 @@ cudaError_t launch_ffn(const FfnParams &p_in, int num_sms, cudaStream_t st, cons
         (fp4_rows_tma && (p.fmt == FTMOE_FMT_NVFP4 || p.fmt == FTMOE_FMT_Q4_0)) || mx_tma || fp8_tma;
     p.x16_emax = p.fmt == FTMOE_FMT_MXFP4 ? 9 : (p.fmt == FTMOE_FMT_Q4_0 ? 8 : 10);
     p.x16_swz = fp4_rows_tma && p.fmt == FTMOE_FMT_NVFP4 ? 1 : (fp4_rows_tma && p.fmt == FTMOE_FMT_Q4_0 ? 2 : 0);
-    p.pass_tokens = (mx_tma || fp8_tma || bf16_mma) ? kMxPassTokens : kPassTokens;
+    p.pass_tokens = bf16_tc05 ? kTc05PassTokens : ((mx_tma || fp8_tma || bf16_mma) ? kMxPassTokens : kPassTokens);
     {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(1 + (want_x16 ? p.bs : 0));
@@ -783,7 +788,10 @@ cudaError_t launch_ffn(const FfnParams &p_in, int num_sms, cudaStream_t st, cons
     const int umax = p.P < p.S ? p.P : p.S;  // distinct slots at most
     const size_t budget = 64 * 1024;
     bool pdl_combine = false;
-    if (bf16_mma) {
+    if (bf16_tc05) {
+        if ((e = launch_ffn_bf16_tc05(p, *mx, num_sms, st)) != cudaSuccess) return e;
+        pdl_combine = true;
+    } else if (bf16_mma) {
         if ((e = launch_ffn_bf16_mma(p, *mx, num_sms, st)) != cudaSuccess) return e;
         pdl_combine = true;
     } else if (fp4_rows_tma) {

@@ -537,6 +537,9 @@ bool make_bf16_tma_maps(MxTmaMaps &m, const unsigned char *const *banks, int S, 
     bool ok = encode_u8(m.gu_blocks, banks[0], 2ull * H, 2ull * I, (uint64_t)S, 64, sw) &&
               encode_u8(m.dn_blocks, banks[1], 2ull * I, (uint64_t)H, (uint64_t)S, 64, sw);
     m.valid = ok;
+    // the tcgen05 pipeline: boxes of 128 bytes x 128 rows (the UMMA's M)
+    m.tc_valid = ok && encode_u8(m.tc_gu, banks[0], 2ull * H, 2ull * I, (uint64_t)S, 128, sw) &&
+                 encode_u8(m.tc_dn, banks[1], 2ull * I, (uint64_t)H, (uint64_t)S, 128, sw);
     return ok;
 }
 

@@ -86,6 +86,7 @@ struct FfnScratch {
 // kernels (mxfp4, block FP8, bf16; the MMA's N = 8) kMxPassTokens.
 constexpr int kPassTokens = 4;
 constexpr int kMxPassTokens = 8;
+constexpr int kTc05PassTokens = 16;  // bf16 tcgen05 pipeline: the UMMA's N
 
 struct FfnParams {
     FfnScratch s;
@@ -113,11 +114,16 @@ struct MxTmaMaps {
     alignas(128) unsigned char dn_blocks[128];
     alignas(128) unsigned char dn_scales[128];
     bool valid = false;
+    // bf16 weight maps of the tcgen05 pipeline (boxes of 128 bytes x 128 rows)
+    alignas(128) unsigned char tc_gu[128];
+    alignas(128) unsigned char tc_dn[128];
+    bool tc_valid = false;
 };
 bool make_mx_tma_maps(MxTmaMaps &m, const unsigned char *const *banks, int S, int H, int I);
-// kernels: FTMOE_FFN_* (bf16 caches: see ffn_bf16_uses_mma; other formats ignore it).
-// Whether a bf16 call runs the tensor-core pipeline (the AUTO rule lives here).
-bool ffn_bf16_uses_mma(const FfnParams &p, int num_sms, const MxTmaMaps *mx, int kernels);
+// kernels: FTMOE_FFN_* (bf16 caches: see ffn_bf16_family; other formats ignore it).
+// The kernel family a bf16 call runs: FTMOE_FFN_ROWS, FTMOE_FFN_MMA or FTMOE_FFN_TC05 (the
+// AUTO rule lives here).
+int ffn_bf16_family(const FfnParams &p, int num_sms, const MxTmaMaps *mx, int kernels);
 cudaError_t launch_ffn(const FfnParams &p, int num_sms, cudaStream_t st, const MxTmaMaps *mx = nullptr,
                        int kernels = FTMOE_FFN_AUTO);
 // Persistent bulk-copy pipeline for the row-major formats (bf16; nvfp4 with H, I multiples of 256).
@@ -134,6 +140,9 @@ cudaError_t launch_ffn_fp8_tma(const FfnParams &p, const MxTmaMaps &maps, int nu
 bool make_bf16_tma_maps(MxTmaMaps &m, const unsigned char *const *banks, int S, int H, int I);
 bool ffn_bf16_mma_supported(const FfnParams &p, const MxTmaMaps *maps);
 cudaError_t launch_ffn_bf16_mma(const FfnParams &p, const MxTmaMaps &maps, int num_sms, cudaStream_t st);
+// tcgen05 pipeline for bf16 (maps tc_gu / tc_dn; H a multiple of 64, I of 128, both phases fit).
+bool ffn_bf16_tc05_supported(const FfnParams &p, const MxTmaMaps *maps);
+cudaError_t launch_ffn_bf16_tc05(const FfnParams &p, const MxTmaMaps &maps, int num_sms, cudaStream_t st);
 
 // Record `msg` as the thread's last error message and return `code`.
 int report_error(int code, const char *msg);

@@ -24,7 +24,7 @@ DT_U8, DT_BF16, DT_F16, DT_E4M3, DT_E8M0, DT_F32, DT_Q4_0 = 0, 1, 2, 3, 4, 5, 6
 DTYPES = {"u8": DT_U8, "bf16": DT_BF16, "f16": DT_F16, "e4m3": DT_E4M3, "e8m0": DT_E8M0, "f32": DT_F32,
           "q4_0": DT_Q4_0}
 COPY_FUSED, COPY_PER_BANK, COPY_ENGINE = 0, 1, 2
-FFN_AUTO, FFN_ROWS, FFN_MMA = 0, 1, 2
+FFN_AUTO, FFN_ROWS, FFN_MMA, FFN_TC05 = 0, 1, 2, 3
 MAX_BANKS = 8
 
 EXPORTS = [

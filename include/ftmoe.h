@@ -106,6 +106,9 @@ extern "C" {
 #define FTMOE_FFN_ROWS 1   /* CUDA-core bulk-copy pipeline: fp32 FMAs, passes of 4 tokens */
 #define FTMOE_FFN_MMA 2    /* tensor-core pipeline: bf16 mma.sync, passes of 8 tokens,
                               h kept as two bf16 terms; needs H and I multiples of 256 */
+#define FTMOE_FFN_TC05 3   /* 5th-generation tensor cores: tcgen05.mma with accumulators in
+                              TMEM (M = 128 rows, N = 16 tokens), passes of 16 tokens, h kept
+                              as two bf16 terms; needs H and I multiples of 256 */
 
 /* Limits of one cache. */
 #define FTMOE_MAX_BANKS 8

@@ -215,6 +215,42 @@ def test_workload_points(key):
     cache.close()
 
 
+@pytest.mark.parametrize("key,bs,mr", [("c2", 16, 1.0), ("c2", 64, 0.5), ("c5", 1, 1.0)])
+def test_bf16_tc05_full_size(key, bs, mr):
+    """The tcgen05 bf16 pipeline on full-size bf16 layers (every token against the oracle):
+    one routed token per expert at bs 16, hot experts over several passes of 16 tokens at
+    bs 64, and the decode-trace layer shape (H 4096, I 1536) at bs 1."""
+    cfg = wl.CONFIGS[key]
+    if key == "c5":  # the trace layer's geometry with a single layer's banks and a small pool
+        cfg = wl.scaled(cfg, E=16, S=16, L=2, steps=0, bs_list=(1,), mr_list=(1.0,), ids="uniform")
+    cache = synthetic_cache(cfg, bs * cfg.topk)
+    cache.set_ffn_kernels(F.FFN_TC05)
+    r = wl.make_route(cfg, bs, mr) if key != "c5" else None
+    if r is None:
+        rng = np.random.default_rng(5)
+        ids = np.stack([rng.choice(cfg.E, cfg.topk, replace=False) for _ in range(bs)]).astype(np.int32)
+        w = rng.random((bs, cfg.topk)).astype(np.float32)
+        w /= w.sum(axis=1, keepdims=True)
+        x = wl.f32_to_bf16_bits(rng.standard_normal((bs, cfg.H)).astype(np.float32))
+    else:
+        ids, w, x = r.topk_ids, r.weights, r.x
+    slot_of = _install_all(cache, cfg, np.random.default_rng(9)) if cfg.E <= cfg.S else None
+    if slot_of is None:  # install only the routed experts, in ascending slots
+        used = sorted(set(int(v) for v in ids.reshape(-1)))
+        slot_of = {e: i for i, e in enumerate(used)}
+        for b in range(cache.nb):
+            for e, sl in slot_of.items():
+                cache.slots[b][sl].copy_(cache.host[b][0][e])
+    slots = np.vectorize(slot_of.get)(ids).astype(np.int32)
+    d_y = torch.empty((bs, cfg.H), dtype=torch.bfloat16, device="cuda")
+    cache.ffn(x_dev(x), to_dev(slots), to_dev(w), d_y)
+    assert cache.status() == F.OK
+    assert F.ftmoe_ffn_kernels_for(cache.handle, bs, cfg.topk) == F.FFN_TC05
+    ref = oracle_ffn(cache, 0, ids, w, x)
+    assert_ffn_close(bf16_to_f64(d_y), ref, f"tc05 {key} bs={bs}")
+    cache.close()
+
+
 # ------------------------------------------------------------------ FFN on small geometries
 
 
@@ -278,6 +314,8 @@ FOLD = [
     ("bf16", F.FFN_ROWS, dict(E=6, H=1024, I=256, L=2, S=6), 3),
     ("bf16", F.FFN_MMA, dict(E=6, H=1024, I=256, L=2, S=6), 3),
     ("bf16", F.FFN_MMA, dict(E=20, H=512, I=768, L=2, S=20), 30),   # 90 pairs, several passes
+    ("bf16", F.FFN_TC05, dict(E=6, H=1024, I=256, L=2, S=6), 3),
+    ("bf16", F.FFN_TC05, dict(E=4, H=512, I=768, L=2, S=4), 30),    # passes of 16 tokens and a ragged one
     ("nvfp4", F.FFN_AUTO, dict(E=5, H=2048, I=512, L=2, S=5), 4),
     ("q4_0", F.FFN_AUTO, dict(E=6, H=512, I=256, L=2, S=6), 4),
     ("mxfp4", F.FFN_AUTO, dict(E=5, H=576, I=320, L=2, S=5), 4),
@@ -342,9 +380,10 @@ def _install_all(cache, cfg, rng):
 
 @pytest.mark.parametrize("geo", [dict(E=6, H=1024, I=256, L=2, S=6), dict(E=5, H=512, I=768, L=2, S=7)])
 def test_bf16_ffn_kernel_families(geo):
-    """Both bf16 FFN kernel families (CUDA-core rows pipeline, tensor-core pipeline) and the
-    automatic choice against the oracle on one routed batch: a hot expert over two passes
-    of eight tokens, duplicates within a row, several 64-row tiles per matrix."""
+    """Every bf16 FFN kernel family (CUDA-core rows pipeline, mma.sync pipeline, tcgen05
+    pipeline) and the automatic choice against the oracle on one routed batch: a hot expert
+    over two passes of eight tokens, duplicates within a row, several 64-row tiles per
+    matrix."""
     cfg = wl.scaled(wl.CONFIGS["c2"], topk=4, **geo)
     bs = 13
     cache = synthetic_cache(cfg, bs * cfg.topk)
@@ -357,7 +396,7 @@ def test_bf16_ffn_kernel_families(geo):
     slot_of = _install_all(cache, cfg, rng)
     slots = np.vectorize(slot_of.get)(ids).astype(np.int32)
     ref = oracle_ffn(cache, 0, ids, w, x)
-    for kind in (F.FFN_ROWS, F.FFN_MMA, F.FFN_AUTO):
+    for kind in (F.FFN_TC05, F.FFN_ROWS, F.FFN_MMA, F.FFN_AUTO):
         cache.set_ffn_kernels(kind)
         d_y = torch.empty((bs, cfg.H), dtype=torch.bfloat16, device="cuda")
         cache.ffn(x_dev(x), to_dev(slots), to_dev(w), d_y)
@@ -378,6 +417,8 @@ def test_ffn_kernel_selector_formats():
     assert kinds == {1: F.FFN_ROWS, 2: F.FFN_ROWS, 3: F.FFN_ROWS, 4: F.FFN_MMA, 8: F.FFN_MMA}, kinds
     c2.set_ffn_kernels(F.FFN_MMA)
     assert F.ftmoe_ffn_kernels_for(c2.handle, 2, 8) == F.FFN_MMA
+    c2.set_ffn_kernels(F.FFN_TC05)
+    assert F.ftmoe_ffn_kernels_for(c2.handle, 2, 8) == F.FFN_TC05
     c2.set_ffn_kernels(F.FFN_ROWS)
     assert F.ftmoe_ffn_kernels_for(c2.handle, 8, 8) == F.FFN_ROWS
     c2.close()
@@ -385,13 +426,14 @@ def test_ffn_kernel_selector_formats():
     assert F.ftmoe_ffn_kernels_for(c1.handle, 8, 1) == F.FFN_ROWS
     c1.set_ffn_kernels(F.FFN_ROWS)
     c1.set_ffn_kernels(F.FFN_AUTO)
-    with pytest.raises(F.FtmoeError) as ei:
-        c1.set_ffn_kernels(F.FFN_MMA)
-    assert ei.value.code == F.ERR_FORMAT
+    for kind in (F.FFN_MMA, F.FFN_TC05):
+        with pytest.raises(F.FtmoeError) as ei:
+            c1.set_ffn_kernels(kind)
+        assert ei.value.code == F.ERR_FORMAT
     c1.close()
     nv = synthetic_cache(wl.scaled(wl.CONFIGS["c3"], E=4, H=512, I=256, L=1, S=4), 8)
     nv.set_ffn_kernels(F.FFN_AUTO)
-    for kind in (F.FFN_ROWS, F.FFN_MMA):
+    for kind in (F.FFN_ROWS, F.FFN_MMA, F.FFN_TC05):
         with pytest.raises(F.FtmoeError) as ei:
             nv.set_ffn_kernels(kind)
         assert ei.value.code == F.ERR_FORMAT
