@@ -740,14 +740,19 @@ cudaError_t launch_dyn(K kernel, int grid, size_t smem, cudaStream_t st, const F
 
 int ffn_bf16_family(const FfnParams &p, int num_sms, const MxTmaMaps *mx, int kernels) {
     if (num_sms <= 0 || p.fmt != FTMOE_FMT_BF16) return FTMOE_FFN_ROWS;
-    if (kernels == FTMOE_FFN_TC05 && ffn_bf16_tc05_supported(p, mx)) return FTMOE_FFN_TC05;
-    // AUTO: the mma.sync pipeline, except around one routed token per expert (E/4 <= P <
-    // 2E), where the CUDA-core pipeline, which needs no cross-warp reduction per item, is
-    // about 1% faster; from two tokens per expert up the tensor cores win by 10-35%
+    if (kernels == FTMOE_FFN_ROWS) return FTMOE_FFN_ROWS;
+    if (kernels == FTMOE_FFN_MMA) return ffn_bf16_mma_supported(p, mx) ? FTMOE_FFN_MMA : FTMOE_FFN_ROWS;
+    const bool tc05 = ffn_bf16_tc05_supported(p, mx);
+    if (kernels == FTMOE_FFN_TC05 && tc05) return FTMOE_FFN_TC05;
+    // AUTO: the tensor cores, except around one routed token per expert (E/4 <= P < 2E), where
+    // the CUDA-core pipeline is 3-6% faster (c2 bs 16: 194 us against 206 us tcgen05 and
+    // 210 us mma.sync); from two tokens per expert up tcgen05 wins (bs 32: 207 / 221 / 218 us,
+    // bs 64: 209 / 242 / 330 us for tcgen05 / mma.sync / CUDA cores) and at bs 1 tcgen05 and
+    // mma.sync tie (28 us)
     const bool one_per_expert = 4 * (int64_t)p.P >= p.E && p.P < 2 * (int64_t)p.E;
-    const bool mma = kernels != FTMOE_FFN_ROWS && ffn_bf16_mma_supported(p, mx) &&
-                     (kernels == FTMOE_FFN_MMA || kernels == FTMOE_FFN_TC05 || !one_per_expert);
-    return mma ? FTMOE_FFN_MMA : FTMOE_FFN_ROWS;
+    if (kernels == FTMOE_FFN_AUTO && one_per_expert) return FTMOE_FFN_ROWS;
+    if (tc05) return FTMOE_FFN_TC05;
+    return ffn_bf16_mma_supported(p, mx) ? FTMOE_FFN_MMA : FTMOE_FFN_ROWS;
 }
 
 cudaError_t launch_ffn(const FfnParams &p_in, int num_sms, cudaStream_t st, const MxTmaMaps *mx, int kernels) {

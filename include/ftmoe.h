@@ -100,9 +100,9 @@ extern "C" {
 
 /* Expert FFN kernel families of a bf16 cache (other formats have one family each and
  * accept FTMOE_FFN_AUTO only) */
-#define FTMOE_FFN_AUTO 0   /* MMA where the shape has it, except ROWS when the call has
-                              about one routed pair per expert (E/4 <= bs*topk < 2E);
-                              default */
+#define FTMOE_FFN_AUTO 0   /* TC05 where the shape has it (else MMA), except ROWS when the
+                              call has about one routed pair per expert
+                              (E/4 <= bs*topk < 2E); default */
 #define FTMOE_FFN_ROWS 1   /* CUDA-core bulk-copy pipeline: fp32 FMAs, passes of 4 tokens */
 #define FTMOE_FFN_MMA 2    /* tensor-core pipeline: bf16 mma.sync, passes of 8 tokens,
                               h kept as two bf16 terms; needs H and I multiples of 256 */

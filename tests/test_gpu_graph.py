@@ -39,10 +39,10 @@ def _calls(cfg, bs, steps, seed):
 
 @pytest.mark.parametrize("bs", [2, 4])
 def test_decode_calls_replay_from_a_graph(bs):
-    # E = 16, topk 8: bs 2 routes 16 pairs (CUDA-core FFN), bs 4 routes 32 (tensor-core FFN)
+    # E = 16, topk 8: bs 2 routes 16 pairs (CUDA-core FFN), bs 4 routes 32 (tcgen05 FFN)
     cfg = wl.scaled(wl.CONFIGS["c2"], E=16, L=3, S=24)
     cache = synthetic_cache(cfg, bs * cfg.topk, host_layers=range(cfg.L))
-    expect = F.FFN_ROWS if bs == 2 else F.FFN_MMA
+    expect = F.FFN_ROWS if bs == 2 else F.FFN_TC05
     assert F.ftmoe_ffn_kernels_for(cache.handle, bs, cfg.topk) == expect
     calls = _calls(cfg, bs, steps=2, seed=bs)
     d_slots = [torch.empty((bs, cfg.topk), dtype=torch.int32, device="cuda") for _ in calls]

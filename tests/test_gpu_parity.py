@@ -413,8 +413,8 @@ def test_ffn_kernel_selector_formats():
     the AUTO choice as reported by ftmoe_ffn_kernels_for."""
     c2 = synthetic_cache(wl.scaled(wl.CONFIGS["c2"], E=16, L=1, S=16), 128)
     kinds = {bs: F.ftmoe_ffn_kernels_for(c2.handle, bs, 8) for bs in (1, 2, 3, 4, 8)}
-    # E = 16: ROWS for 4 <= 8 bs < 32 routed pairs (about one per expert), MMA otherwise
-    assert kinds == {1: F.FFN_ROWS, 2: F.FFN_ROWS, 3: F.FFN_ROWS, 4: F.FFN_MMA, 8: F.FFN_MMA}, kinds
+    # E = 16: ROWS for 4 <= 8 bs < 32 routed pairs (about one per expert), tcgen05 otherwise
+    assert kinds == {1: F.FFN_ROWS, 2: F.FFN_ROWS, 3: F.FFN_ROWS, 4: F.FFN_TC05, 8: F.FFN_TC05}, kinds
     c2.set_ffn_kernels(F.FFN_MMA)
     assert F.ftmoe_ffn_kernels_for(c2.handle, 2, 8) == F.FFN_MMA
     c2.set_ffn_kernels(F.FFN_TC05)
