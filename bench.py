@@ -188,7 +188,9 @@ def recorded_traffic(workload: str, kind: str, units: int = 0):
     `traffic-per-unit: <name> <kind> <hash> <read> <write> <units>` is a capture of a smaller
     case of the same layer (fewer experts) whose traffic grows in proportion to the units one
     launch processes (missed experts for the copy, distinct experts for the FFN): it is scaled
-    by `units` / <units>."""
+    by `units` / <units>; `traffic-affine: <name> <kind> <hash> <bytes per unit> <offset>` is
+    fitted to two such captures when traffic grows by a fixed amount per unit plus a constant
+    (the copy kernel: its last written lines are still dirty in L2 when it ends)."""
     pdir = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles")
     if not os.path.isdir(pdir):
         return None
@@ -207,6 +209,9 @@ def recorded_traffic(workload: str, kind: str, units: int = 0):
                 if len(parts) == 7 and parts[0] == "traffic-per-unit:" and parts[1] == name and parts[2] == kind \
                         and parts[3] == cur and units > 0:
                     scaled = int(round((int(parts[4]) + int(parts[5])) * units / int(parts[6])))
+                if len(parts) == 6 and parts[0] == "traffic-affine:" and parts[1] == name and parts[2] == kind \
+                        and parts[3] == cur and units > 0:
+                    scaled = int(round(float(parts[4]) * units + float(parts[5])))
     return scaled
 
 
