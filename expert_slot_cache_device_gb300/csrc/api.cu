@@ -148,6 +148,8 @@ struct ftmoe_cache {
     int num_sms;
     int copy_mode = FTMOE_COPY_FUSED;
     int ffn_kernels = FTMOE_FFN_AUTO;
+    int64_t dbg_wait_ns = 0;  // test settings (ftmoe_set_debug)
+    int dbg_skip_stage = 0;
     int last_layer = -1;
     bool vec16 = true;
     std::vector<std::vector<const void *>> host;      // [nb][L] host addresses
@@ -326,6 +328,21 @@ int ftmoe_set_copy_mode(ftmoe_cache_t *c, int32_t mode) {
         return fail(FTMOE_ERR_INVALID_ARG, "unknown copy mode %d", mode);
     c->copy_mode = mode;
     return FTMOE_OK;
+}
+
+int ftmoe_set_debug(ftmoe_cache_t *c, int32_t what, int64_t value) {
+    if (!c) return fail(FTMOE_ERR_INVALID_ARG, "cache is NULL");
+    if (what == FTMOE_DEBUG_WAIT_NS) {
+        if (value < 0) return fail(FTMOE_ERR_INVALID_ARG, "wait limit must be >= 0");
+        c->dbg_wait_ns = value;
+        return FTMOE_OK;
+    }
+    if (what == FTMOE_DEBUG_FFN_SKIP_STAGE) {
+        if (value != 0 && value != 1) return fail(FTMOE_ERR_INVALID_ARG, "skip setting must be 0 or 1");
+        c->dbg_skip_stage = (int)value;
+        return FTMOE_OK;
+    }
+    return fail(FTMOE_ERR_INVALID_ARG, "unknown debug setting %d", what);
 }
 
 int ftmoe_set_ffn_kernels(ftmoe_cache_t *c, int32_t kind) {
@@ -522,6 +539,8 @@ int ftmoe_expert_ffn_hybrid(ftmoe_cache_t *c, const void *d_x_bf16, int32_t bs, 
     p.status = c->t.status;
     p.fmt = c->fmt; p.H = c->H; p.I = c->I; p.S = c->S; p.bs = bs; p.topk = topk; p.P = (int)P;
     p.E = c->E;
+    p.wait_ns = (uint64_t)c->dbg_wait_ns;
+    p.debug_skip_stage = c->dbg_skip_stage;
     CK(launch_ffn(p, c->num_sms, static_cast<cudaStream_t>(stream), &c->mx, c->ffn_kernels), "ffn kernels");
     return FTMOE_OK;
 }

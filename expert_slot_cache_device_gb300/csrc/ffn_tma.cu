@@ -21,16 +21,19 @@
 // routing kernel, down's producer starts streaming its weights while gate_up drains
 // and waits only before it copies the h rows gate_up writes.
 //
-// Every mbarrier wait is bounded: on expiry the waiting thread records
-// FTMOE_ERR_STATE in the status word and leaves, and the producer waits (again
-// bounded) for its own copies in flight before it exits.
+// Every mbarrier wait is bounded (pipe::bar_wait): on expiry the waiting thread records
+// FTMOE_ERR_STATE in the status word and leaves, and the producer waits (again bounded) for
+// its own copies in flight before it exits. A test setting shortens the limit and leaves one
+// stage unfilled to exercise that path.
 #include "ffn_common.cuh"
 #include "internal.cuh"
+#include "pipeline.cuh"
 
 namespace ftmoe {
 namespace {
 
 using namespace ffn;
+using namespace pipe;
 
 enum { kGateUp = 0, kDown = 1 };
 
@@ -47,7 +50,6 @@ template <int FMT, int PHASE>
 constexpr int kTmaThreads = (kConsumerWarps<FMT, PHASE> + 1) * 32;
 constexpr int kMaxStages = 4;
 constexpr int kMaxTok = 4;  // tokens per stage
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any healthy wait
 
 struct StageHdr {
     int32_t slot, n0, rows, ntok, done, pad0, pad1, pad2;
@@ -64,69 +66,6 @@ struct TmaCfg {
     int32_t tok_bytes;   // bytes of one token vector
     int32_t tg;          // tokens per stage (<= kMaxTok)
 };
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Bounded wait for the phase with the given parity; false if the limit expired.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-    const uint32_t a = smem_u32(bar);
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t i = 0;; i++) {
-        uint32_t ok;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(ok)
-            : "r"(a), "r"(parity)
-            : "memory");
-        if (ok) return true;
-        if ((i & 255) == 255 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
-    }
-}
-
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
-                                         uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
-            "r"(smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-        : "memory");
-}
-
-__device__ __forceinline__ void bulk_g2s_plain(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ uint64_t evict_first_policy() {
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
 
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" :::); }
@@ -432,11 +371,12 @@ __global__ void __launch_bounds__(kTmaThreads<FMT, PHASE>, 1) ffn_rows_tma_kerne
     StageHdr *hdr = reinterpret_cast<StageHdr *>(sm + 128);
     unsigned char *stage0 = sm + 128 + kMaxStages * sizeof(StageHdr);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint64_t lim = p.wait_ns ? p.wait_ns : kWaitNs;  // limit of every bounded wait
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < c.stages; s++) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps<FMT, PHASE>);
+            bar_init(&full[s], 1);
+            bar_init(&empty[s], kConsumerWarps<FMT, PHASE>);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -453,7 +393,7 @@ __global__ void __launch_bounds__(kTmaThreads<FMT, PHASE>, 1) ffn_rows_tma_kerne
         const int npass = nu > 0 ? *p.s.n_passes : 0;
         const int items = npass * c.tiles;
         const int first = blockIdx.x;
-        const uint64_t pol = evict_first_policy();
+        const uint64_t pol = evict_first_l2();
         const int H = p.H, I = p.I, R = c.R;
         const int nout = PHASE == kGateUp ? I : H;
         const int64_t wr = Seg<FMT, PHASE>::wrow(H, I), sr = Seg<FMT, PHASE>::srow(H, I);
@@ -473,9 +413,15 @@ __global__ void __launch_bounds__(kTmaThreads<FMT, PHASE>, 1) ffn_rows_tma_kerne
                 const int ntok = cnt - g0 < c.tg ? cnt - g0 : c.tg;
                 const int s = issued % c.stages;
                 const uint32_t ph = (issued / c.stages) & 1;
-                if (!mbar_wait(&empty[s], ph ^ 1)) {
+                if (!bar_wait(&empty[s], ph ^ 1, lim)) {
                     ok = false;
                     break;
+                }
+                if (PHASE == kGateUp && p.debug_skip_stage && blockIdx.x == 0 && issued == 0) {
+                    // test setting: this CTA's first stage is left unfilled (no copies, no
+                    // arrive), so its consumers' bounded wait runs out
+                    issued++;
+                    continue;
                 }
                 StageHdr &hh = hdr[s];
                 hh.slot = slot; hh.n0 = n0; hh.rows = rows; hh.ntok = ntok; hh.done = 0;
@@ -484,32 +430,32 @@ __global__ void __launch_bounds__(kTmaThreads<FMT, PHASE>, 1) ffn_rows_tma_kerne
                     hh.texp[i] = (PHASE == kGateUp && kF16Act<FMT>) ? p.s.xexp[hh.pairs[i] / p.topk] : 0;
                 }
                 const uint32_t wbytes = (uint32_t)Seg<FMT, PHASE>::bytes(rows, H, I);
-                mbar_expect_tx(&full[s], wbytes + (uint32_t)(ntok * c.tok_bytes));
+                bar_expect(&full[s], wbytes + (uint32_t)(ntok * c.tok_bytes));
                 unsigned char *st = stage0 + (size_t)s * c.stage_bytes;
                 if (PHASE == kGateUp) {
                     const unsigned char *wb = p.bank[0] + (int64_t)slot * p.bank_bytes[0];
-                    bulk_g2s(st, wb + n0 * wr, (uint32_t)(rows * wr), &full[s], pol);
-                    bulk_g2s(st + R * wr, wb + ((int64_t)I + n0) * wr, (uint32_t)(rows * wr), &full[s], pol);
+                    bulk1d_hint(st, wb + n0 * wr, (uint32_t)(rows * wr), &full[s], pol);
+                    bulk1d_hint(st + R * wr, wb + ((int64_t)I + n0) * wr, (uint32_t)(rows * wr), &full[s], pol);
                     if (FMT == FTMOE_FMT_NVFP4) {
                         const unsigned char *sb = p.bank[1] + (int64_t)slot * p.bank_bytes[1];
-                        bulk_g2s(st + 2 * R * wr, sb + n0 * sr, (uint32_t)(rows * sr), &full[s], pol);
-                        bulk_g2s(st + 2 * R * wr + R * sr, sb + ((int64_t)I + n0) * sr, (uint32_t)(rows * sr),
+                        bulk1d_hint(st + 2 * R * wr, sb + n0 * sr, (uint32_t)(rows * sr), &full[s], pol);
+                        bulk1d_hint(st + 2 * R * wr + R * sr, sb + ((int64_t)I + n0) * sr, (uint32_t)(rows * sr),
                                  &full[s], pol);
                         // per-row globals: rows * 2 bytes, a multiple of 16 (rows is a multiple of 8)
                         const unsigned char *gb = p.bank[2] + (int64_t)slot * p.bank_bytes[2];
                         unsigned char *gd = st + Seg<FMT, PHASE>::goff(R, H, I);
-                        bulk_g2s(gd, gb + 2 * (int64_t)n0, (uint32_t)(2 * rows), &full[s], pol);
-                        bulk_g2s(gd + 2 * R, gb + 2 * ((int64_t)I + n0), (uint32_t)(2 * rows), &full[s], pol);
+                        bulk1d_hint(gd, gb + 2 * (int64_t)n0, (uint32_t)(2 * rows), &full[s], pol);
+                        bulk1d_hint(gd + 2 * R, gb + 2 * ((int64_t)I + n0), (uint32_t)(2 * rows), &full[s], pol);
                     }
                 } else {
                     const int wb_i = FMT == FTMOE_FMT_NVFP4 ? 3 : 1;
                     const unsigned char *wb = p.bank[wb_i] + (int64_t)slot * p.bank_bytes[wb_i];
-                    bulk_g2s(st, wb + n0 * wr, (uint32_t)(rows * wr), &full[s], pol);
+                    bulk1d_hint(st, wb + n0 * wr, (uint32_t)(rows * wr), &full[s], pol);
                     if (FMT == FTMOE_FMT_NVFP4) {
                         const unsigned char *sb = p.bank[4] + (int64_t)slot * p.bank_bytes[4];
-                        bulk_g2s(st + R * wr, sb + n0 * sr, (uint32_t)(rows * sr), &full[s], pol);
+                        bulk1d_hint(st + R * wr, sb + n0 * sr, (uint32_t)(rows * sr), &full[s], pol);
                         const unsigned char *gb = p.bank[5] + (int64_t)slot * p.bank_bytes[5];
-                        bulk_g2s(st + Seg<FMT, PHASE>::goff(R, H, I), gb + 2 * (int64_t)n0, (uint32_t)(2 * rows),
+                        bulk1d_hint(st + Seg<FMT, PHASE>::goff(R, H, I), gb + 2 * (int64_t)n0, (uint32_t)(2 * rows),
                                  &full[s], pol);
                     }
                 }
@@ -536,16 +482,16 @@ __global__ void __launch_bounds__(kTmaThreads<FMT, PHASE>, 1) ffn_rows_tma_kerne
                     const void *src = PHASE == kGateUp
                                           ? static_cast<const void *>(xsrc + (int64_t)(q / p.topk) * H)
                                           : static_cast<const void *>(p.s.h + (int64_t)q * I);
-                    bulk_g2s_plain(st + c.tok_off + i * c.tok_bytes, src, (uint32_t)c.tok_bytes, &full[s]);
+                    bulk1d(st + c.tok_off + i * c.tok_bytes, src, (uint32_t)c.tok_bytes, &full[s]);
                 }
                 issued++;
             }
         }
         if (ok) {  // end marker
             const int s = issued % c.stages;
-            if (mbar_wait(&empty[s], ((issued / c.stages) & 1) ^ 1)) {
+            if (bar_wait(&empty[s], ((issued / c.stages) & 1) ^ 1, lim)) {
                 hdr[s].done = 1;
-                mbar_arrive(&full[s]);
+                bar_arrive(&full[s]);
             } else {
                 ok = false;
             }
@@ -554,7 +500,7 @@ __global__ void __launch_bounds__(kTmaThreads<FMT, PHASE>, 1) ffn_rows_tma_kerne
             atomicCAS(p.status, 0, FTMOE_ERR_STATE);
             // wait (bounded) until the copies already issued have landed
             for (int j = issued - c.stages < 0 ? 0 : issued - c.stages; j < issued; j++)
-                mbar_wait(&full[j % c.stages], (j / c.stages) & 1);
+                bar_wait(&full[j % c.stages], (j / c.stages) & 1, lim);
         }
         return;
     }
@@ -563,7 +509,7 @@ __global__ void __launch_bounds__(kTmaThreads<FMT, PHASE>, 1) ffn_rows_tma_kerne
     HMax hm;
     for (int k = 0;; k++) {
         const int s = k % c.stages;
-        if (!mbar_wait(&full[s], (k / c.stages) & 1)) {
+        if (!bar_wait(&full[s], (k / c.stages) & 1, lim)) {
             if (lane == 0) atomicCAS(p.status, 0, FTMOE_ERR_STATE);
             return;
         }
@@ -589,7 +535,7 @@ __global__ void __launch_bounds__(kTmaThreads<FMT, PHASE>, 1) ffn_rows_tma_kerne
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+        if (lane == 0) bar_arrive(&empty[s]);
     }
 }
 

@@ -104,6 +104,10 @@ struct FfnParams {
     int32_t x16_emax;  // f16 activation copy keeps max |x| < 2^x16_emax
     int32_t x16_swz;   // f16 activation copy layout: 0 plain, 1 swz_x16 (nvfp4), 2 swz_q4x16 (Q4_0)
     int32_t pass_tokens;  // tokens per pass of the pipelined kernels (kPassTokens / kMxPassTokens)
+    // test settings (ftmoe_set_debug): limit of the CUDA-core pipeline's bounded waits (0: the
+    // default), and 1 to leave CTA 0's first gate_up stage unfilled so that a wait runs out
+    uint64_t wait_ns;
+    int32_t debug_skip_stage;
 };
 
 // Tensor maps (CUtensorMap, 128 bytes each) of the tensor-map pipelines: the transposed

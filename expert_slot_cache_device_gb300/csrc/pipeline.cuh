@@ -26,7 +26,9 @@ __device__ __forceinline__ void bar_expect(uint64_t *b, uint32_t bytes) {
 __device__ __forceinline__ void bar_arrive(uint64_t *b) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
 }
-__device__ __forceinline__ bool bar_wait(uint64_t *b, uint32_t parity) {
+// Bounded wait for the phase with the given parity: false once `limit_ns` of %globaltimer have
+// passed (the default is far beyond any healthy wait; a shorter limit is a test setting).
+__device__ __forceinline__ bool bar_wait(uint64_t *b, uint32_t parity, uint64_t limit_ns = kWaitNs) {
     const uint64_t t0 = gtimer();
     for (uint32_t i = 0;; i++) {
         uint32_t ok;
@@ -38,7 +40,7 @@ __device__ __forceinline__ bool bar_wait(uint64_t *b, uint32_t parity) {
             : "r"(su32(b)), "r"(parity)
             : "memory");
         if (ok) return true;
-        if ((i & 255) == 255 && gtimer() - t0 > kWaitNs) return false;
+        if ((i & 255) == 255 && gtimer() - t0 > limit_ns) return false;
     }
 }
 
@@ -66,6 +68,16 @@ __device__ __forceinline__ uint64_t evict_first_l2() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
     return pol;
+}
+
+// 1-D bulk copy global -> shared with an L2 cache policy, completing on an mbarrier.
+__device__ __forceinline__ void bulk1d_hint(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                            uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+            "r"(su32(dst)),
+        "l"(src), "r"(bytes), "r"(su32(bar)), "l"(policy)
+        : "memory");
 }
 
 __device__ __forceinline__ void bulk1d(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {

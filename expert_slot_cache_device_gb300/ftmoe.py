@@ -25,6 +25,7 @@ DTYPES = {"u8": DT_U8, "bf16": DT_BF16, "f16": DT_F16, "e4m3": DT_E4M3, "e8m0": 
           "q4_0": DT_Q4_0}
 COPY_FUSED, COPY_PER_BANK, COPY_ENGINE = 0, 1, 2
 FFN_AUTO, FFN_ROWS, FFN_MMA, FFN_TC05 = 0, 1, 2, 3
+DEBUG_WAIT_NS, DEBUG_FFN_SKIP_STAGE = 1, 2
 MAX_BANKS = 8
 
 EXPORTS = [
@@ -34,7 +35,7 @@ EXPORTS = [
     "ftmoe_last_error", "ftmoe_expert_ffn_noalloc", "ftmoe_ensure_experts_hybrid", "ftmoe_hybrid_fetch_fraction",
     "ftmoe_expert_ffn_hybrid", "ftmoe_cpu_expert_ffn", "ftmoe_prefetch_layer", "ftmoe_prefill_layers",
     "ftmoe_measure_link", "ftmoe_measure_cpu_moe", "ftmoe_moe_backend_decision", "ftmoe_get_counters",
-    "ftmoe_set_ffn_kernels", "ftmoe_ffn_kernels_for", "ftmoe_measure_cpu_read",
+    "ftmoe_set_ffn_kernels", "ftmoe_ffn_kernels_for", "ftmoe_measure_cpu_read", "ftmoe_set_debug",
 ]
 BACKEND_OFFLOAD, BACKEND_HYBRID = 0, 1
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -79,6 +80,7 @@ def lib() -> ctypes.CDLL:
         "ftmoe_expert_ffn": [P, P, i32, P, P, i32, P, P],
         "ftmoe_set_copy_mode": [P, i32],
         "ftmoe_set_ffn_kernels": [P, i32],
+        "ftmoe_set_debug": [P, i32, ctypes.c_int64],
         "ftmoe_ffn_kernels_for": [P, i32, i32, P],
         "ftmoe_cache_get_state": [P, P, P, P, P],
         "ftmoe_cache_set_state": [P, P, P, u32, P],
@@ -171,6 +173,11 @@ def ftmoe_set_copy_mode(cache: int, mode: int) -> None:
 
 def ftmoe_set_ffn_kernels(cache: int, kind: int) -> None:
     _check(lib().ftmoe_set_ffn_kernels(cache, kind))
+
+
+def ftmoe_set_debug(cache: int, what: int, value: int) -> None:
+    """Test settings (bounded-wait limit, a stage left unfilled); see include/ftmoe.h."""
+    _check(lib().ftmoe_set_debug(cache, what, value))
 
 
 def ftmoe_ffn_kernels_for(cache: int, bs: int, topk: int) -> int:

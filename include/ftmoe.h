@@ -347,6 +347,20 @@ int ftmoe_set_ffn_kernels(ftmoe_cache_t *cache, int32_t kind);
  * FFN scratch. Host only. */
 int ftmoe_ffn_kernels_for(ftmoe_cache_t *cache, int32_t bs, int32_t topk, int32_t *kind);
 
+/* Test settings of one cache, for exercising the bounded-wait error path (the pages define
+ * nothing of the kind; production callers leave them at 0):
+ *   FTMOE_DEBUG_WAIT_NS        value = the limit, in ns, of every bounded wait of the CUDA-core
+ *                              FFN pipeline (0 restores the default of 2 s);
+ *   FTMOE_DEBUG_FFN_SKIP_STAGE value = 1: later FFN calls that run the CUDA-core pipeline leave
+ *                              the first gate_up stage of CTA 0 unfilled (no copies issued, no
+ *                              arrive), so that CTA's consumers stop when their wait runs out:
+ *                              the call records FTMOE_ERR_STATE in the status word, leaves y
+ *                              undefined and returns with nothing in flight; 0 turns it off.
+ * FTMOE_ERR_INVALID_ARG for an unknown setting or value. Host only. */
+#define FTMOE_DEBUG_WAIT_NS 1
+#define FTMOE_DEBUG_FFN_SKIP_STAGE 2
+int ftmoe_set_debug(ftmoe_cache_t *cache, int32_t what, int64_t value);
+
 /* Read the state into host arrays h_owner[S] (flat id or -1), h_stamp[S], *h_clock.
  * Synchronises the stream. */
 int ftmoe_cache_get_state(ftmoe_cache_t *cache, int32_t *h_owner, uint32_t *h_stamp,

@@ -102,7 +102,7 @@ def test_binding_constants_match_the_header():
         if hasattr(F, name):
             assert getattr(F, name) == val, name
             checked += 1
-    for family in ("ERR_", "FMT_", "DT_", "COPY_", "FFN_", "BACKEND_"):
+    for family in ("ERR_", "FMT_", "DT_", "COPY_", "FFN_", "BACKEND_", "DEBUG_"):
         names = [n for n in defs if n.startswith(family)]
         assert names and all(hasattr(F, n) for n in names), family
     assert checked >= 30
