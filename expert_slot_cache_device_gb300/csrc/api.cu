@@ -5,11 +5,22 @@
 #include <cstring>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "internal.cuh"
 
 using namespace ftmoe;
 
 namespace {
+
+// NVTX range around a hot-path call (K1 ensure, K2 copy, K3 FFN, prefetch, prefill): shown by
+// Nsight tools on the host timeline; without a tool attached it costs two no-op calls.
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
 
 thread_local char g_err[512] = "";
 
@@ -410,12 +421,14 @@ static int ensure_impl(ftmoe_cache_t *c, int32_t layer, const int32_t *d_topk_id
 
 int ftmoe_ensure_experts(ftmoe_cache_t *c, int32_t layer, const int32_t *d_topk_ids, int32_t bs, int32_t topk,
                          int32_t *d_slots_out, void *stream) {
+    NvtxRange nvtx_range("ftmoe_ensure_experts");
     return ensure_impl(c, layer, d_topk_ids, bs, topk, d_slots_out, 0, -1, 0.f, nullptr, stream);
 }
 
 int ftmoe_ensure_experts_hybrid(ftmoe_cache_t *c, int32_t layer, const int32_t *d_topk_ids, int32_t bs,
                                 int32_t topk, int32_t max_fetch, float fetch_fraction, int32_t *d_slots_out,
                                 int32_t *d_counts, void *stream) {
+    NvtxRange nvtx_range("ftmoe_ensure_experts_hybrid");
     return ensure_impl(c, layer, d_topk_ids, bs, topk, d_slots_out, 1, max_fetch, fetch_fraction, d_counts, stream);
 }
 
@@ -434,6 +447,10 @@ static void fill_copy_params(const ftmoe_cache *c, int b_first, int b_count, Cop
     memset(&p, 0, sizeof p);
     p.nb = b_count;
     p.E = c->E;
+    p.L = c->L;
+    p.S = c->S;
+    p.maxm = c->E < c->S ? c->E : c->S;
+    p.status = c->t.status;
     p.miss_ids = c->t.miss_ids;
     p.miss_slots = c->t.miss_slots;
     p.num_miss = c->t.num_miss;
@@ -486,6 +503,7 @@ static int copy_engine(ftmoe_cache_t *c, cudaStream_t read_st, cudaStream_t copy
 }
 
 int ftmoe_copy_missing(ftmoe_cache_t *c, void *stream) {
+    NvtxRange nvtx_range("ftmoe_copy_missing");
     if (!c) return fail(FTMOE_ERR_INVALID_ARG, "cache is NULL");
     if (c->last_layer < 0) return fail(FTMOE_ERR_STATE, "copy_missing before any ensure_experts call");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -508,12 +526,14 @@ int ftmoe_copy_missing(ftmoe_cache_t *c, void *stream) {
 
 int ftmoe_expert_ffn(ftmoe_cache_t *c, const void *d_x_bf16, int32_t bs, const int32_t *d_slots,
                      const float *d_weights, int32_t topk, void *d_y_bf16, void *stream) {
+    NvtxRange nvtx_range("ftmoe_expert_ffn");
     return ftmoe_expert_ffn_hybrid(c, d_x_bf16, bs, d_slots, d_weights, topk, nullptr, d_y_bf16, stream);
 }
 
 int ftmoe_expert_ffn_hybrid(ftmoe_cache_t *c, const void *d_x_bf16, int32_t bs, const int32_t *d_slots,
                             const float *d_weights, int32_t topk, const float *d_addend, void *d_y_bf16,
                             void *stream) {
+    NvtxRange nvtx_range("ftmoe_expert_ffn_hybrid");
     if (!c) return fail(FTMOE_ERR_INVALID_ARG, "cache is NULL");
     if (c->fmt == FTMOE_FMT_RAW) return fail(FTMOE_ERR_FORMAT, "a raw-format cache has no FFN");
     if (!c->ffn) return fail(FTMOE_ERR_INVALID_ARG, "cache created with max_pairs = 0");
@@ -546,6 +566,7 @@ int ftmoe_expert_ffn_hybrid(ftmoe_cache_t *c, const void *d_x_bf16, int32_t bs, 
 }
 
 int ftmoe_prefetch_layer(ftmoe_cache_t *c, int32_t layer, void *stream) {
+    NvtxRange nvtx_range("ftmoe_prefetch_layer");
     if (!c) return fail(FTMOE_ERR_INVALID_ARG, "cache is NULL");
     int rc = ensure_impl(c, layer, c->all_ids, 1, c->E, c->pf_slots, 0, -1, 0.f, nullptr, stream);
     if (rc) return rc;
@@ -556,6 +577,7 @@ int ftmoe_prefill_layers(ftmoe_cache_t *c, int32_t num_layers, const int32_t *h_
                          const int32_t *const *d_topk_ids, int32_t bs, int32_t topk, const void *const *d_x_bf16,
                          const float *const *d_weights, void *const *d_y_bf16, void *compute_stream,
                          void *copy_stream) {
+    NvtxRange nvtx_range("ftmoe_prefill_layers");
     if (!c) return fail(FTMOE_ERR_INVALID_ARG, "cache is NULL");
     if (!c->ffn || c->fmt == FTMOE_FMT_RAW) return fail(FTMOE_ERR_INVALID_ARG, "the cache has no FFN");
     if (num_layers <= 0) return FTMOE_OK;

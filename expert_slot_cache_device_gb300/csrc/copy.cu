@@ -62,6 +62,7 @@ __global__ void __launch_bounds__(kCopyThreads) copy_missing_kernel(CopyParams p
     asm volatile("griddepcontrol.launch_dependents;" :::);
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int m = *p.num_miss;
+    if (!FTMOE_DCHECK(m >= 0 && m <= p.maxm, p.status)) return;
     const int64_t tpe = p.tile0[p.nb];  // tiles per expert over all banks
     const int64_t total = (int64_t)m * tpe;
     for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
@@ -74,6 +75,8 @@ __global__ void __launch_bounds__(kCopyThreads) copy_missing_kernel(CopyParams p
         const int64_t n = bb - off < kCopyTile ? bb - off : kCopyTile;
         const int64_t e = p.miss_ids[j] % p.E;
         const int64_t s = p.miss_slots[j];
+        if (!FTMOE_DCHECK(s >= 0 && s < p.S && p.miss_ids[j] >= 0 && p.miss_ids[j] < (int64_t)p.L * p.E, p.status))
+            continue;
         copy_tile<VEC>(p.dst[b] + s * bb + off, p.src[b] + e * bb + off, n);
     }
 }

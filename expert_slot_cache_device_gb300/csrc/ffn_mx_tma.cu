@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                 while (u + 1 < nu && p.s.upoff[u + 1] <= pi) u++;
                 cur_pi = pi;
                 slot = p.s.uslot[u];
+                FTMOE_DCHECK(slot >= 0 && slot < p.S, p.status);
                 slot = slot < 0 ? 0 : (slot >= p.S ? p.S - 1 : slot);
                 const int pbase = (pi - p.s.upoff[u]) * kMxTokMax;
                 cnt = p.s.ucnt[u] - pbase < kMxTokMax ? p.s.ucnt[u] - pbase : kMxTokMax;

@@ -296,6 +296,7 @@ __device__ __forceinline__ void rows_mma_body(const FfnParams &p, const F8Cfg &c
                 while (u + 1 < nu && p.s.upoff[u + 1] <= pi) u++;
                 cur_pi = pi;
                 slot = p.s.uslot[u];
+                FTMOE_DCHECK(slot >= 0 && slot < p.S, p.status);
                 slot = slot < 0 ? 0 : (slot >= p.S ? p.S - 1 : slot);
                 const int pbase = (pi - p.s.upoff[u]) * kFTok;
                 cnt = p.s.ucnt[u] - pbase < kFTok ? p.s.ucnt[u] - pbase : kFTok;

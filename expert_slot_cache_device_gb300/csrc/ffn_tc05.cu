@@ -122,6 +122,7 @@ __device__ __forceinline__ ItemInfo item_info(const FfnParams &p, int nu, int ti
     while (u + 1 < nu && p.s.upoff[u + 1] <= pi) u++;  // increasing passes: walk forward
     ItemInfo f;
     f.slot = p.s.uslot[u];
+    FTMOE_DCHECK(f.slot >= 0 && f.slot < p.S, p.status);
     f.slot = f.slot < 0 ? 0 : (f.slot >= p.S ? p.S - 1 : f.slot);
     const int pbase = (pi - p.s.upoff[u]) * kTN;
     f.cnt = p.s.ucnt[u] - pbase < kTN ? p.s.ucnt[u] - pbase : kTN;

@@ -404,7 +404,8 @@ __global__ void __launch_bounds__(kTmaThreads<FMT, PHASE>, 1) ffn_rows_tma_kerne
             const int pi = it / c.tiles, tile = it - pi * c.tiles;
             while (u + 1 < nu && p.s.upoff[u + 1] <= pi) u++;  // increasing passes: walk forward
             int slot = p.s.uslot[u];
-            slot = slot < 0 ? 0 : (slot >= p.S ? p.S - 1 : slot);
+            FTMOE_DCHECK(slot >= 0 && slot < p.S, p.status);
+                slot = slot < 0 ? 0 : (slot >= p.S ? p.S - 1 : slot);
             const int pbase = (pi - p.s.upoff[u]) * kPassTokens;
             const int pcnt = p.s.ucnt[u] - pbase < kPassTokens ? p.s.ucnt[u] - pbase : kPassTokens;
             const int off = p.s.uoff[u] + pbase, cnt = pcnt;

@@ -8,6 +8,15 @@
 
 namespace ftmoe {
 
+// Bounds-checked debug builds (compiled with -DFTMOE_CHECK, see build.build(check=True)) test
+// device-side indices before they are used: a failed test records FTMOE_ERR_STATE in the
+// status word and the access is skipped; nothing traps. Release builds compile the tests out.
+#ifdef FTMOE_CHECK
+#define FTMOE_DCHECK(cond, status) ((cond) || (atomicCAS((status), 0, FTMOE_ERR_STATE), false))
+#else
+#define FTMOE_DCHECK(cond, status) true
+#endif
+
 // ---------------------------------------------------------------- cache tables
 // Device-resident state of one cache; all pointers point into the caller's
 // workspace.
@@ -55,6 +64,8 @@ struct CopyParams {
     const int32_t *miss_slots;
     const int32_t *num_miss;
     int32_t nb, E;
+    int32_t L, S, maxm;  // bounds of the miss list (checked in -DFTMOE_CHECK builds)
+    int32_t *status;
 };
 cudaError_t launch_copy(const CopyParams &p, bool vec16, int grid, cudaStream_t st);
 cudaError_t launch_linear_copy(unsigned char *dst, const unsigned char *src, int64_t bytes, bool vec16,

@@ -12,7 +12,8 @@ import os
 from typing import Sequence
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libftmoe.so")
+# FTMOE_CHECKED=1 loads the bounds-checked debug build (build.build(check=True)) instead
+LIB_PATH = os.path.join(_HERE, "libftmoe_check.so" if os.environ.get("FTMOE_CHECKED") == "1" else "libftmoe.so")
 
 OK = 0
 ERR_INVALID_ARG, ERR_CAPACITY, ERR_ID_RANGE, ERR_CUDA, ERR_FORMAT, ERR_STATE = -1, -2, -3, -4, -5, -6

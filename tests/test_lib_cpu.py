@@ -106,3 +106,15 @@ def test_binding_constants_match_the_header():
         names = [n for n in defs if n.startswith(family)]
         assert names and all(hasattr(F, n) for n in names), family
     assert checked >= 30
+
+
+def test_bounds_checked_build_exports_every_symbol():
+    """The debug build with device-side index checks (-DFTMOE_CHECK) compiles and exports the
+    same entry points as the release library."""
+    import ctypes
+
+    path = B.build(check=True)
+    assert path.endswith("libftmoe_check.so")
+    lib_check = ctypes.CDLL(path)
+    for n in declared_functions():
+        assert hasattr(lib_check, n), n
