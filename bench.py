@@ -638,19 +638,36 @@ def graph_probe(cfg, cache, torch, F, wl, bs=1, calls=None, reps=20):
             out.append(a.elapsed_time(b) * 1e3 / calls)
         return statistics.median(out)
 
+    def run_ensure_copy():
+        for _ in range(calls):
+            cache.ensure(0, d_ids, d_slots, stream=st)
+            cache.copy_missing(stream=st)
+
+    def run_ffn():
+        for _ in range(calls):
+            cache.ffn(d_x, d_slots, d_w, d_y, stream=st)
+
+    def replayed(fn):
+        g = torch.cuda.CUDAGraph()
+        st.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(g, stream=st, capture_error_mode="thread_local"):
+            fn()
+        t = timed(g.replay)
+        del g
+        return t
+
     cache.set_state(r.owner, r.stamp, r.clock, stream=st)
     run()
     torch.cuda.synchronize()
     eager = timed(run)
-    g = torch.cuda.CUDAGraph()
-    st.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.graph(g, stream=st, capture_error_mode="thread_local"):
-        run()
-    replay = timed(g.replay)
+    replay = replayed(run)
+    # the parts of a call on their own (graph replays): ensure + copy (nothing to copy), FFN
+    ensure_copy = replayed(run_ensure_copy)
+    ffn_only = replayed(run_ffn)
     assert cache.status() == F.OK
-    del g
     return {"bs": bs, "calls": calls, "misses_per_call": 0, "eager_us_per_call": eager,
-            "graph_us_per_call": replay, "speedup": eager / replay if replay > 0 else None}
+            "graph_us_per_call": replay, "speedup": eager / replay if replay > 0 else None,
+            "graph_ensure_copy_us_per_call": ensure_copy, "graph_ffn_us_per_call": ffn_only}
 
 
 def prefill_probe(cfg, cache, torch, F):

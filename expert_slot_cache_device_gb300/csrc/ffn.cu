@@ -72,6 +72,64 @@ __device__ int block_scan_sum(int v, int *warp_tot, int *total) {
     return r;
 }
 
+// The routing tables of a call of at most 32 routed pairs, by warp 0 of the routing CTA with
+// register shuffles (no block barriers): lane q holds the key slot * 32 + q of pair q (slot -1,
+// computed elsewhere, and lanes past P sort last), a bitonic network sorts the keys ascending,
+// runs of equal slots become the distinct slots (ascending, their pairs grouped), and a warp
+// scan of each slot's pass count gives its first pass. Same tables as the block path below.
+__device__ void route_warp(const FfnParams &p) {
+    const int lane = threadIdx.x & 31;
+    const int s0 = lane < p.P ? p.slots[lane] : -1;
+    const bool bad = s0 != -1 && (unsigned)s0 >= (unsigned)p.S;
+    if (__any_sync(0xffffffffu, bad)) {
+        if (lane == 0) {
+            *p.s.n_unique = -1;
+            atomicCAS(p.status, 0, FTMOE_ERR_INVALID_ARG);
+        }
+        return;
+    }
+    if (p.s.hmax && lane < p.P) p.s.hmax[lane] = 0u;
+    constexpr int kNone = 0x7fffffff;
+    int key = s0 >= 0 ? (s0 << 5) | lane : kNone;
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const int other = __shfl_xor_sync(0xffffffffu, key, j);
+            const bool up = (lane & k) == 0, low = (lane & j) == 0;
+            key = (low == up) ? min(key, other) : max(key, other);
+        }
+    const bool valid = key != kNone;
+    const int slot = key >> 5, q = key & 31;
+    const int prev = __shfl_up_sync(0xffffffffu, slot, 1);
+    const bool start = valid && (lane == 0 || prev != slot);
+    const unsigned starts = __ballot_sync(0xffffffffu, start);
+    const int nvalid = __popc(__ballot_sync(0xffffffffu, valid));
+    const unsigned below = (1u << lane) - 1u;
+    const unsigned after = starts & ~(below | (1u << lane));
+    const int run = start ? ((after ? __ffs(after) - 1 : nvalid) - lane) : 0;
+    const int np = start ? (run + p.pass_tokens - 1) / p.pass_tokens : 0;
+    int incl = np;  // inclusive scan of the pass counts over the lanes
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += v;
+    }
+    if (valid) p.s.upairs[lane] = q;
+    if (start) {
+        const int u = __popc(starts & below);
+        p.s.uslot[u] = slot;
+        p.s.ucnt[u] = run;
+        p.s.uoff[u] = lane;
+        if (p.s.upoff) p.s.upoff[u] = incl - np;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (lane == 0) {
+        if (p.s.n_passes) *p.s.n_passes = total;
+        *p.s.n_unique = __popc(starts);
+    }
+}
+
 // CTA 0 groups the routed pairs by slot (and clears the per-pair max |h| words). CTAs
 // 1..bs (launched only when the fp4 activation copy is wanted) convert token
 // t = blockIdx.x - 1 to f16 with a power-of-two scale 2^-e chosen so that
@@ -115,6 +173,10 @@ __global__ void __launch_bounds__(1024) ffn_route_kernel(FfnParams p) {
             dst[p.x16_swz == 1 ? swz_x16(k) : (p.x16_swz == 2 ? swz_q4x16(k) : k)] =
                 __half_as_ushort(__float2half_rn(__uint_as_float((uint32_t)xr[k] << 16) * sc));
         if (tid == 0) p.s.xexp[t] = e;
+        return;
+    }
+    if (p.P <= 32) {  // one warp routes small calls (every decode step of one token)
+        if (tid < 32) route_warp(p);
         return;
     }
     if (tid == 0) s_bad = 0;
