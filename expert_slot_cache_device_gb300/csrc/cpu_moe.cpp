@@ -6,14 +6,22 @@
 // computes the resident and fetched ones (architecture deep-dive, section 五: the CPU
 // side runs a GEMV over the host expert banks). This is that executor for the bf16,
 // nvfp4 and transposed mxfp4 bank schemas, with fp32 accumulation, split over std::thread
-// workers (gate_up + SiLU * up for every CPU pair, then down); on the Grace host the inner
-// loops are NEON (bf16 rows 16 weights per step in four accumulators; e2m1 codes through a
-// table lookup of twice their values as int8, so the block scale takes the factor one half).
+// workers (gate_up + SiLU * up for every CPU pair, then down). On the Grace host the inner
+// loops use the BF16 extension's dot product (BFDOT: fp32 += two bf16 products per lane): bf16
+// weights and activations enter unchanged, e2m1 codes become their exact bf16 values by two
+// byte-table lookups, and the fp32 h rows of down enter as two bf16 vectors hi + lo (hi = h
+// rounded to bf16, lo = the remainder rounded), about 16 significant bits. Arm hosts without
+// it run NEON fp32 loops (bf16 rows 16 weights per step in four accumulators; e2m1 codes
+// through a table lookup of twice their values as int8, so the block scale takes the factor
+// one half); other hosts run the plain loops.
 #include <algorithm>
 #include <chrono>
 #include <cmath>
+#include <condition_variable>
 #include <cstdint>
 #include <cstring>
+#include <functional>
+#include <mutex>
 #include <thread>
 #include <vector>
 
@@ -23,7 +31,11 @@
 // widening shifts, table lookups, fp32 fused multiply-adds); other hosts run the plain loops.
 #if defined(__aarch64__) && defined(__ARM_NEON)
 #include <arm_neon.h>
+#include <sys/auxv.h>
 #define FTMOE_CPU_NEON 1
+#ifndef HWCAP2_BF16
+#define HWCAP2_BF16 (1UL << 14)  // Linux aarch64 hwcap bit of the BF16 extension
+#endif
 #else
 #define FTMOE_CPU_NEON 0
 #endif
@@ -55,11 +67,18 @@ float f16_to_f(uint16_t h) {
 struct Tables {
     float e2m1[16];
     float e4m3[256];
+    float e8m0[256];          // 2^(b - 127), as ldexp gives it (b = 255: infinity)
+    uint8_t e2m1_lo[16], e2m1_hi[16];  // low and high byte of each e2m1 value as bf16 (exact)
     Tables() {
+        for (int b = 0; b < 256; b++) e8m0[b] = std::ldexp(1.0f, b - 127);
         for (int c = 0; c < 16; c++) {
             const int mag = c & 7;
             const float v = mag < 2 ? 0.5f * mag : std::ldexp(1.0f + 0.5f * (mag & 1), (mag >> 1) - 1);
             e2m1[c] = (c & 8) ? -v : v;
+            uint32_t u;
+            std::memcpy(&u, &e2m1[c], sizeof u);  // two significant bits: the bf16 is the top half
+            e2m1_lo[c] = static_cast<uint8_t>(u >> 16);
+            e2m1_hi[c] = static_cast<uint8_t>(u >> 24);
         }
         for (int b = 0; b < 256; b++) {
             const int e = (b >> 3) & 15, m = b & 7;
@@ -77,6 +96,76 @@ const Tables &tables() {
 
 float silu(float z) { return z / (1.0f + std::exp(-z)); }
 
+// Persistent workers of parallel_for: started on first use (and grown on demand), then parked
+// on a condition variable between calls, so a call pays a wake-up instead of a thread start
+// per worker. One call runs at a time (calls from several host threads queue on the mutex).
+class WorkerPool {
+  public:
+    static WorkerPool &get() {
+        static WorkerPool pool;
+        return pool;
+    }
+    // fn(a, b) over [0, n) split into nt contiguous ranges; range 0 runs on the calling thread.
+    void run(int64_t n, int nt, const std::function<void(int64_t, int64_t)> &fn) {
+        std::lock_guard<std::mutex> call(call_mu_);
+        {
+            std::unique_lock<std::mutex> lk(mu_);
+            while (static_cast<int>(workers_.size()) < nt - 1) {
+                const int id = static_cast<int>(workers_.size()) + 1;
+                workers_.emplace_back([this, id] { loop(id); });
+            }
+            fn_ = &fn;
+            n_ = n;
+            nt_ = nt;
+            pending_ = nt - 1;
+            gen_++;
+        }
+        cv_.notify_all();
+        fn(0, n / nt);
+        std::unique_lock<std::mutex> lk(mu_);
+        done_cv_.wait(lk, [this] { return pending_ == 0; });
+        fn_ = nullptr;
+    }
+    ~WorkerPool() {
+        {
+            std::lock_guard<std::mutex> lk(mu_);
+            stop_ = true;
+        }
+        cv_.notify_all();
+        for (auto &t : workers_) t.join();
+    }
+
+  private:
+    void loop(int id) {
+        uint64_t seen = 0;
+        for (;;) {
+            const std::function<void(int64_t, int64_t)> *fn;
+            int64_t a, b;
+            {
+                std::unique_lock<std::mutex> lk(mu_);
+                cv_.wait(lk, [&] { return stop_ || gen_ != seen; });
+                if (stop_) return;
+                seen = gen_;
+                if (id >= nt_) continue;  // not part of this call
+                fn = fn_;
+                a = n_ * id / nt_;
+                b = n_ * (id + 1) / nt_;
+            }
+            (*fn)(a, b);
+            std::lock_guard<std::mutex> lk(mu_);
+            if (--pending_ == 0) done_cv_.notify_one();
+        }
+    }
+    std::mutex call_mu_, mu_;
+    std::condition_variable cv_, done_cv_;
+    std::vector<std::thread> workers_;
+    const std::function<void(int64_t, int64_t)> *fn_ = nullptr;
+    int64_t n_ = 0;
+    int nt_ = 0, pending_ = 0;
+    uint64_t gen_ = 0;
+    bool stop_ = false;
+};
+
 template <typename F>
 void parallel_for(int64_t n, int threads, F &&fn) {
     if (n <= 0) return;
@@ -85,13 +174,8 @@ void parallel_for(int64_t n, int threads, F &&fn) {
         fn(0, n);
         return;
     }
-    std::vector<std::thread> pool;
-    pool.reserve(nt);
-    for (int i = 0; i < nt; i++) {
-        const int64_t a = n * i / nt, b = n * (i + 1) / nt;
-        pool.emplace_back([&fn, a, b] { fn(a, b); });
-    }
-    for (auto &th : pool) th.join();
+    const std::function<void(int64_t, int64_t)> f = fn;
+    WorkerPool::get().run(n, nt, f);
 }
 
 #if FTMOE_CPU_NEON
@@ -146,6 +230,182 @@ inline void cols16_e2m1_neon(const uint8_t *codes, float x0, float x1, int8x16_t
                          vcvtq_f32_s32(vmovl_s16(vget_low_s16(h1))), x1);
     acc[3] = vfmaq_n_f32(vfmaq_n_f32(acc[3], vcvtq_f32_s32(vmovl_high_s16(l1)), x0),
                          vcvtq_f32_s32(vmovl_high_s16(h1)), x1);
+}
+
+bool host_has_bf16() {
+    static const bool has = (getauxval(AT_HWCAP2) & HWCAP2_BF16) != 0;
+    return has;
+}
+
+#define FTMOE_BF16_FN __attribute__((target("+bf16")))
+
+FTMOE_BF16_FN inline bfloat16x8_t ld_bf16(const uint16_t *p) {
+    return vld1q_bf16(reinterpret_cast<const bfloat16_t *>(p));
+}
+
+// bf16 row . (vh + vl), vl only when LO: 32 weights per step, four accumulators (K % 8 == 0).
+template <bool LO>
+FTMOE_BF16_FN float dot_bf16_bfdot(const uint16_t *w, const uint16_t *vh, const uint16_t *vl, int64_t K) {
+    float32x4_t a0 = vdupq_n_f32(0.f), a1 = a0, a2 = a0, a3 = a0;
+    int64_t k = 0;
+    for (; k + 32 <= K; k += 32) {
+        const bfloat16x8_t w0 = ld_bf16(w + k), w1 = ld_bf16(w + k + 8), w2 = ld_bf16(w + k + 16),
+                           w3 = ld_bf16(w + k + 24);
+        a0 = vbfdotq_f32(a0, w0, ld_bf16(vh + k));
+        a1 = vbfdotq_f32(a1, w1, ld_bf16(vh + k + 8));
+        a2 = vbfdotq_f32(a2, w2, ld_bf16(vh + k + 16));
+        a3 = vbfdotq_f32(a3, w3, ld_bf16(vh + k + 24));
+        if (LO) {
+            a0 = vbfdotq_f32(a0, w0, ld_bf16(vl + k));
+            a1 = vbfdotq_f32(a1, w1, ld_bf16(vl + k + 8));
+            a2 = vbfdotq_f32(a2, w2, ld_bf16(vl + k + 16));
+            a3 = vbfdotq_f32(a3, w3, ld_bf16(vl + k + 24));
+        }
+    }
+    for (; k + 8 <= K; k += 8) {
+        const bfloat16x8_t w0 = ld_bf16(w + k);
+        a0 = vbfdotq_f32(a0, w0, ld_bf16(vh + k));
+        if (LO) a1 = vbfdotq_f32(a1, w0, ld_bf16(vl + k));
+    }
+    return vaddvq_f32(vaddq_f32(vaddq_f32(a0, a1), vaddq_f32(a2, a3)));
+}
+
+// The sixteen e2m1 codes of one nvfp4 scale block (eight bytes, low nibble = even k) as two
+// bf16x8 vectors in k order: nibbles interleaved into k order, then the low and high bytes of
+// their bf16 values looked up and interleaved.
+FTMOE_BF16_FN inline void e2m1x16_bf16(const uint8_t *codes, uint8x16_t tlo, uint8x16_t thi, bfloat16x8_t &w0,
+                                       bfloat16x8_t &w1) {
+    const uint8x8_t c = vld1_u8(codes);
+    const uint8x8_t ev = vand_u8(c, vdup_n_u8(15)), od = vshr_n_u8(c, 4);
+    const uint8x16_t idx = vcombine_u8(vzip1_u8(ev, od), vzip2_u8(ev, od));
+    const uint8x16_t lo = vqtbl1q_u8(tlo, idx), hi = vqtbl1q_u8(thi, idx);
+    w0 = vreinterpretq_bf16_u8(vzip1q_u8(lo, hi));
+    w1 = vreinterpretq_bf16_u8(vzip2q_u8(lo, hi));
+}
+
+// nvfp4 row . (vh + vl): per 16-element block two BFDOTs into a fresh partial (and two more
+// for vl, a second chain), scaled by the block's e4m3 scale into one of four accumulators; the
+// row's f16 global last.
+template <bool LO>
+FTMOE_BF16_FN float row_nvfp4_bfdot(const uint8_t *codes, const uint8_t *sc, float g, const uint16_t *vh,
+                                    const uint16_t *vl, int64_t K, const float *e4m3, uint8x16_t tlo,
+                                    uint8x16_t thi) {
+    float32x4_t acc[4] = {vdupq_n_f32(0.f), vdupq_n_f32(0.f), vdupq_n_f32(0.f), vdupq_n_f32(0.f)};
+    const int64_t nb = K / 16;
+    for (int64_t blk = 0; blk < nb; blk++) {
+        bfloat16x8_t w0, w1;
+        e2m1x16_bf16(codes + blk * 8, tlo, thi, w0, w1);
+        const float s = e4m3[sc[blk]];
+        float32x4_t p = vbfdotq_f32(vdupq_n_f32(0.f), w0, ld_bf16(vh + blk * 16));
+        p = vbfdotq_f32(p, w1, ld_bf16(vh + blk * 16 + 8));
+        acc[blk & 1] = vfmaq_n_f32(acc[blk & 1], p, s);
+        if (LO) {
+            float32x4_t q = vbfdotq_f32(vdupq_n_f32(0.f), w0, ld_bf16(vl + blk * 16));
+            q = vbfdotq_f32(q, w1, ld_bf16(vl + blk * 16 + 8));
+            acc[2 + (blk & 1)] = vfmaq_n_f32(acc[2 + (blk & 1)], q, s);
+        }
+    }
+    return vaddvq_f32(vaddq_f32(vaddq_f32(acc[0], acc[1]), vaddq_f32(acc[2], acc[3]))) * g;
+}
+
+// The gate and the up row of one nvfp4 neuron against the same bf16 activations (each
+// activation vector loaded once for both rows): out[0] = gate . v, out[1] = up . v.
+FTMOE_BF16_FN void row2_nvfp4_bfdot(const uint8_t *cg, const uint8_t *sg, float gg, const uint8_t *cu,
+                                    const uint8_t *su, float gu, const uint16_t *vh, int64_t K, const float *e4m3,
+                                    uint8x16_t tlo, uint8x16_t thi, float (&out)[2]) {
+    float32x4_t ag[2] = {vdupq_n_f32(0.f), vdupq_n_f32(0.f)}, au[2] = {vdupq_n_f32(0.f), vdupq_n_f32(0.f)};
+    const int64_t nb = K / 16;
+    for (int64_t blk = 0; blk < nb; blk++) {
+        bfloat16x8_t g0, g1, u0, u1;
+        e2m1x16_bf16(cg + blk * 8, tlo, thi, g0, g1);
+        e2m1x16_bf16(cu + blk * 8, tlo, thi, u0, u1);
+        const bfloat16x8_t x0 = ld_bf16(vh + blk * 16), x1 = ld_bf16(vh + blk * 16 + 8);
+        const float32x4_t pg = vbfdotq_f32(vbfdotq_f32(vdupq_n_f32(0.f), g0, x0), g1, x1);
+        const float32x4_t pu = vbfdotq_f32(vbfdotq_f32(vdupq_n_f32(0.f), u0, x0), u1, x1);
+        ag[blk & 1] = vfmaq_n_f32(ag[blk & 1], pg, e4m3[sg[blk]]);
+        au[blk & 1] = vfmaq_n_f32(au[blk & 1], pu, e4m3[su[blk]]);
+    }
+    out[0] = vaddvq_f32(vaddq_f32(ag[0], ag[1])) * gg;
+    out[1] = vaddvq_f32(vaddq_f32(au[0], au[1])) * gu;
+}
+
+// One k-pair row of 16 columns of a transposed mxfp4 matrix (16 code bytes, low nibble = even
+// k) against the k pair (vh[0], vh[1]) (and (vl[0], vl[1]) when LO), into the hi / lo
+// accumulators of the four 4-column groups.
+template <bool LO>
+FTMOE_BF16_FN inline void mx_row16_bfdot(const uint8_t *codes, const uint16_t *vh, const uint16_t *vl, uint8x16_t tlo,
+                                         uint8x16_t thi, float32x4_t (&ah)[4], float32x4_t (&al)[4]) {
+    const uint8x16_t c = vld1q_u8(codes);
+    const uint8x16_t ev = vandq_u8(c, vdupq_n_u8(15)), od = vshrq_n_u8(c, 4);
+    const uint8x16_t z0 = vzip1q_u8(ev, od), z1 = vzip2q_u8(ev, od);
+    const uint8x16_t l0 = vqtbl1q_u8(tlo, z0), h0 = vqtbl1q_u8(thi, z0);
+    const uint8x16_t l1 = vqtbl1q_u8(tlo, z1), h1 = vqtbl1q_u8(thi, z1);
+    const bfloat16x8_t w[4] = {vreinterpretq_bf16_u8(vzip1q_u8(l0, h0)), vreinterpretq_bf16_u8(vzip2q_u8(l0, h0)),
+                               vreinterpretq_bf16_u8(vzip1q_u8(l1, h1)), vreinterpretq_bf16_u8(vzip2q_u8(l1, h1))};
+    uint32_t xp;
+    std::memcpy(&xp, vh, sizeof xp);  // (v[2i], v[2i+1]), v[2i] in the low half
+    const bfloat16x8_t xh = vreinterpretq_bf16_u32(vdupq_n_u32(xp));
+    for (int q = 0; q < 4; q++) ah[q] = vbfdotq_f32(ah[q], w[q], xh);
+    if (LO) {
+        std::memcpy(&xp, vl, sizeof xp);
+        const bfloat16x8_t xl = vreinterpretq_bf16_u32(vdupq_n_u32(xp));
+        for (int q = 0; q < 4; q++) al[q] = vbfdotq_f32(al[q], w[q], xl);
+    }
+}
+
+// Columns [n0, n1) of a transposed mxfp4 matrix against vh + vl (see cols_dot): per k-pair row
+// and 16 columns, the 16 code bytes become four bf16x8 vectors (4 columns x (even k, odd k))
+// and meet the k pair of v broadcast to every lane.
+template <bool LO>
+FTMOE_BF16_FN void cols_mx_bfdot(const uint8_t *const *b, int which, int64_t N, int64_t K, const uint16_t *vh,
+                                 const uint16_t *vl, int64_t n0, int64_t n1, float *out) {
+    const Tables &T = tables();
+    const uint8x16_t tlo = vld1q_u8(T.e2m1_lo), thi = vld1q_u8(T.e2m1_hi);
+    const uint8_t *blocks = b[3 * which], *scales = b[3 * which + 1];
+    const uint16_t *bias = reinterpret_cast<const uint16_t *>(b[3 * which + 2]);
+    for (int64_t n = n0; n < n1; n++) out[n - n0] = 0.f;
+    for (int64_t blk = 0; blk < K / 32; blk++) {
+        const uint8_t *srow = scales + blk * N;
+        int64_t n = n0;
+        for (; n + 16 <= n1; n += 16) {
+            // accumulators per (row parity, hi / lo, 4-column group): short dependency chains
+            float32x4_t ah0[4], ah1[4], al0[4], al1[4];
+            for (int q = 0; q < 4; q++) ah0[q] = ah1[q] = al0[q] = al1[q] = vdupq_n_f32(0.f);
+            for (int64_t i = blk * 16; i < blk * 16 + 16; i += 2) {
+                mx_row16_bfdot<LO>(blocks + i * N + n, vh + 2 * i, LO ? vl + 2 * i : nullptr, tlo, thi, ah0, al0);
+                mx_row16_bfdot<LO>(blocks + (i + 1) * N + n, vh + 2 * i + 2, LO ? vl + 2 * i + 2 : nullptr, tlo, thi,
+                                   ah1, al1);
+            }
+            float s[16];
+            for (int j = 0; j < 16; j++) s[j] = T.e8m0[srow[n + j]];
+            for (int q = 0; q < 4; q++) {
+                float32x4_t a = vaddq_f32(ah0[q], ah1[q]);
+                if (LO) a = vaddq_f32(a, vaddq_f32(al0[q], al1[q]));
+                vst1q_f32(out + (n - n0) + 4 * q,
+                          vfmaq_f32(vld1q_f32(out + (n - n0) + 4 * q), a, vld1q_f32(s + 4 * q)));
+            }
+        }
+        for (; n < n1; n++) {  // ragged columns
+            float part = 0.f;
+            for (int64_t i = blk * 16; i < blk * 16 + 16; i++) {
+                const uint8_t c = blocks[i * N + n];
+                const float x0 = bf16_to_f(vh[2 * i]) + (LO ? bf16_to_f(vl[2 * i]) : 0.f);
+                const float x1 = bf16_to_f(vh[2 * i + 1]) + (LO ? bf16_to_f(vl[2 * i + 1]) : 0.f);
+                part += T.e2m1[c & 15] * x0 + T.e2m1[c >> 4] * x1;
+            }
+            out[n - n0] += part * T.e8m0[srow[n]];
+        }
+    }
+    for (int64_t n = n0; n < n1; n++) out[n - n0] += bf16_to_f(bias[n]);
+}
+#endif
+
+#if FTMOE_CPU_NEON
+// fp32 -> bf16 bits, rounded to nearest even (finite inputs).
+uint16_t f_to_bf16(float f) {
+    uint32_t u;
+    std::memcpy(&u, &f, sizeof u);
+    return static_cast<uint16_t>((u + 0x7fffu + ((u >> 16) & 1u)) >> 16);
 }
 #endif
 
@@ -233,10 +493,90 @@ void cols_dot(const uint8_t *const *b, int which, int64_t N, int64_t K, const fl
         }
 #endif
         const uint8_t *srow = scales + blk * N;
-        for (int64_t n = n0; n < n1; n++) out[n - n0] += part[n - n0] * std::ldexp(1.0f, static_cast<int>(srow[n]) - 127);
+        for (int64_t n = n0; n < n1; n++) out[n - n0] += part[n - n0] * T.e8m0[srow[n]];
     }
     for (int64_t n = n0; n < n1; n++) out[n - n0] += bf16_to_f(bias[n]);
 }
+
+#if FTMOE_CPU_NEON
+// Row n of a row-major expert matrix (bf16 or nvfp4) . (vh + vl) on the BF16 dot product.
+template <bool LO>
+float row_dot_bfdot(int fmt, const uint8_t *const *b, int which, int64_t n, int64_t K, const uint16_t *vh,
+                    const uint16_t *vl) {
+    if (fmt == FTMOE_FMT_BF16)
+        return dot_bf16_bfdot<LO>(reinterpret_cast<const uint16_t *>(b[which]) + n * K, vh, vl, K);
+    const Tables &T = tables();
+    const uint16_t g = reinterpret_cast<const uint16_t *>(b[3 * which + 2])[n];
+    return row_nvfp4_bfdot<LO>(b[3 * which] + n * (K / 2), b[3 * which + 1] + n * (K / 16), f16_to_f(g), vh, vl, K,
+                               T.e4m3, vld1q_u8(T.e2m1_lo), vld1q_u8(T.e2m1_hi));
+}
+
+// gate_up + SiLU * up, then down, of every CPU pair on the BF16 dot product: the activations
+// enter as they are (bf16), the h rows as hi + lo bf16 vectors. Same work split as the fp32
+// paths of ftmoe_cpu_expert_ffn.
+void expert_ffn_bfdot(int format, int64_t H, int64_t I, int topk, const std::vector<int> &pairs,
+                      const std::vector<const uint8_t *> &eb, int nb, const uint16_t *h_x, std::vector<float> &hs,
+                      std::vector<float> &os, int threads) {
+    const int64_t np = static_cast<int64_t>(pairs.size());
+    auto xrow = [&](int64_t i) { return h_x + (int64_t)(pairs[static_cast<size_t>(i)] / topk) * H; };
+    const int64_t chunk = 64;
+    if (format == FTMOE_FMT_MXFP4) {
+        const int64_t nch = (I + chunk - 1) / chunk;
+        parallel_for(np * nch, threads, [&](int64_t a, int64_t b) {
+            float g[chunk], u[chunk];
+            for (int64_t w = a; w < b; w++) {
+                const int64_t i = w / nch, c0 = (w % nch) * chunk, c1 = std::min<int64_t>(I, c0 + chunk);
+                const uint8_t *const *bk = &eb[static_cast<size_t>(i * nb)];
+                cols_mx_bfdot<false>(bk, 0, 2 * I, H, xrow(i), nullptr, c0, c1, g);
+                cols_mx_bfdot<false>(bk, 0, 2 * I, H, xrow(i), nullptr, I + c0, I + c1, u);
+                for (int64_t n = c0; n < c1; n++) hs[i * I + n] = silu(g[n - c0]) * u[n - c0];
+            }
+        });
+    } else {
+        const Tables &T = tables();
+        parallel_for(np * I, threads, [&](int64_t a, int64_t b) {
+            for (int64_t w = a; w < b; w++) {
+                const int64_t i = w / I, n = w % I;
+                const uint8_t *const *bk = &eb[static_cast<size_t>(i * nb)];
+                float gu[2];
+                if (format == FTMOE_FMT_BF16) {
+                    gu[0] = row_dot_bfdot<false>(format, bk, 0, n, H, xrow(i), nullptr);
+                    gu[1] = row_dot_bfdot<false>(format, bk, 0, I + n, H, xrow(i), nullptr);
+                } else {
+                    const uint16_t *gl = reinterpret_cast<const uint16_t *>(bk[2]);
+                    row2_nvfp4_bfdot(bk[0] + n * (H / 2), bk[1] + n * (H / 16), f16_to_f(gl[n]),
+                                     bk[0] + (I + n) * (H / 2), bk[1] + (I + n) * (H / 16), f16_to_f(gl[I + n]),
+                                     xrow(i), H, T.e4m3, vld1q_u8(T.e2m1_lo), vld1q_u8(T.e2m1_hi), gu);
+                }
+                hs[i * I + n] = silu(gu[0]) * gu[1];
+            }
+        });
+    }
+    std::vector<uint16_t> hh(static_cast<size_t>(np * I)), hl(static_cast<size_t>(np * I));
+    for (size_t k = 0; k < hh.size(); k++) {
+        hh[k] = f_to_bf16(hs[k]);
+        hl[k] = f_to_bf16(hs[k] - bf16_to_f(hh[k]));
+    }
+    if (format == FTMOE_FMT_MXFP4) {
+        const int64_t nchd = (H + chunk - 1) / chunk;
+        parallel_for(np * nchd, threads, [&](int64_t a, int64_t b) {
+            for (int64_t w = a; w < b; w++) {
+                const int64_t i = w / nchd, c0 = (w % nchd) * chunk, c1 = std::min<int64_t>(H, c0 + chunk);
+                cols_mx_bfdot<true>(&eb[static_cast<size_t>(i * nb)], 1, H, I, &hh[i * I], &hl[i * I], c0, c1,
+                                    &os[i * H + c0]);
+            }
+        });
+    } else {
+        parallel_for(np * H, threads, [&](int64_t a, int64_t b) {
+            for (int64_t w = a; w < b; w++) {
+                const int64_t i = w / H, n = w % H;
+                os[i * H + n] = row_dot_bfdot<true>(format, &eb[static_cast<size_t>(i * nb)], 1, n, I, &hh[i * I],
+                                                    &hl[i * I]);
+            }
+        });
+    }
+}
+#endif
 
 }  // namespace
 
@@ -268,13 +608,21 @@ extern "C" int ftmoe_cpu_expert_ffn(int32_t format, int32_t H, int32_t I, int32_
         for (int b = 0; b < nb; b++)
             eb[i * nb + b] = static_cast<const uint8_t *>(h_layer_banks[b]) + (int64_t)e * bank_bytes[b];
     }
-    std::vector<float> xs(static_cast<size_t>(np * H)), hs(static_cast<size_t>(np * I)),
-        os(static_cast<size_t>(np * H));
-    for (int64_t i = 0; i < np; i++) {
+    std::vector<float> hs(static_cast<size_t>(np * I)), os(static_cast<size_t>(np * H));
+#if FTMOE_CPU_NEON
+    const bool bfdot = host_has_bf16();
+    if (bfdot) expert_ffn_bfdot(format, H, I, topk, pairs, eb, nb, h_x, hs, os, threads);
+#else
+    const bool bfdot = false;
+#endif
+    std::vector<float> xs(bfdot ? 0 : static_cast<size_t>(np * H));
+    for (int64_t i = 0; i < np && !bfdot; i++) {
         const int64_t t = pairs[i] / topk;
         for (int64_t k = 0; k < H; k++) xs[i * H + k] = bf16_to_f(h_x[t * H + k]);
     }
-    if (format == FTMOE_FMT_MXFP4) {
+    if (bfdot) {
+        // computed above
+    } else if (format == FTMOE_FMT_MXFP4) {
         // gate_up: columns split over the workers, in chunks of 64 columns per pair
         const int64_t chunk = 64, nch = (I + chunk - 1) / chunk;
         parallel_for(np * nch, threads, [&](int64_t a, int64_t b) {

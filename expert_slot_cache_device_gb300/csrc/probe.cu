@@ -84,13 +84,15 @@ int ftmoe_measure_cpu_moe(int32_t format, int32_t H, int32_t I, int32_t E, const
     const int nb = format == FTMOE_FMT_BF16 ? 2 : 6;
     int64_t per_expert = 0;
     for (int b = 0; b < nb; b++) per_expert += bank_bytes[b];
-    // one token per expert, each routed to a different expert, all computed on the CPU
+    // one token per expert, each routed to a different expert, all computed on the CPU; each
+    // repetition takes the next `experts` experts of the layer (so a repetition does not find
+    // the previous one's weights in the host caches while the layer has enough experts)
     std::vector<int32_t> ids(experts), slots(experts, -1);
-    for (int t = 0; t < experts; t++) ids[t] = t % E;
     std::vector<uint16_t> x((size_t)experts * H, 0x3f80u);  // bf16 1.0
     std::vector<float> w(experts, 1.f), y((size_t)experts * H);
     double best = 1e30;
     for (int r = 0; r < reps; r++) {
+        for (int t = 0; t < experts; t++) ids[t] = (int32_t)(((int64_t)r * experts + t) % E);
         const auto t0 = std::chrono::steady_clock::now();
         int rc = ftmoe_cpu_expert_ffn(format, H, I, experts, 1, ids.data(), slots.data(), h_layer_banks, bank_bytes,
                                       x.data(), w.data(), y.data(), threads);

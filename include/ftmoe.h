@@ -307,8 +307,10 @@ int ftmoe_measure_link(const void *h_src, void *d_dst, size_t bytes, int32_t rep
 
 /* CPU MoE probe (benchmark guide, section 5.2: the bandwidth the CPU MoE kernel reaches on
  * the host's memory). Runs ftmoe_cpu_expert_ffn on `experts` tokens, each routed to a
- * different expert (t % E) of the layer banks h_layer_banks (host, schema order, bank_bytes
- * per expert), best of `reps`; *gbps = experts * bytes per expert / time. Host only.
+ * different expert of the layer banks h_layer_banks (host, schema order, bank_bytes per
+ * expert): repetition r routes token t to expert (r * experts + t) % E, so repetitions read
+ * different experts while E allows. Best of `reps`; *gbps = experts * bytes per expert /
+ * time. Host only.
  * FTMOE_ERR_FORMAT for formats without a CPU MoE path. */
 int ftmoe_measure_cpu_moe(int32_t format, int32_t H, int32_t I, int32_t E, const void *const *h_layer_banks,
                           const int64_t *bank_bytes, int32_t experts, int32_t threads, int32_t reps,
