@@ -3,7 +3,9 @@
 FreeToken benchmark guide, section 5.4: misses beyond the fetch cap get slot -1 and are
 computed by a CPU executor from the host banks. This runs on the CPU only: for every
 format, the executor's fp32 partial output over the -1 positions must match the fp64
-oracle FFN restricted to those positions.
+oracle FFN restricted to those positions. On an Arm host with the BF16 extension (the Grace
+host of the GPU machines) the executor's dot products run on BFDOT, elsewhere on fp32 loops;
+the same tolerance holds for both.
 """
 import numpy as np
 import pytest
@@ -80,3 +82,44 @@ def test_cpu_read_ceiling_probe(lib):
         with pytest.raises(F.FtmoeError) as e:
             F.ftmoe_measure_cpu_read(*args)
         assert e.value.code == F.ERR_INVALID_ARG
+
+
+def test_cpu_executor_concurrent_calls(lib):
+    """The executor's worker pool is shared: calls from several host threads at once (ctypes
+    releases the GIL), with different formats and worker counts, queue on it and each returns
+    exactly what the same call returns alone."""
+    import threading
+
+    jobs = []
+    for i, (fmt, geo) in enumerate(CASES * 2):
+        base = {"bf16": "c2", "nvfp4": "c3", "mxfp4": "c4"}[fmt]
+        cfg = wl.scaled(wl.CONFIGS[base], topk=2, L=2, S=4, **geo)
+        banks = wl.make_banks(cfg)
+        rng = np.random.default_rng(100 + i)
+        bs = 3
+        ids = np.stack([rng.choice(cfg.E, cfg.topk, replace=False) for _ in range(bs)]).astype(np.int32)
+        slots = np.full(ids.shape, -1, np.int32)
+        w = rng.random(ids.shape).astype(np.float32)
+        x = wl.f32_to_bf16_bits(rng.standard_normal((bs, cfg.H)).astype(np.float32))
+        jobs.append((fmt, cfg, banks, ids, slots, w, x, 1 + (3 * i) % 7))
+
+    def run(job, out):
+        fmt, cfg, banks, ids, slots, w, x, threads = job
+        F.ftmoe_cpu_expert_ffn(F.FORMATS[fmt], cfg.H, cfg.I, ids.shape[0], cfg.topk, ids.ctypes.data,
+                               slots.ctypes.data, [b.ctypes.data for b in banks], [b.shape[1] for b in banks],
+                               x.ctypes.data, w.ctypes.data, out.ctypes.data, threads)
+
+    alone = []
+    for job in jobs:
+        y = np.empty((job[3].shape[0], job[1].H), np.float32)
+        run(job, y)
+        alone.append(y)
+    for _ in range(3):
+        outs = [np.full_like(y, np.nan) for y in alone]
+        ts = [threading.Thread(target=run, args=(job, out)) for job, out in zip(jobs, outs)]
+        for t in ts:
+            t.start()
+        for t in ts:
+            t.join()
+        for y, y0 in zip(outs, alone):
+            assert np.array_equal(y, y0)
