@@ -10,7 +10,9 @@
 // loops use the BF16 extension's dot product (BFDOT: fp32 += two bf16 products per lane): bf16
 // weights and activations enter unchanged, e2m1 codes become their exact bf16 values by two
 // byte-table lookups, and the fp32 h rows of down enter as two bf16 vectors hi + lo (hi = h
-// rounded to bf16, lo = the remainder rounded), about 16 significant bits. Arm hosts without
+// rounded to bf16, lo = the remainder rounded), about 16 significant bits. nvfp4 rows read their
+// vectors in the even/odd order of each 16-element scale block, so that a code byte's two nibbles
+// need no interleaving. Arm hosts without
 // it run NEON fp32 loops (bf16 rows 16 weights per step in four accumulators; e2m1 codes
 // through a table lookup of twice their values as int8, so the block scale takes the factor
 // one half); other hosts run the plain loops.
@@ -270,60 +272,73 @@ FTMOE_BF16_FN float dot_bf16_bfdot(const uint16_t *w, const uint16_t *vh, const 
     return vaddvq_f32(vaddq_f32(vaddq_f32(a0, a1), vaddq_f32(a2, a3)));
 }
 
-// The sixteen e2m1 codes of one nvfp4 scale block (eight bytes, low nibble = even k) as two
-// bf16x8 vectors in k order: nibbles interleaved into k order, then the low and high bytes of
-// their bf16 values looked up and interleaved.
-FTMOE_BF16_FN inline void e2m1x16_bf16(const uint8_t *codes, uint8x16_t tlo, uint8x16_t thi, bfloat16x8_t &w0,
-                                       bfloat16x8_t &w1) {
-    const uint8x8_t c = vld1_u8(codes);
-    const uint8x8_t ev = vand_u8(c, vdup_n_u8(15)), od = vshr_n_u8(c, 4);
-    const uint8x16_t idx = vcombine_u8(vzip1_u8(ev, od), vzip2_u8(ev, od));
-    const uint8x16_t lo = vqtbl1q_u8(tlo, idx), hi = vqtbl1q_u8(thi, idx);
-    w0 = vreinterpretq_bf16_u8(vzip1q_u8(lo, hi));
-    w1 = vreinterpretq_bf16_u8(vzip2q_u8(lo, hi));
+// nvfp4 rows run against activation vectors in the even/odd order of each 16-element scale block
+// (its eight even elements, then its eight odd ones; see eo16_permute): a block's low nibbles are
+// its even elements and its high nibbles its odd ones, so the nibbles need no interleaving, and
+// BFDOT's lane pairs meet matching elements on both sides. Sixteen code bytes (two blocks) per
+// step: nibbles split, bf16 low and high bytes looked up and interleaved.
+FTMOE_BF16_FN inline void e2m1x32_bf16_eo(const uint8_t *codes, uint8x16_t tlo, uint8x16_t thi, bfloat16x8_t (&w)[4]) {
+    const uint8x16_t c = vld1q_u8(codes);
+    const uint8x16_t ev = vandq_u8(c, vdupq_n_u8(15)), od = vshrq_n_u8(c, 4);
+    const uint8x16_t le = vqtbl1q_u8(tlo, ev), he = vqtbl1q_u8(thi, ev);
+    const uint8x16_t lo = vqtbl1q_u8(tlo, od), ho = vqtbl1q_u8(thi, od);
+    w[0] = vreinterpretq_bf16_u8(vzip1q_u8(le, he));  // first block, even elements
+    w[1] = vreinterpretq_bf16_u8(vzip1q_u8(lo, ho));  // first block, odd elements
+    w[2] = vreinterpretq_bf16_u8(vzip2q_u8(le, he));  // second block, even elements
+    w[3] = vreinterpretq_bf16_u8(vzip2q_u8(lo, ho));  // second block, odd elements
 }
 
-// nvfp4 row . (vh + vl): per 16-element block two BFDOTs into a fresh partial (and two more
-// for vl, a second chain), scaled by the block's e4m3 scale into one of four accumulators; the
-// row's f16 global last.
+// nvfp4 row . (vh + vl) over even/odd-ordered vectors (K % 32 == 0): per block two BFDOTs into a
+// fresh partial (two more for vl, a second chain), scaled by the block's e4m3 scale into one of
+// four accumulators; the row's f16 global last.
 template <bool LO>
 FTMOE_BF16_FN float row_nvfp4_bfdot(const uint8_t *codes, const uint8_t *sc, float g, const uint16_t *vh,
                                     const uint16_t *vl, int64_t K, const float *e4m3, uint8x16_t tlo,
                                     uint8x16_t thi) {
     float32x4_t acc[4] = {vdupq_n_f32(0.f), vdupq_n_f32(0.f), vdupq_n_f32(0.f), vdupq_n_f32(0.f)};
-    const int64_t nb = K / 16;
-    for (int64_t blk = 0; blk < nb; blk++) {
-        bfloat16x8_t w0, w1;
-        e2m1x16_bf16(codes + blk * 8, tlo, thi, w0, w1);
-        const float s = e4m3[sc[blk]];
-        float32x4_t p = vbfdotq_f32(vdupq_n_f32(0.f), w0, ld_bf16(vh + blk * 16));
-        p = vbfdotq_f32(p, w1, ld_bf16(vh + blk * 16 + 8));
-        acc[blk & 1] = vfmaq_n_f32(acc[blk & 1], p, s);
+    for (int64_t b2 = 0; b2 < K / 32; b2++) {
+        bfloat16x8_t w[4];
+        e2m1x32_bf16_eo(codes + b2 * 16, tlo, thi, w);
+        const uint16_t *v = vh + b2 * 32;
+        const float s0 = e4m3[sc[2 * b2]], s1 = e4m3[sc[2 * b2 + 1]];
+        const float32x4_t p0 = vbfdotq_f32(vbfdotq_f32(vdupq_n_f32(0.f), w[0], ld_bf16(v)), w[1], ld_bf16(v + 8));
+        const float32x4_t p1 =
+            vbfdotq_f32(vbfdotq_f32(vdupq_n_f32(0.f), w[2], ld_bf16(v + 16)), w[3], ld_bf16(v + 24));
+        acc[0] = vfmaq_n_f32(acc[0], p0, s0);
+        acc[1] = vfmaq_n_f32(acc[1], p1, s1);
         if (LO) {
-            float32x4_t q = vbfdotq_f32(vdupq_n_f32(0.f), w0, ld_bf16(vl + blk * 16));
-            q = vbfdotq_f32(q, w1, ld_bf16(vl + blk * 16 + 8));
-            acc[2 + (blk & 1)] = vfmaq_n_f32(acc[2 + (blk & 1)], q, s);
+            const uint16_t *u = vl + b2 * 32;
+            const float32x4_t q0 =
+                vbfdotq_f32(vbfdotq_f32(vdupq_n_f32(0.f), w[0], ld_bf16(u)), w[1], ld_bf16(u + 8));
+            const float32x4_t q1 =
+                vbfdotq_f32(vbfdotq_f32(vdupq_n_f32(0.f), w[2], ld_bf16(u + 16)), w[3], ld_bf16(u + 24));
+            acc[2] = vfmaq_n_f32(acc[2], q0, s0);
+            acc[3] = vfmaq_n_f32(acc[3], q1, s1);
         }
     }
     return vaddvq_f32(vaddq_f32(vaddq_f32(acc[0], acc[1]), vaddq_f32(acc[2], acc[3]))) * g;
 }
 
-// The gate and the up row of one nvfp4 neuron against the same bf16 activations (each
-// activation vector loaded once for both rows): out[0] = gate . v, out[1] = up . v.
+// The gate and the up row of one nvfp4 neuron against the same even/odd-ordered bf16
+// activations (each activation vector loaded once for both rows): out = {gate . v, up . v}.
 FTMOE_BF16_FN void row2_nvfp4_bfdot(const uint8_t *cg, const uint8_t *sg, float gg, const uint8_t *cu,
                                     const uint8_t *su, float gu, const uint16_t *vh, int64_t K, const float *e4m3,
                                     uint8x16_t tlo, uint8x16_t thi, float (&out)[2]) {
     float32x4_t ag[2] = {vdupq_n_f32(0.f), vdupq_n_f32(0.f)}, au[2] = {vdupq_n_f32(0.f), vdupq_n_f32(0.f)};
-    const int64_t nb = K / 16;
-    for (int64_t blk = 0; blk < nb; blk++) {
-        bfloat16x8_t g0, g1, u0, u1;
-        e2m1x16_bf16(cg + blk * 8, tlo, thi, g0, g1);
-        e2m1x16_bf16(cu + blk * 8, tlo, thi, u0, u1);
-        const bfloat16x8_t x0 = ld_bf16(vh + blk * 16), x1 = ld_bf16(vh + blk * 16 + 8);
-        const float32x4_t pg = vbfdotq_f32(vbfdotq_f32(vdupq_n_f32(0.f), g0, x0), g1, x1);
-        const float32x4_t pu = vbfdotq_f32(vbfdotq_f32(vdupq_n_f32(0.f), u0, x0), u1, x1);
-        ag[blk & 1] = vfmaq_n_f32(ag[blk & 1], pg, e4m3[sg[blk]]);
-        au[blk & 1] = vfmaq_n_f32(au[blk & 1], pu, e4m3[su[blk]]);
+    for (int64_t b2 = 0; b2 < K / 32; b2++) {
+        bfloat16x8_t wg[4], wu[4];
+        e2m1x32_bf16_eo(cg + b2 * 16, tlo, thi, wg);
+        e2m1x32_bf16_eo(cu + b2 * 16, tlo, thi, wu);
+        const uint16_t *v = vh + b2 * 32;
+        const bfloat16x8_t x0 = ld_bf16(v), x1 = ld_bf16(v + 8), x2 = ld_bf16(v + 16), x3 = ld_bf16(v + 24);
+        const float32x4_t pg0 = vbfdotq_f32(vbfdotq_f32(vdupq_n_f32(0.f), wg[0], x0), wg[1], x1);
+        const float32x4_t pg1 = vbfdotq_f32(vbfdotq_f32(vdupq_n_f32(0.f), wg[2], x2), wg[3], x3);
+        const float32x4_t pu0 = vbfdotq_f32(vbfdotq_f32(vdupq_n_f32(0.f), wu[0], x0), wu[1], x1);
+        const float32x4_t pu1 = vbfdotq_f32(vbfdotq_f32(vdupq_n_f32(0.f), wu[2], x2), wu[3], x3);
+        ag[0] = vfmaq_n_f32(ag[0], pg0, e4m3[sg[2 * b2]]);
+        ag[1] = vfmaq_n_f32(ag[1], pg1, e4m3[sg[2 * b2 + 1]]);
+        au[0] = vfmaq_n_f32(au[0], pu0, e4m3[su[2 * b2]]);
+        au[1] = vfmaq_n_f32(au[1], pu1, e4m3[su[2 * b2 + 1]]);
     }
     out[0] = vaddvq_f32(vaddq_f32(ag[0], ag[1])) * gg;
     out[1] = vaddvq_f32(vaddq_f32(au[0], au[1])) * gu;
@@ -401,6 +416,16 @@ FTMOE_BF16_FN void cols_mx_bfdot(const uint8_t *const *b, int which, int64_t N, 
 #endif
 
 #if FTMOE_CPU_NEON
+// out = v in the even/odd order of each 16-element block (n % 16 == 0): out[16b + i] =
+// v[16b + 2i], out[16b + 8 + i] = v[16b + 2i + 1], i < 8.
+void eo16_permute(const uint16_t *v, int64_t n, uint16_t *out) {
+    for (int64_t b = 0; b < n; b += 16)
+        for (int i = 0; i < 8; i++) {
+            out[b + i] = v[b + 2 * i];
+            out[b + 8 + i] = v[b + 2 * i + 1];
+        }
+}
+
 // fp32 -> bf16 bits, rounded to nearest even (finite inputs).
 uint16_t f_to_bf16(float f) {
     uint32_t u;
@@ -519,6 +544,11 @@ void expert_ffn_bfdot(int format, int64_t H, int64_t I, int topk, const std::vec
                       std::vector<float> &os, int threads) {
     const int64_t np = static_cast<int64_t>(pairs.size());
     auto xrow = [&](int64_t i) { return h_x + (int64_t)(pairs[static_cast<size_t>(i)] / topk) * H; };
+    // nvfp4 rows read even/odd-ordered activation and h vectors (see row_nvfp4_bfdot)
+    const bool eo = format == FTMOE_FMT_NVFP4;
+    std::vector<uint16_t> xp(eo ? static_cast<size_t>(np * H) : 0);
+    for (int64_t i = 0; i < np && eo; i++) eo16_permute(xrow(i), H, &xp[static_cast<size_t>(i * H)]);
+    auto xv = [&](int64_t i) { return eo ? &xp[static_cast<size_t>(i * H)] : xrow(i); };
     const int64_t chunk = 64;
     if (format == FTMOE_FMT_MXFP4) {
         const int64_t nch = (I + chunk - 1) / chunk;
@@ -540,13 +570,13 @@ void expert_ffn_bfdot(int format, int64_t H, int64_t I, int topk, const std::vec
                 const uint8_t *const *bk = &eb[static_cast<size_t>(i * nb)];
                 float gu[2];
                 if (format == FTMOE_FMT_BF16) {
-                    gu[0] = row_dot_bfdot<false>(format, bk, 0, n, H, xrow(i), nullptr);
-                    gu[1] = row_dot_bfdot<false>(format, bk, 0, I + n, H, xrow(i), nullptr);
+                    gu[0] = row_dot_bfdot<false>(format, bk, 0, n, H, xv(i), nullptr);
+                    gu[1] = row_dot_bfdot<false>(format, bk, 0, I + n, H, xv(i), nullptr);
                 } else {
                     const uint16_t *gl = reinterpret_cast<const uint16_t *>(bk[2]);
                     row2_nvfp4_bfdot(bk[0] + n * (H / 2), bk[1] + n * (H / 16), f16_to_f(gl[n]),
                                      bk[0] + (I + n) * (H / 2), bk[1] + (I + n) * (H / 16), f16_to_f(gl[I + n]),
-                                     xrow(i), H, T.e4m3, vld1q_u8(T.e2m1_lo), vld1q_u8(T.e2m1_hi), gu);
+                                     xv(i), H, T.e4m3, vld1q_u8(T.e2m1_lo), vld1q_u8(T.e2m1_hi), gu);
                 }
                 hs[i * I + n] = silu(gu[0]) * gu[1];
             }
@@ -556,6 +586,14 @@ void expert_ffn_bfdot(int format, int64_t H, int64_t I, int topk, const std::vec
     for (size_t k = 0; k < hh.size(); k++) {
         hh[k] = f_to_bf16(hs[k]);
         hl[k] = f_to_bf16(hs[k] - bf16_to_f(hh[k]));
+    }
+    if (eo) {
+        std::vector<uint16_t> t(static_cast<size_t>(I));
+        for (int64_t i = 0; i < np; i++)
+            for (std::vector<uint16_t> *v : {&hh, &hl}) {
+                eo16_permute(v->data() + i * I, I, t.data());
+                std::copy(t.begin(), t.end(), v->begin() + i * I);
+            }
     }
     if (format == FTMOE_FMT_MXFP4) {
         const int64_t nchd = (H + chunk - 1) / chunk;
