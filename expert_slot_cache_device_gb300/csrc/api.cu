@@ -122,7 +122,8 @@ Layout make_layout(int fmt, int E, int L, int S, int H, int I, int max_pairs) {
         l.upairs = off; off += align256(P * 4);
         l.h = off; off += align256(P * (size_t)I * 4);
         l.o = off; off += align256(P * (size_t)H * 4);
-        l.x16 = off; off += align256(P * (size_t)H * 2);
+        // f16 activations [P, H], or for Q4_0 per token int16 [H] + fp32 block scales [H / 32]
+        l.x16 = off; off += align256(P * ((size_t)H * 2 + (size_t)H / 8));
         l.xexp = off; off += align256(P * 4);
         l.hmax = off; off += align256(P * 4);
         l.upoff = off; off += align256(P * 4);

@@ -146,6 +146,28 @@ __global__ void __launch_bounds__(1024) ffn_route_kernel(FfnParams p) {
     // launched as a programmatic dependent of the previous kernel (the copy of the missed
     // experts, whose bytes the FFN reads): wait for it before reading slots or x
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (blockIdx.x > 0 && p.x16_swz == 2) {
+        // Q4_0: token t as int16 with one scale per 32-element block (the Q4_0 block), so the
+        // gate_up kernel multiplies integer nibbles by integer activations (dp2a): warp w takes
+        // block k / 32, d = max |x| over the block / 32767, x_int = rint(x / d); stored after
+        // the int16 row is d / 16 (the weights enter as 16 (q - 8)).
+        const int t = blockIdx.x - 1;
+        const uint16_t *xr = p.x + (int64_t)t * p.H;
+        unsigned char *row = reinterpret_cast<unsigned char *>(p.s.x16) + (int64_t)t * (2 * (int64_t)p.H + p.H / 8);
+        int16_t *xi = reinterpret_cast<int16_t *>(row);
+        float *xs = reinterpret_cast<float *>(row + 2 * (int64_t)p.H);
+        for (int k = tid; k < p.H; k += nt) {  // nt is a multiple of 32 and H of 256: whole blocks per warp
+            const float v = __uint_as_float((uint32_t)xr[k] << 16);
+            const float m = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v))));
+            const float d = m > 0.f && m < INFINITY ? m * (1.f / 32767.f) : 0.f;
+            int q = d > 0.f ? __float2int_rn(v / d) : 0;
+            q = q > 32767 ? 32767 : (q < -32767 ? -32767 : q);
+            xi[swz_q4x16(k)] = (int16_t)q;
+            if ((tid & 31) == 0) xs[k >> 5] = d * 0.0625f;
+        }
+        if (tid == 0) p.s.xexp[t] = 0;
+        return;
+    }
     if (blockIdx.x > 0) {
         const int t = blockIdx.x - 1;
         const uint16_t *xr = p.x + (int64_t)t * p.H;

@@ -157,32 +157,60 @@ __device__ __forceinline__ void gu_consume(const FfnParams &p, const TmaCfg &c, 
                 }
             }
         } else if (FMT == FTMOE_FMT_Q4_0) {
-            // lane step = one 32-element Q4_0 block of the gate and of the up row: nibbles ->
-            // exact f16x2 (nibble - 8), 32 exact f16 products summed in two f16 halves of
-            // sixteen, the block's binary16 scale applied in fp32. Activations are staged in
-            // the swz_q4x16 layout: unit u of this lane's block sits at u ^ ((b >> 1) & 3).
+            // lane step = one 32-element Q4_0 block of the gate and of the up row, in integers:
+            // w ^ 0x88888888 turns every nibble q into the 4-bit two's complement of q - 8, and
+            // masked into the top half of a byte it reads as the int8 16 (q - 8); dp2a multiplies
+            // two of them by two int16 activations (the token's block as int16 with one scale,
+            // staged after the int16 row) and every block sums exactly in int32. The block's sum
+            // is then scaled by the f16 weight scale times the activation scale (which carries
+            // the 1/16). The int16 activations are staged in the swz_q4x16 layout: unit u of this
+            // lane's block sits at u ^ ((b >> 1) & 3).
             const unsigned char *rg = st + j * wr, *ru = st + (R + j) * wr;
             const int nb = H >> 5;
             const int rot = (lane >> 1) & 3;
             for (int b = lane; b < nb; b += 32) {
-                uint32_t dg, du, qg[4], qu[4], fa[16], fb[16];
+                uint32_t dg, du, qg[4], qu[4];
                 q4_block(rg, b, dg, qg);
                 q4_block(ru, b, du, qu);
-                q4_decode(qg, fa);
-                q4_decode(qu, fb);
+                uint32_t lg[4], hg[4], lu[4], hu[4];  // int8 16 (q - 8): elements 4i.. and 16 + 4i..
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    const uint32_t a = qg[i] ^ 0x88888888u, e = qu[i] ^ 0x88888888u;
+                    lg[i] = (a << 4) & 0xF0F0F0F0u;
+                    hg[i] = a & 0xF0F0F0F0u;
+                    lu[i] = (e << 4) & 0xF0F0F0F0u;
+                    hu[i] = e & 0xF0F0F0F0u;
+                }
+                const float fdg = __half2float(__ushort_as_half((unsigned short)dg));
+                const float fdu = __half2float(__ushort_as_half((unsigned short)du));
 #pragma unroll
                 for (int t = 0; t < NT; t++) {
-                    uint32_t xw[16];
+                    const unsigned char *tok = st + c.tok_off + t * c.tok_bytes;
+                    const uint4 *xv = reinterpret_cast<const uint4 *>(tok);
+                    uint32_t xw[16];  // xw[k] = int16 elements (2k, 2k + 1) of the block
 #pragma unroll
                     for (int uu = 0; uu < 4; uu++) {
-                        const uint4 xv = xs[t * nxv + 4 * b + (uu ^ rot)];
-                        xw[4 * uu] = xv.x;
-                        xw[4 * uu + 1] = xv.y;
-                        xw[4 * uu + 2] = xv.z;
-                        xw[4 * uu + 3] = xv.w;
+                        const uint4 v = xv[4 * b + (uu ^ rot)];
+                        xw[4 * uu] = v.x;
+                        xw[4 * uu + 1] = v.y;
+                        xw[4 * uu + 2] = v.z;
+                        xw[4 * uu + 3] = v.w;
                     }
-                    g[t] = fma_h2_scale(dot32_h2(fa, xw), (uint16_t)dg, g[t]);
-                    u[t] = fma_h2_scale(dot32_h2(fb, xw), (uint16_t)du, u[t]);
+                    const float xsc = reinterpret_cast<const float *>(tok + 2 * H)[b];
+                    int g0 = 0, g1 = 0, u0 = 0, u1 = 0;
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        g0 = __dp2a_lo((int)xw[2 * i], (int)lg[i], g0);
+                        g0 = __dp2a_hi((int)xw[2 * i + 1], (int)lg[i], g0);
+                        g1 = __dp2a_lo((int)xw[8 + 2 * i], (int)hg[i], g1);
+                        g1 = __dp2a_hi((int)xw[9 + 2 * i], (int)hg[i], g1);
+                        u0 = __dp2a_lo((int)xw[2 * i], (int)lu[i], u0);
+                        u0 = __dp2a_hi((int)xw[2 * i + 1], (int)lu[i], u0);
+                        u1 = __dp2a_lo((int)xw[8 + 2 * i], (int)hu[i], u1);
+                        u1 = __dp2a_hi((int)xw[9 + 2 * i], (int)hu[i], u1);
+                    }
+                    g[t] = fmaf((float)(g0 + g1), fdg * xsc, g[t]);
+                    u[t] = fmaf((float)(u0 + u1), fdu * xsc, u[t]);
                 }
             }
         } else {
@@ -481,7 +509,10 @@ __global__ void __launch_bounds__(kTmaThreads<FMT, PHASE>, 1) ffn_rows_tma_kerne
                     const int q = hh.pairs[i];
                     const uint16_t *xsrc = kF16Act<FMT> ? p.s.x16 : p.x;
                     const void *src = PHASE == kGateUp
-                                          ? static_cast<const void *>(xsrc + (int64_t)(q / p.topk) * H)
+                                          ? (FMT == FTMOE_FMT_Q4_0  // prepared rows of tok_bytes each
+                                                 ? static_cast<const void *>(reinterpret_cast<const unsigned char *>(p.s.x16) +
+                                                                             (int64_t)(q / p.topk) * c.tok_bytes)
+                                                 : static_cast<const void *>(xsrc + (int64_t)(q / p.topk) * H))
                                           : static_cast<const void *>(p.s.h + (int64_t)q * I);
                     bulk1d(st + c.tok_off + i * c.tok_bytes, src, (uint32_t)c.tok_bytes, &full[s]);
                 }
@@ -547,7 +578,8 @@ template <int FMT, int PHASE>
 bool make_cfg(const FfnParams &p, TmaCfg &c) {
     const int H = p.H, I = p.I;
     const int nout = PHASE == kGateUp ? I : H;
-    c.tok_bytes = PHASE == kGateUp ? 2 * H : 4 * I;
+    // gate_up token: f16 activations (2H bytes); Q4_0: int16 activations and fp32 block scales
+    c.tok_bytes = PHASE == kGateUp ? (FMT == FTMOE_FMT_Q4_0 ? 2 * H + H / 8 : 2 * H) : 4 * I;
     const int rmax = PHASE == kGateUp ? 16 : 64;
     // Prefer enough rows per item to keep all consumer warps busy (gate_up: one neuron per
     // warp; down: four rows per warp), then as many token slots as fit.

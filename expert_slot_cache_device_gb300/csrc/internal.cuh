@@ -84,7 +84,8 @@ struct FfnScratch {
     int32_t *upairs;    // [P] pair indices t * topk + j grouped by slot
     float *h;           // [P, I] SiLU(gate) * up per pair
     float *o;           // [P, H] down output per pair
-    uint16_t *x16;      // [bs, H] activations as f16, scaled by 2^-xexp[t] (nullptr: not prepared)
+    uint16_t *x16;      // [bs, H] activations as f16, scaled by 2^-xexp[t] (nullptr: not prepared);
+                        // Q4_0: per token 2H + H/8 bytes, int16 [H] then fp32 [H/32] block scales / 16
     int32_t *xexp;      // [bs] per-token power-of-two exponent of x16
     uint32_t *hmax;     // [P] bit pattern of max |h| per pair (order-independent atomicMax)
     int32_t *upoff;     // [P] first pass (group of pass_tokens pairs) of each distinct slot
@@ -113,7 +114,7 @@ struct FfnParams {
     int32_t fmt, H, I, S, bs, topk, P;
     int32_t E;         // experts per layer (0: unknown; used only to choose kernels)
     int32_t x16_emax;  // f16 activation copy keeps max |x| < 2^x16_emax
-    int32_t x16_swz;   // f16 activation copy layout: 0 plain, 1 swz_x16 (nvfp4), 2 swz_q4x16 (Q4_0)
+    int32_t x16_swz;   // activation copy layout: 0 plain, 1 swz_x16 (nvfp4), 2 int16 in swz_q4x16 (Q4_0)
     int32_t pass_tokens;  // tokens per pass of the pipelined kernels (kPassTokens / kMxPassTokens)
     // test settings (ftmoe_set_debug): limit of the CUDA-core pipeline's bounded waits (0: the
     // default), and 1 to leave CTA 0's first gate_up stage unfilled so that a wait runs out
