@@ -368,18 +368,18 @@ FTMOE_BF16_FN inline void mx_row16_bfdot(const uint8_t *codes, const uint16_t *v
     }
 }
 
-// Columns [n0, n1) of a transposed mxfp4 matrix against vh + vl (see cols_dot): per k-pair row
-// and 16 columns, the 16 code bytes become four bf16x8 vectors (4 columns x (even k, odd k))
-// and meet the k pair of v broadcast to every lane.
+// Columns [n0, n1) of a transposed mxfp4 matrix over the scale blocks [blk0, blk1) of the
+// reduction axis, against vh + vl (see cols_dot): per k-pair row and 16 columns, the 16 code
+// bytes become four bf16x8 vectors (4 columns x (even k, odd k)) and meet the k pair of v
+// broadcast to every lane. out[n - n0] = the range's partial sum (no bias).
 template <bool LO>
-FTMOE_BF16_FN void cols_mx_bfdot(const uint8_t *const *b, int which, int64_t N, int64_t K, const uint16_t *vh,
-                                 const uint16_t *vl, int64_t n0, int64_t n1, float *out) {
+FTMOE_BF16_FN void cols_mx_bfdot(const uint8_t *const *b, int which, int64_t N, int64_t blk0, int64_t blk1,
+                                 const uint16_t *vh, const uint16_t *vl, int64_t n0, int64_t n1, float *out) {
     const Tables &T = tables();
     const uint8x16_t tlo = vld1q_u8(T.e2m1_lo), thi = vld1q_u8(T.e2m1_hi);
     const uint8_t *blocks = b[3 * which], *scales = b[3 * which + 1];
-    const uint16_t *bias = reinterpret_cast<const uint16_t *>(b[3 * which + 2]);
     for (int64_t n = n0; n < n1; n++) out[n - n0] = 0.f;
-    for (int64_t blk = 0; blk < K / 32; blk++) {
+    for (int64_t blk = blk0; blk < blk1; blk++) {
         const uint8_t *srow = scales + blk * N;
         int64_t n = n0;
         for (; n + 16 <= n1; n += 16) {
@@ -411,7 +411,6 @@ FTMOE_BF16_FN void cols_mx_bfdot(const uint8_t *const *b, int which, int64_t N, 
             out[n - n0] += part * T.e8m0[srow[n]];
         }
     }
-    for (int64_t n = n0; n < n1; n++) out[n - n0] += bf16_to_f(bias[n]);
 }
 #endif
 
@@ -549,19 +548,43 @@ void expert_ffn_bfdot(int format, int64_t H, int64_t I, int topk, const std::vec
     std::vector<uint16_t> xp(eo ? static_cast<size_t>(np * H) : 0);
     for (int64_t i = 0; i < np && eo; i++) eo16_permute(xrow(i), H, &xp[static_cast<size_t>(i * H)]);
     auto xv = [&](int64_t i) { return eo ? &xp[static_cast<size_t>(i * H)] : xrow(i); };
-    const int64_t chunk = 64;
-    if (format == FTMOE_FMT_MXFP4) {
-        const int64_t nch = (I + chunk - 1) / chunk;
-        parallel_for(np * nch, threads, [&](int64_t a, int64_t b) {
-            float g[chunk], u[chunk];
+    // mxfp4 (transposed [K/2, N] codes): a work item is one pair's range of scale blocks over all
+    // N columns, so a worker reads whole contiguous rows (16 rows x N bytes per block) instead of
+    // one line per row at a stride of N bytes; the ranges' partial sums are added in range order.
+    auto mx_matrix = [&](int which, int64_t N, int64_t K, const uint16_t *const *vh, const uint16_t *const *vl,
+                         float *outp) {
+        const int64_t KB = K / 32;
+        const int64_t R = std::max<int64_t>(1, std::min<int64_t>(KB, (2 * threads + np - 1) / np));
+        std::vector<float> part(static_cast<size_t>(np * R * N));
+        parallel_for(np * R, threads, [&](int64_t a, int64_t b) {
             for (int64_t w = a; w < b; w++) {
-                const int64_t i = w / nch, c0 = (w % nch) * chunk, c1 = std::min<int64_t>(I, c0 + chunk);
+                const int64_t i = w / R, r = w % R;
                 const uint8_t *const *bk = &eb[static_cast<size_t>(i * nb)];
-                cols_mx_bfdot<false>(bk, 0, 2 * I, H, xrow(i), nullptr, c0, c1, g);
-                cols_mx_bfdot<false>(bk, 0, 2 * I, H, xrow(i), nullptr, I + c0, I + c1, u);
-                for (int64_t n = c0; n < c1; n++) hs[i * I + n] = silu(g[n - c0]) * u[n - c0];
+                float *dst = &part[static_cast<size_t>(w * N)];
+                if (vl)
+                    cols_mx_bfdot<true>(bk, which, N, KB * r / R, KB * (r + 1) / R, vh[i], vl[i], 0, N, dst);
+                else
+                    cols_mx_bfdot<false>(bk, which, N, KB * r / R, KB * (r + 1) / R, vh[i], nullptr, 0, N, dst);
             }
         });
+        parallel_for(np, threads, [&](int64_t a, int64_t b) {
+            for (int64_t i = a; i < b; i++) {
+                const uint16_t *bias = reinterpret_cast<const uint16_t *>(eb[static_cast<size_t>(i * nb + 3 * which + 2)]);
+                for (int64_t n = 0; n < N; n++) {
+                    float v = 0.f;
+                    for (int64_t r = 0; r < R; r++) v += part[static_cast<size_t>((i * R + r) * N + n)];
+                    outp[i * N + n] = v + bf16_to_f(bias[n]);
+                }
+            }
+        });
+    };
+    if (format == FTMOE_FMT_MXFP4) {
+        std::vector<const uint16_t *> xr(static_cast<size_t>(np));
+        for (int64_t i = 0; i < np; i++) xr[static_cast<size_t>(i)] = xrow(i);
+        std::vector<float> gu(static_cast<size_t>(np * 2 * I));
+        mx_matrix(0, 2 * I, H, xr.data(), nullptr, gu.data());
+        for (int64_t i = 0; i < np; i++)
+            for (int64_t n = 0; n < I; n++) hs[i * I + n] = silu(gu[i * 2 * I + n]) * gu[i * 2 * I + I + n];
     } else {
         const Tables &T = tables();
         parallel_for(np * I, threads, [&](int64_t a, int64_t b) {
@@ -596,14 +619,12 @@ void expert_ffn_bfdot(int format, int64_t H, int64_t I, int topk, const std::vec
             }
     }
     if (format == FTMOE_FMT_MXFP4) {
-        const int64_t nchd = (H + chunk - 1) / chunk;
-        parallel_for(np * nchd, threads, [&](int64_t a, int64_t b) {
-            for (int64_t w = a; w < b; w++) {
-                const int64_t i = w / nchd, c0 = (w % nchd) * chunk, c1 = std::min<int64_t>(H, c0 + chunk);
-                cols_mx_bfdot<true>(&eb[static_cast<size_t>(i * nb)], 1, H, I, &hh[i * I], &hl[i * I], c0, c1,
-                                    &os[i * H + c0]);
-            }
-        });
+        std::vector<const uint16_t *> hr(static_cast<size_t>(np)), lr(static_cast<size_t>(np));
+        for (int64_t i = 0; i < np; i++) {
+            hr[static_cast<size_t>(i)] = &hh[static_cast<size_t>(i * I)];
+            lr[static_cast<size_t>(i)] = &hl[static_cast<size_t>(i * I)];
+        }
+        mx_matrix(1, H, I, hr.data(), lr.data(), os.data());
     } else {
         parallel_for(np * H, threads, [&](int64_t a, int64_t b) {
             for (int64_t w = a; w < b; w++) {
