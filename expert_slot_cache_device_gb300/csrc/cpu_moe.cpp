@@ -27,6 +27,8 @@
 #include <thread>
 #include <vector>
 
+#include <unistd.h>
+
 #include "ftmoe.h"
 
 // The Grace host (aarch64) runs the executor's inner loops on NEON (ARMv8-A base SIMD: 16-bit
@@ -101,11 +103,21 @@ float silu(float z) { return z / (1.0f + std::exp(-z)); }
 // Persistent workers of parallel_for: started on first use (and grown on demand), then parked
 // on a condition variable between calls, so a call pays a wake-up instead of a thread start
 // per worker. One call runs at a time (calls from several host threads queue on the mutex).
+// The pool belongs to the process that made it: a forked child has none of its threads, so it
+// leaves the inherited pool untouched (never destroyed, never joined) and makes its own. Pools
+// are never destroyed; their parked workers end with the process.
 class WorkerPool {
   public:
     static WorkerPool &get() {
-        static WorkerPool pool;
-        return pool;
+        static std::mutex mu;
+        static WorkerPool *pool = nullptr;
+        static pid_t owner = 0;
+        std::lock_guard<std::mutex> lk(mu);
+        if (!pool || owner != getpid()) {
+            pool = new WorkerPool();
+            owner = getpid();
+        }
+        return *pool;
     }
     // fn(a, b) over [0, n) split into nt contiguous ranges; range 0 runs on the calling thread.
     void run(int64_t n, int nt, const std::function<void(int64_t, int64_t)> &fn) {
@@ -128,15 +140,6 @@ class WorkerPool {
         done_cv_.wait(lk, [this] { return pending_ == 0; });
         fn_ = nullptr;
     }
-    ~WorkerPool() {
-        {
-            std::lock_guard<std::mutex> lk(mu_);
-            stop_ = true;
-        }
-        cv_.notify_all();
-        for (auto &t : workers_) t.join();
-    }
-
   private:
     void loop(int id) {
         uint64_t seen = 0;
@@ -145,8 +148,7 @@ class WorkerPool {
             int64_t a, b;
             {
                 std::unique_lock<std::mutex> lk(mu_);
-                cv_.wait(lk, [&] { return stop_ || gen_ != seen; });
-                if (stop_) return;
+                cv_.wait(lk, [&] { return gen_ != seen; });
                 seen = gen_;
                 if (id >= nt_) continue;  // not part of this call
                 fn = fn_;
@@ -165,7 +167,6 @@ class WorkerPool {
     int64_t n_ = 0;
     int nt_ = 0, pending_ = 0;
     uint64_t gen_ = 0;
-    bool stop_ = false;
 };
 
 template <typename F>

@@ -123,3 +123,49 @@ def test_cpu_executor_concurrent_calls(lib):
             t.join()
         for y, y0 in zip(outs, alone):
             assert np.array_equal(y, y0)
+
+
+@pytest.mark.filterwarnings("ignore::DeprecationWarning")  # Python warns about fork in a threaded process
+def test_cpu_executor_after_fork(lib):
+    """A process forked after the executor has run (its worker pool started) runs the executor
+    itself with a pool of its own and gets the parent's result."""
+    import os
+
+    fmt, geo = CASES[0]
+    cfg = wl.scaled(wl.CONFIGS["c2"], topk=2, L=2, S=4, **geo)
+    banks = wl.make_banks(cfg)
+    rng = np.random.default_rng(5)
+    ids = np.stack([rng.choice(cfg.E, cfg.topk, replace=False) for _ in range(3)]).astype(np.int32)
+    slots = np.full(ids.shape, -1, np.int32)
+    w = rng.random(ids.shape).astype(np.float32)
+    x = wl.f32_to_bf16_bits(rng.standard_normal((3, cfg.H)).astype(np.float32))
+
+    def run():
+        y = np.empty((3, cfg.H), np.float32)
+        F.ftmoe_cpu_expert_ffn(F.FMT_BF16, cfg.H, cfg.I, 3, cfg.topk, ids.ctypes.data, slots.ctypes.data,
+                               [b.ctypes.data for b in banks], [b.shape[1] for b in banks], x.ctypes.data,
+                               w.ctypes.data, y.ctypes.data, 4)
+        return y
+
+    y0 = run()  # starts the parent's workers
+    pid = os.fork()
+    if pid == 0:  # child: exit status 0 only if the call returns the parent's bits
+        code = 1
+        try:
+            code = 0 if np.array_equal(run(), y0) else 2
+        finally:
+            os._exit(code)
+    import time
+
+    deadline = time.monotonic() + 60
+    while True:
+        done, status = os.waitpid(pid, os.WNOHANG)
+        if done:
+            break
+        if time.monotonic() > deadline:
+            os.kill(pid, 9)
+            os.waitpid(pid, 0)
+            raise AssertionError("the forked executor call did not return")
+        time.sleep(0.05)
+    assert os.WIFEXITED(status) and os.WEXITSTATUS(status) == 0
+    assert np.array_equal(run(), y0)
